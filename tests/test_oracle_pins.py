@@ -1,0 +1,370 @@
+"""Pins of the float64 oracle to things other than itself (CPU only).
+
+Each test checks the oracle against a closed form, a hand-worked instance, an invariant, a library routine or a
+brute-force evaluation, chosen so that a plausible slip (a dropped term, a swapped gate/up half, a transposed
+matrix, a wrong tie-break or sort key, double rounding) fails at least one of them.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax
+
+from conftest import bf16_bits, read_fixture
+
+
+# ---------------------------------------------------------------- bf16 rounding (every BF16 store of the layer)
+
+def _bf16_neighbours(b):
+    """(value, next value up) for a positive bf16 bit pattern, as float64."""
+    lo = np.array([b], dtype=np.uint32) << 16
+    hi = np.array([b + 1], dtype=np.uint32) << 16
+    return float(lo.view(np.float32)[0]), float(hi.view(np.float32)[0])
+
+
+def test_bf16_rounding_midpoints_closed_form(oracle_lib):
+    o = oracle_lib
+    rng = np.random.default_rng(1)
+    for b in list(rng.integers(0x0080, 0x7F00, size=400)) + [0x3F80, 0x3F81, 0x4000, 0x0080]:
+        b = int(b)
+        lo, hi = _bf16_neighbours(b)
+        mid = (lo + hi) / 2  # exact in double
+        even = b if b % 2 == 0 else b + 1
+        tiny = (hi - lo) * 2.0 ** -30
+        got = o.bf16_from_double([mid, mid + tiny, mid - tiny, lo, -mid, -(mid + tiny)])
+        assert got[0] == even, "exact midpoint must round to the even neighbour"
+        assert got[1] == b + 1
+        assert got[2] == b
+        assert got[3] == b
+        assert got[4] == (even | 0x8000)
+        assert got[5] == ((b + 1) | 0x8000)
+
+
+def test_bf16_rounding_single_step_not_via_float(oracle_lib):
+    # A double just above a bf16 midpoint whose float rounding lands exactly on the midpoint: rounding through
+    # float (twice) would give the even neighbour; one correct rounding gives the upper one.
+    lo, hi = _bf16_neighbours(0x3F80)  # 1.0 and 1.0078125
+    mid = (lo + hi) / 2
+    v = mid + 2.0 ** -40  # rounds to `mid` in float32
+    assert float(np.float32(v)) == mid
+    assert oracle_lib.bf16_from_double([v])[0] == 0x3F81
+
+
+def test_bf16_rounding_matches_library_on_float32_values(oracle_lib):
+    rng = np.random.default_rng(2)
+    v = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    lib = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle_lib.bf16_from_double(v.astype(np.float64))
+    np.testing.assert_array_equal(got, lib)
+
+
+def test_bf16_special_values(oracle_lib):
+    got = oracle_lib.bf16_from_double([0.0, -0.0, np.inf, -np.inf, 3.5e38, 2.0 ** -133, 2.0 ** -134 * 3])
+    assert list(got[:5]) == [0x0000, 0x8000, 0x7F80, 0xFF80, 0x7F80]
+    assert got[5] == 0x0001            # smallest bf16 subnormal
+    assert got[6] == 0x0002            # 1.5 * 2^-133 is a tie between 1 and 2 quanta: even -> 2
+    back = oracle_lib.bf16_to_double(np.array([0x3F80, 0xC040, 0x0001], dtype=np.uint16))
+    assert list(back) == [1.0, -3.0, 2.0 ** -133]
+
+
+# ---------------------------------------------------------------- router logits
+
+def _rand_bf16(rng, shape, std):
+    return torch.from_numpy((rng.standard_normal(shape) * std).astype(np.float32)).to(torch.bfloat16)
+
+
+def _as_f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def test_router_logits_match_library_matmul(oracle_lib):
+    rng = np.random.default_rng(3)
+    x, wr = _rand_bf16(rng, (37, 320), 1.0), _rand_bf16(rng, (24, 320), 0.05)
+    got = oracle_lib.router_logits(x, wr)
+    ref = _as_f64(x) @ _as_f64(wr).T
+    scale = np.abs(_as_f64(x)) @ np.abs(_as_f64(wr)).T
+    assert np.all(np.abs(got - ref) <= 1e-13 * scale + 1e-300)
+    # a transposed weight matrix would not even match in shape
+    assert got.shape == (37, 24)
+
+
+def test_router_logits_exact_on_integer_inputs(oracle_lib):
+    rng = np.random.default_rng(4)
+    xi = rng.integers(-8, 9, (9, 64)).astype(np.float32)
+    wi = rng.integers(-8, 9, (5, 64)).astype(np.float32)
+    got = oracle_lib.router_logits(bf16_bits(xi), bf16_bits(wi))
+    np.testing.assert_array_equal(got, xi.astype(np.int64) @ wi.astype(np.int64).T)
+
+
+# ---------------------------------------------------------------- top-k and weights
+
+def test_topk_invariants(oracle_lib):
+    rng = np.random.default_rng(5)
+    T, E, k = 300, 40, 6
+    l = rng.standard_normal((T, E))
+    ids, w = oracle_lib.topk(l, k)
+    for t in range(T):
+        assert len(set(ids[t])) == k and list(ids[t]) == sorted(ids[t])
+        sel = l[t, ids[t]]
+        rest = np.delete(l[t], ids[t])
+        assert sel.min() > rest.max()
+        np.testing.assert_allclose(w[t], softmax(sel), rtol=1e-14, atol=0)
+    assert abs(np.sum(w, axis=1) - 1).max() < 1e-15 * 8
+    counts = np.bincount(ids.ravel(), minlength=E)
+    assert counts.sum() == T * k
+
+
+def test_topk_matches_stable_library_sort(oracle_lib):
+    rng = np.random.default_rng(6)
+    # Coarse logits (multiples of 1/4) give many exact ties.
+    l = np.round(rng.standard_normal((500, 16)) * 4) / 4
+    ids, _ = oracle_lib.topk(l, 5)
+    ref = np.sort(np.argsort(-l, axis=1, kind="stable")[:, :5], axis=1)
+    np.testing.assert_array_equal(ids, ref)
+
+
+def test_topk_planted_tie_goes_to_lower_id(oracle_lib):
+    l = np.array([[0.5, 2.0, 1.0, 2.0, 1.0, 1.0]])
+    ids, w = oracle_lib.topk(l, 3)
+    assert list(ids[0]) == [1, 2, 3]
+    np.testing.assert_allclose(w[0], softmax([2.0, 1.0, 2.0]), rtol=1e-15)
+
+
+def test_topk_k_equals_E_is_full_softmax(oracle_lib):
+    rng = np.random.default_rng(7)
+    l = rng.standard_normal((20, 12)) * 3
+    ids, w = oracle_lib.topk(l, 12)
+    assert np.all(ids == np.arange(12))
+    np.testing.assert_allclose(w, softmax(l, axis=1), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- SwiGLU expert
+
+def _bf16_round_torch(v64):
+    """Library BF16 rounding (through float32). Asserts that no value sits so close to a bf16 midpoint that the
+    float32 step could change the result, so it equals one correct rounding of the float64 value."""
+    v64 = np.asarray(v64, dtype=np.float64)
+    inexact = v64[(v64 != 0) & (v64.astype(np.float32).astype(np.float64) != v64)]  # exact float32: one rounding
+    a = np.abs(inexact)
+    e = np.floor(np.log2(a)) + 1
+    frac = a / 2.0 ** (e - 8)
+    assert np.all(np.abs(frac - np.floor(frac) - 0.5) > 2.0 ** -14), "value too close to a bf16 midpoint"
+    return torch.from_numpy(v64.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def test_swiglu_matches_textbook_numpy(oracle_lib):
+    rng = np.random.default_rng(8)
+    H, I = 96, 40
+    x = _rand_bf16(rng, (H,), 1.0)
+    wgu = _rand_bf16(rng, (2 * I, H), 0.1)
+    wd = _rand_bf16(rng, (H, I), 0.1)
+    y, h_bits = oracle_lib.swiglu_ffn(x, wgu, wd)
+    X, G, U, D = _as_f64(x), _as_f64(wgu[:I]), _as_f64(wgu[I:]), _as_f64(wd)
+    g, u = G @ X, U @ X
+    h_exact = g / (1 + np.exp(-g)) * u
+    h = oracle_lib.bf16_to_double(h_bits)
+    # RNE: |round(v) - v| <= half the bf16 spacing at v (2^-8 relative at most)
+    assert np.all(np.abs(h - h_exact) <= np.abs(h_exact) * 2.0 ** -8 + 1e-300)
+    np.testing.assert_allclose(h, _bf16_round_torch(h_exact), rtol=0, atol=0)
+    np.testing.assert_allclose(y, D @ h, rtol=1e-13, atol=1e-15)
+    # swapping the gate and up halves changes the result: the pin distinguishes the two orders
+    h_swapped = u / (1 + np.exp(-u)) * g
+    assert not np.allclose(h_swapped, h_exact)
+
+
+def test_single_expert_layer_is_textbook_ffn(oracle_lib):
+    rng = np.random.default_rng(9)
+    H, I, T = 64, 32, 11
+    inp = {"x": _rand_bf16(rng, (T, H), 1.0), "w_router": _rand_bf16(rng, (1, H), 0.1),
+           "w_gu": _rand_bf16(rng, (1, 2 * I, H), 0.1), "w_down": _rand_bf16(rng, (1, H, I), 0.1)}
+    out_ref, out_bf, ids, w = oracle_lib.moe_forward(inp, top_k=1)
+    assert np.all(ids == 0) and np.all(w == 1.0)
+    X = _as_f64(inp["x"])
+    G, U, D = _as_f64(inp["w_gu"][0, :I]), _as_f64(inp["w_gu"][0, I:]), _as_f64(inp["w_down"][0])
+    g, u = X @ G.T, X @ U.T
+    h = _bf16_round_torch(g / (1 + np.exp(-g)) * u)
+    np.testing.assert_allclose(out_ref, h @ D.T, rtol=1e-12, atol=1e-14)
+
+
+# ---------------------------------------------------------------- whole layer
+
+def _dense_masked_numpy(inp, k, oracle_round):
+    """Brute force: every expert evaluated on every token; unselected experts get weight 0."""
+    X = _as_f64(inp["x"])
+    Wr = _as_f64(inp["w_router"])
+    E = Wr.shape[0]
+    I = inp["w_gu"].shape[1] // 2
+    l = X @ Wr.T
+    order = np.argsort(-l, axis=1, kind="stable")
+    mask = np.zeros_like(l, dtype=bool)
+    np.put_along_axis(mask, order[:, :k], True, axis=1)
+    lsel = np.where(mask, l, -np.inf)
+    wfull = np.exp(lsel - lsel.max(axis=1, keepdims=True))
+    wfull /= wfull.sum(axis=1, keepdims=True)
+    acc = np.zeros((X.shape[0], X.shape[1]))
+    for e in range(E):
+        G, U, D = _as_f64(inp["w_gu"][e, :I]), _as_f64(inp["w_gu"][e, I:]), _as_f64(inp["w_down"][e])
+        g, u = X @ G.T, X @ U.T
+        h = oracle_round(g / (1 + np.exp(-g)) * u)
+        acc += wfull[:, e:e + 1] * (h @ D.T)
+    if inp.get("ws_gu") is not None:
+        Is = inp["ws_gu"].shape[0] // 2
+        G, U, D = _as_f64(inp["ws_gu"][:Is]), _as_f64(inp["ws_gu"][Is:]), _as_f64(inp["ws_down"])
+        g, u = X @ G.T, X @ U.T
+        acc += oracle_round(g / (1 + np.exp(-g)) * u) @ D.T
+    return acc, np.sort(order[:, :k], axis=1), l
+
+
+def _tiny_inputs(rng, T=23, H=64, E=8, I=32, Is=16):
+    return {"x": _rand_bf16(rng, (T, H), 1.0), "w_router": _rand_bf16(rng, (E, H), 0.3),
+            "w_gu": _rand_bf16(rng, (E, 2 * I, H), 0.1), "w_down": _rand_bf16(rng, (E, H, I), 0.1),
+            "ws_gu": _rand_bf16(rng, (2 * Is, H), 0.1), "ws_down": _rand_bf16(rng, (H, Is), 0.1)}
+
+
+def test_layer_matches_dense_masked_brute_force(oracle_lib):
+    rng = np.random.default_rng(10)
+    inp = _tiny_inputs(rng)
+    k = 3
+    rnd = lambda v: oracle_lib.bf16_to_double(oracle_lib.bf16_from_double(v))
+    dense, ids_dense, l = _dense_masked_numpy(inp, k, rnd)
+    # the numpy logits differ from the oracle's sequential sums in the last bits: make sure no selection is that close
+    srt = np.sort(l, axis=1)[:, ::-1]
+    assert np.min(srt[:, k - 1] - srt[:, k]) > 1e-9
+    out_ref, out_bf, ids, w = oracle_lib.moe_forward(inp, top_k=k)
+    np.testing.assert_array_equal(ids, ids_dense)
+    np.testing.assert_allclose(out_ref, dense, rtol=1e-11, atol=1e-13)
+    np.testing.assert_array_equal(out_bf, oracle_lib.bf16_from_double(out_ref))
+
+
+def test_layer_hand_worked_example(oracle_lib):
+    fx = read_fixture("hand_worked_layer.txt")
+    H, E, I, k, Is = (int(v) for v in fx["dims"])
+    inp = {"x": bf16_bits(np.reshape(fx["x"], (2, H))),
+           "w_router": bf16_bits(np.reshape(fx["w_router"], (E, H))),
+           "w_gu": bf16_bits(np.reshape(fx["w_gu"], (E, 2 * I, H))),
+           "w_down": bf16_bits(np.reshape(fx["w_down"], (E, H, I))),
+           "ws_gu": bf16_bits(np.reshape(fx["ws_gu"], (2 * Is, H))),
+           "ws_down": bf16_bits(np.reshape(fx["ws_down"], (H, Is)))}
+    out_ref, out_bf, ids, w = oracle_lib.moe_forward(inp, top_k=k)
+    np.testing.assert_array_equal(ids.ravel(), np.array(fx["topk_id"], dtype=np.int32))
+    a, b = 1 / (1 + math.e), math.e / (1 + math.e)
+    np.testing.assert_allclose(w, [[a, b], [a, b]], rtol=1e-15)
+    for t, o, ca, cb, c0 in fx["closed"]:
+        assert out_ref[int(t), int(o)] == pytest.approx(ca * a + cb * b + c0, rel=1e-15, abs=1e-16)
+    np.testing.assert_array_equal(out_bf.ravel(), bf16_bits(fx["out_bf16"]))
+    _, h1 = oracle_lib.swiglu_ffn(inp["x"][0], inp["w_gu"][1], inp["w_down"][1])
+    assert oracle_lib.bf16_to_double(h1)[0] == fx["h_e1_t0"][0]
+
+
+def test_layer_token_subset_equals_full(oracle_lib):
+    rng = np.random.default_rng(11)
+    inp = _tiny_inputs(rng, T=17)
+    full = oracle_lib.moe_forward(inp, top_k=2)
+    idx = [16, 3, 3, 0]
+    sub = oracle_lib.moe_forward(inp, top_k=2, token_idx=idx)
+    for a, b in zip(full, sub):
+        np.testing.assert_array_equal(a[idx], b)
+
+
+def test_layer_zero_routed_down_gives_shared_only(oracle_lib):
+    rng = np.random.default_rng(12)
+    inp = _tiny_inputs(rng, T=9)
+    inp["w_down"] = torch.zeros_like(inp["w_down"])
+    out_ref, _, _, _ = oracle_lib.moe_forward(inp, top_k=2)
+    X = _as_f64(inp["x"])
+    Is = inp["ws_gu"].shape[0] // 2
+    ys = np.stack([oracle_lib.swiglu_ffn(inp["x"][t], inp["ws_gu"], inp["ws_down"])[0] for t in range(X.shape[0])])
+    np.testing.assert_array_equal(out_ref, ys)
+
+
+def test_layer_identical_experts_weights_sum_to_one(oracle_lib):
+    rng = np.random.default_rng(13)
+    inp = _tiny_inputs(rng, T=7)
+    inp["w_gu"] = inp["w_gu"][:1].repeat(inp["w_gu"].shape[0], 1, 1)
+    inp["w_down"] = inp["w_down"][:1].repeat(inp["w_down"].shape[0], 1, 1)
+    del inp["ws_gu"], inp["ws_down"]
+    out_ref, _, _, _ = oracle_lib.moe_forward(inp, top_k=4)
+    y0 = np.stack([oracle_lib.swiglu_ffn(inp["x"][t], inp["w_gu"][0], inp["w_down"][0])[0] for t in range(7)])
+    np.testing.assert_allclose(out_ref, y0, rtol=1e-14, atol=1e-16)
+
+
+# ---------------------------------------------------------------- member lists
+
+def test_permutation_hand_worked_example(oracle_lib):
+    fx = read_fixture("hand_worked_permutation.txt")
+    T, k, E, chunk = (int(v) for v in fx["dims"])
+    ids = np.array(fx["topk_id"], dtype=np.int32).reshape(T, k)
+    offs, row_token, token_row = oracle_lib.permutation(ids, E, chunk)
+    np.testing.assert_array_equal(offs.ravel(), np.array(fx["expert_offsets"], dtype=np.int32))
+    np.testing.assert_array_equal(row_token, np.array(fx["row_token"], dtype=np.int32))
+    np.testing.assert_array_equal(token_row.ravel(), np.array(fx["token_row"], dtype=np.int32))
+
+
+@pytest.mark.parametrize("chunk", [1, 7, 64, 1000])
+def test_permutation_is_stable_sort_per_chunk(oracle_lib, chunk):
+    rng = np.random.default_rng(14)
+    T, E, k = 301, 24, 4
+    ids = np.sort(np.stack([rng.choice(E, k, replace=False) for _ in range(T)]), axis=1).astype(np.int32)
+    offs, row_token, token_row = oracle_lib.permutation(ids, E, chunk)
+    for c in range((T + chunk - 1) // chunk):
+        t0, t1 = c * chunk, min((c + 1) * chunk, T)
+        flat = ids[t0:t1].ravel()
+        order = np.argsort(flat, kind="stable")
+        np.testing.assert_array_equal(row_token[t0 * k: t1 * k], t0 + order // k)
+        np.testing.assert_array_equal(offs[c], np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+        rows = token_row[t0:t1].ravel()
+        assert sorted(rows) == list(range((t1 - t0) * k))        # a bijection onto the chunk's rows
+        np.testing.assert_array_equal(np.argsort(rows), order)
+
+
+# ---------------------------------------------------------------- combine
+
+def test_combine_f32_canonical_exact_cases(oracle_lib):
+    rng = np.random.default_rng(15)
+    n, k, H = 50, 4, 33
+    y = rng.integers(-64, 65, (n * k, H)).astype(np.float32)
+    w = (2.0 ** rng.integers(-3, 2, (n, k))).astype(np.float32)
+    s = rng.integers(-64, 65, (n, H)).astype(np.float32)
+    tr = rng.permutation(n * k).reshape(n, k).astype(np.int32)
+    out = oracle_lib.combine_f32_canonical(y, w, tr, s)
+    exact = np.einsum("nk,nkh->nh", w.astype(np.float64), y[tr].astype(np.float64)) + s
+    np.testing.assert_array_equal(oracle_lib.bf16_to_double(out), _bf16_round_torch(exact))
+    ref, out64 = oracle_lib.combine_f64(y, w, tr, s)
+    np.testing.assert_array_equal(ref, exact)
+    np.testing.assert_array_equal(out64, out)
+
+
+def test_combine_f32_canonical_order_and_rounding(oracle_lib):
+    # slot order matters in float32: (1e8 + 1) - 1e8 = 0, but (1e8 - 1e8) + 1 = 1
+    y = np.array([[1.0e8], [1.0], [-1.0e8]], dtype=np.float32)
+    w = np.ones((1, 3), dtype=np.float32)
+    tr = np.array([[0, 1, 2]], dtype=np.int32)
+    assert oracle_lib.bf16_to_double(oracle_lib.combine_f32_canonical(y, w, tr))[0, 0] == 0.0
+    tr_swap = np.array([[0, 2, 1]], dtype=np.int32)
+    assert oracle_lib.bf16_to_double(oracle_lib.combine_f32_canonical(y, w, tr_swap))[0, 0] == 1.0
+    # the shared term is added last, after the routed sum
+    s = np.array([[-1.0e8]], dtype=np.float32)
+    y2 = np.array([[1.0e8], [1.0]], dtype=np.float32)
+    out = oracle_lib.combine_f32_canonical(y2, np.ones((1, 2), np.float32), np.array([[0, 1]], np.int32), s)
+    assert oracle_lib.bf16_to_double(out)[0, 0] == 0.0
+    # a float32 result exactly on a bf16 midpoint rounds to even: 1 + 2^-8 -> 1.0 ; 1 + 3*2^-8 -> 1 + 2^-6
+    y3 = np.array([[1.0], [2.0 ** -8]], dtype=np.float32)
+    o3 = oracle_lib.combine_f32_canonical(y3, np.ones((1, 2), np.float32), np.array([[0, 1]], np.int32))
+    assert oracle_lib.bf16_to_double(o3)[0, 0] == 1.0
+    y4 = np.array([[1.0], [3 * 2.0 ** -8]], dtype=np.float32)
+    o4 = oracle_lib.combine_f32_canonical(y4, np.ones((1, 2), np.float32), np.array([[0, 1]], np.int32))
+    assert oracle_lib.bf16_to_double(o4)[0, 0] == 1.0 + 2.0 ** -6
+
+
+def test_combine_f64_matches_library(oracle_lib):
+    rng = np.random.default_rng(16)
+    n, k, H = 40, 5, 24
+    y = rng.standard_normal((n * k, H)).astype(np.float32)
+    w = rng.random((n, k)).astype(np.float32)
+    s = rng.standard_normal((n, H)).astype(np.float32)
+    tr = rng.permutation(n * k).reshape(n, k).astype(np.int32)
+    ref, _ = oracle_lib.combine_f64(y, w, tr, s)
+    exact = np.einsum("nk,nkh->nh", w.astype(np.float64), y[tr].astype(np.float64)) + s
+    np.testing.assert_allclose(ref, exact, rtol=1e-14, atol=1e-15)
