@@ -1,0 +1,461 @@
+"""Benchmark of the expert-major chunked MoE prefill layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME] [--chunk C]
+
+One step = one call of the layer (moe_prefill_run) over all tokens of the workload: per chunk the router GEMM,
+top-k, histogram/scan/permute, grouped gate/up + SwiGLU, grouped down, shared expert and the canonical combine.
+`value` is tokens/s over all ranks with inputs resident in device memory; `e2e` repeats the measurement through
+the same call with the activations in pinned host memory, the host->device copy of x and the device->host copy of
+the output inside the timed region. Prints one JSON line (rank 0).
+
+--impl reference times the float64 CPU oracle (oracle/) on the host cores on a bounded sample of the same
+workload: the reference arm of this layer is that plain CPU implementation.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer prefill tokens/s (1×GB300); grouped-GEMM tensor-pipe % of peak"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "e512_t16022"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--chunk", type=int, default=0, help="chunk size (default: the workload's first chunk size)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single-pass", action="store_true", help="also time chunk = T (one pass over all tokens)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate_rate(units_per_rank: list, seconds_per_rank: list) -> float:
+    """Whole-job throughput of weakly scaled replicas: all units processed over the slowest rank's time."""
+    return sum(units_per_rank) / max(seconds_per_rank)
+
+
+# ------------------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, log_path: str | None = None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.log_path = log_path
+
+    def start(self):
+        exe = shutil.which("nvidia-smi")
+        if not exe:
+            return
+        self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                      "-lms", "200", "-i", self.gpu_id], stdout=subprocess.PIPE,
+                                     stderr=subprocess.DEVNULL, text=True)
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=5)
+        if self.log_path:
+            with open(self.log_path, "w") as f:
+                f.write(self.FIELDS + "\n" + "\n".join(self.lines) + "\n")
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_selector(torch, device_index: int) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[device_index] if vis else str(device_index)
+
+
+# ------------------------------------------------------------------------------------------------ helpers
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("expert_major_chunked_gb300/csrc/gemm.cu", "expert_major_chunked_gb300/csrc/ptx.cuh",
+                "expert_major_chunked_gb300/csrc/internal.h"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, chunk: int):
+    """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken on the current kernel."""
+    path = os.path.join(ROOT, "profiles", f"gate_up_traffic_{workload}_c{chunk}.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------------ reference arm
+
+def run_reference(args, dist: Dist):
+    if dist.rank != 0:
+        dist.close()
+        return
+    import numpy as np
+    import oracle
+    from expert_major_chunked_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    chunk = args.chunk or wl.chunks[0]
+    inp = workloads.generate(wl)
+    cores = oracle.num_threads()
+    # calibrate, then size each step so that warm-up + timed steps fit in about two minutes
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp, wl.top_k, token_idx=np.arange(min(32, wl.tokens)))
+    rate = min(32, wl.tokens) / (time.perf_counter() - t0)
+    per_step = int(max(1, min(wl.tokens, rate * 120.0 / (args.steps + args.warmup))))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.moe_forward(inp, wl.top_k, token_idx=rng.choice(wl.tokens, per_step, replace=False))
+    secs = 0.0
+    for _ in range(args.steps):
+        idx = rng.choice(wl.tokens, per_step, replace=False)
+        t0 = time.perf_counter()
+        oracle.moe_forward(inp, wl.top_k, token_idx=idx)
+        secs += time.perf_counter() - t0
+    value = per_step * args.steps / secs
+    sample = f"{per_step} random tokens per step of the {wl.tokens}-token workload, float64 oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, chunk, args.gpus),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def workload_config(wl, chunk: int, n_gpus: int) -> dict:
+    return {"workload": wl.name, "tokens": wl.tokens, "hidden": wl.hidden, "experts": wl.n_experts,
+            "inter": wl.inter, "top_k": wl.top_k, "shared_inter": wl.shared_inter, "chunk": chunk,
+            "router": "zipf(1.1) prior" if wl.zipf_prior else "uniform N(0,1) logits",
+            "l2": "inputs larger than L2: every chunk streams all touched expert weights (GBs) from HBM",
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "1 GPU"}
+
+
+# ------------------------------------------------------------------------------------------------ our arm
+
+def cpu_baseline(inp, wl, budget_s: float = 10.0) -> dict:
+    import numpy as np
+    import oracle
+    cores = oracle.num_threads()
+    t0 = time.perf_counter()
+    probe = min(64, wl.tokens)
+    oracle.moe_forward(inp, wl.top_k, token_idx=np.arange(probe))
+    rate = probe / (time.perf_counter() - t0)
+    n = int(min(wl.tokens, max(probe, rate * budget_s)))
+    t0 = time.perf_counter()
+    oracle.moe_forward(inp, wl.top_k, token_idx=np.arange(n))
+    secs = time.perf_counter() - t0
+    return {"value": n / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {wl.tokens} tokens, full layer in float64 ({secs:.1f} s)"}
+
+
+def gate_up_bytes_and_flops(wl, offs_per_chunk, chunk_sizes):
+    """Algorithmic DRAM bytes and useful FLOPs of one gate/up launch (per chunk, averaged over the chunks):
+    weights of the touched experts + shared expert, the gathered input rows read once, h written once."""
+    H, I, Is, k = wl.hidden, wl.inter, wl.shared_inter, wl.top_k
+    tot_b = tot_f = 0.0
+    for offs, n in zip(offs_per_chunk, chunk_sizes):
+        counts = offs[1:] - offs[:-1]
+        touched = int((counts > 0).sum())
+        R = n * k
+        b = touched * 2 * I * H * 2 + (2 * Is * H * 2 if Is else 0) + (R + (n if Is else 0)) * H * 2 \
+            + (R * I + n * Is) * 2
+        f = 2.0 * R * H * 2 * I + 2.0 * n * H * 2 * Is
+        tot_b += b
+        tot_f += f
+    m = len(chunk_sizes)
+    return tot_b / m, tot_f / m
+
+
+def down_bytes_and_flops(wl, offs_per_chunk, chunk_sizes):
+    H, I, Is, k = wl.hidden, wl.inter, wl.shared_inter, wl.top_k
+    tot_b = tot_f = 0.0
+    for offs, n in zip(offs_per_chunk, chunk_sizes):
+        counts = offs[1:] - offs[:-1]
+        touched = int((counts > 0).sum())
+        R = n * k
+        b = touched * H * I * 2 + (H * Is * 2 if Is else 0) + (R * I + n * Is) * 2 + (R + (n if Is else 0)) * H * 4
+        f = 2.0 * R * I * H + 2.0 * n * Is * H
+        tot_b += b
+        tot_f += f
+    m = len(chunk_sizes)
+    return tot_b / m, tot_f / m
+
+
+def run_ours(args, dist: Dist):
+    import numpy as np
+    import torch
+    from expert_major_chunked_gb300 import binding, workloads
+
+    assert torch.cuda.is_available(), "the benchmark needs a CUDA device"
+    torch.cuda.set_device(dist.local_rank)
+    wl = workloads.WORKLOADS[args.workload]
+    chunk = args.chunk or wl.chunks[0]
+    T = wl.tokens
+    inp = workloads.generate(wl)
+    dev = {k: v.cuda() for k, v in inp.items() if k != "x"}
+    layer = binding.MoePrefill(dev, top_k=wl.top_k, max_chunk=max(chunk, T if args.single_pass else chunk))
+    stream = torch.cuda.current_stream()
+    x = inp["x"].cuda()
+    out = torch.empty_like(x)
+    n_chunks = (T + chunk - 1) // chunk
+    offs = torch.empty((n_chunks, wl.n_experts + 1), dtype=torch.int32, device="cuda")
+
+    def step(xd, od, ch=chunk, offs_buf=None):
+        layer.run(xd, ch, out=od, expert_offsets=offs_buf)
+
+    # warm-up (also records the per-chunk expert offsets for the byte/FLOP accounting)
+    step(x, out, offs_buf=offs)
+    layer.raise_on_device_error()
+    for _ in range(max(0, args.warmup - 1)):
+        step(x, out)
+    layer.raise_on_device_error()
+    offs_host = offs.cpu().numpy()
+    chunk_sizes = [min(chunk, T - c0) for c0 in range(0, T, chunk)]
+
+    # ---------------------------------------------------------------- timed region (device-resident inputs)
+    clocks = ClockSampler(gpu_selector(torch, dist.local_rank))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = binding.moe_prefill_launch_count(layer.plan)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(x, out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks_info = clocks.stop()
+    dist.barrier()
+    gpu_launches = binding.moe_prefill_launch_count(layer.plan) - launches0
+    st = layer.check()
+    if st != 0:
+        raise binding.MoeError(st, binding.moe_prefill_last_error())
+    secs = ev0.elapsed_time(ev1) / 1e3
+    secs_max = dist.max(secs)
+    value = aggregate_rate([T * args.steps] * dist.world, [secs_max] * dist.world)
+    ms_per_step = secs_max / args.steps * 1e3
+
+    # ---------------------------------------------------------------- per-kernel CUDA-event timing
+    k_steps = max(3, min(args.steps, 50))
+    binding.moe_prefill_set_profiling(layer.plan, True)
+    binding.moe_prefill_kernel_times(layer.plan)  # clear
+    for _ in range(k_steps):
+        step(x, out)
+    times = binding.moe_prefill_kernel_times(layer.plan)
+    binding.moe_prefill_set_profiling(layer.plan, False)
+    peaks = load_peaks()
+    gu_ms, gu_n = times["gate_up"]
+    dn_ms, dn_n = times["down"]
+    gu_avg_s = gu_ms / gu_n / 1e3
+    dn_avg_s = dn_ms / dn_n / 1e3
+    gu_bytes, gu_flops = gate_up_bytes_and_flops(wl, offs_host, chunk_sizes)
+    dn_bytes, dn_flops = down_bytes_and_flops(wl, offs_host, chunk_sizes)
+    achieved = gu_bytes / gu_avg_s / 1e9
+    roofline = {"bound": "hbm", "kernel": "grouped gate/up GEMM + SwiGLU", "achieved": achieved,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": ncu_traffic(wl.name, chunk), "algorithmic_bytes_per_launch": gu_bytes,
+                "avg_launch_ms": gu_avg_s * 1e3, "peak_source": peaks["source"] + " (hbm_gbs)"}
+    tc_peak = peaks["bf16_tflops_sustained"]
+    grouped = {
+        "gate_up": {"avg_ms": gu_avg_s * 1e3, "tflops": gu_flops / gu_avg_s / 1e12,
+                    "tc_frac_of_sustained_bf16": gu_flops / gu_avg_s / 1e12 / tc_peak,
+                    "gbs": achieved, "hbm_frac": achieved / peaks["hbm_gbs"]},
+        "down": {"avg_ms": dn_avg_s * 1e3, "tflops": dn_flops / dn_avg_s / 1e12,
+                 "tc_frac_of_sustained_bf16": dn_flops / dn_avg_s / 1e12 / tc_peak,
+                 "gbs": dn_bytes / dn_avg_s / 1e9, "hbm_frac": dn_bytes / dn_avg_s / 1e9 / peaks["hbm_gbs"]},
+        "per_kernel_ms_per_step": {k: v[0] / k_steps for k, v in times.items()},
+        "profiled_steps": k_steps,
+    }
+    R = T * wl.top_k
+    grouped["combine_gbs"] = (R * wl.hidden * 4 + T * wl.hidden * (4 + 2)) / (times["combine"][0] / k_steps / 1e3) / 1e9
+    grouped["topk_gbs"] = (T * wl.n_experts * 4 + T * wl.hidden * 2 + T * wl.top_k * 8) / \
+        (times["topk"][0] / k_steps / 1e3) / 1e9
+
+    # ---------------------------------------------------------------- end to end: host buffers through the ABI
+    x_host = inp["x"].pin_memory()
+    out_host = torch.empty(x_host.shape, dtype=x_host.dtype).pin_memory()
+    x_dev = torch.empty_like(x)
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_secs = dist.max(ev0.elapsed_time(ev1) / 1e3)
+    e2e = {"value": T * e2e_steps * dist.world / e2e_secs, "unit": UNIT,
+           "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+           "d2h_bytes_per_step": out_host.numel() * out_host.element_size()}
+
+    # ---------------------------------------------------------------- optional single pass (chunk = T)
+    single = None
+    if args.single_pass:
+        step(x, out, ch=T)
+        torch.cuda.synchronize()
+        binding.moe_prefill_set_profiling(layer.plan, True)
+        binding.moe_prefill_kernel_times(layer.plan)
+        sp_steps = 20
+        ev0.record(stream)
+        for _ in range(sp_steps):
+            step(x, out, ch=T)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        sp_secs = ev0.elapsed_time(ev1) / 1e3
+        t2 = binding.moe_prefill_kernel_times(layer.plan)
+        binding.moe_prefill_set_profiling(layer.plan, False)
+        offs1 = torch.empty((1, wl.n_experts + 1), dtype=torch.int32, device="cuda")
+        step(x, out, ch=T, offs_buf=offs1)
+        o1 = offs1.cpu().numpy()
+        b1, f1 = gate_up_bytes_and_flops(wl, o1, [T])
+        b2, f2 = down_bytes_and_flops(wl, o1, [T])
+        g_s = t2["gate_up"][0] / t2["gate_up"][1] / 1e3
+        d_s = t2["down"][0] / t2["down"][1] / 1e3
+        single = {"tokens_per_s": T * sp_steps / sp_secs, "ms_per_step": sp_secs / sp_steps * 1e3,
+                  "gate_up_tc_frac_of_sustained_bf16": f1 / g_s / 1e12 / tc_peak,
+                  "down_tc_frac_of_sustained_bf16": f2 / d_s / 1e12 / tc_peak,
+                  "grouped_tc_frac_of_sustained_bf16": (f1 + f2) / (g_s + d_s) / 1e12 / tc_peak,
+                  "gate_up_hbm_frac": b1 / g_s / 1e9 / peaks["hbm_gbs"]}
+        layer.raise_on_device_error()
+
+    chunks_done, band_tokens = layer.stats()
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, wl)
+
+    if dist.rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": workload_config(wl, chunk, dist.world),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
+                "clocks": clocks_info, "grouped_gemm": grouped,
+                "routing": {"float64_recheck_tokens_last_run": band_tokens, "chunks_last_run": chunks_done}}
+        if single is not None:
+            line["single_pass"] = single
+        print(json.dumps(line), flush=True)
+    del layer
+    dist.close()
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    main()

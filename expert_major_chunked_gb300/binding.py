@@ -1,0 +1,207 @@
+"""ctypes binding of libmoe_prefill.so (include/moe_prefill.h), argument marshalling only.
+
+The functions carry the C names and take raw device pointers (ints) and sizes; `MoePrefill` below wraps them for
+torch tensors (PyTorch supplies device memory and streams). Every step of the layer runs in the library's CUDA
+kernels. If the library cannot be built or loaded, the import of the library raises: there is no other code path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import threading
+from typing import Optional
+
+from . import build as _build
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_WORKSPACE",
+                -4: "MOE_ERR_CUDA", -5: "MOE_ERR_DEVICE_TIMEOUT", -6: "MOE_ERR_ARCH", -7: "MOE_ERR_DEVICE_BOUNDS"}
+KERNEL_NAMES = ["norms", "router", "topk", "count", "scan", "permute", "gate_up", "down", "combine"]
+KERNEL_KINDS = len(KERNEL_NAMES)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class moe_dims(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("inter", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("shared_inter", ctypes.c_int32), ("renormalize", ctypes.c_int32),
+                ("max_chunk", ctypes.c_int32), ("offload_slots", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+_P = ctypes.c_void_p
+_SIGS = {
+    "moe_prefill_plan": ([ctypes.POINTER(moe_dims), _P, _P, _P, _P, _P, ctypes.POINTER(ctypes.c_size_t),
+                          ctypes.POINTER(_P)], ctypes.c_int),
+    "moe_prefill_run": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P, _P, _P],
+                        ctypes.c_int),
+    "moe_prefill_combine": ([_P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
+    "moe_prefill_check": ([_P, _P], ctypes.c_int),
+    "moe_prefill_destroy": ([_P], None),
+    "moe_prefill_last_error": ([], ctypes.c_char_p),
+    "moe_prefill_set_profiling": ([_P, ctypes.c_int32], ctypes.c_int),
+    "moe_prefill_kernel_times": ([_P, _P, _P], ctypes.c_int),
+    "moe_prefill_launch_count": ([_P], ctypes.c_int64),
+    "moe_prefill_set_wait_timeout": ([_P, ctypes.c_uint64], ctypes.c_int),
+    "moe_prefill_run_stats": ([_P, _P, _P, _P], ctypes.c_int),
+    "moe_prefill_debug_gemm": ([_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                ctypes.c_uint64, _P], ctypes.c_int),
+}
+
+
+def lib(build_if_needed: bool = True):
+    """Load libmoe_prefill.so (building it with nvcc first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build_if_needed else _build.LIB_PATH
+            L = ctypes.CDLL(path)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        raise MoeError(status, lib().moe_prefill_last_error().decode())
+
+
+def moe_prefill_last_error() -> str:
+    return lib().moe_prefill_last_error().decode()
+
+
+def moe_prefill_plan(dims: moe_dims, w_router: int, w_gu: int, w_down: int, ws_gu: Optional[int],
+                     ws_down: Optional[int]):
+    """Returns (plan handle, workspace bytes)."""
+    ws = ctypes.c_size_t(0)
+    plan = _P(None)
+    _check(lib().moe_prefill_plan(ctypes.byref(dims), w_router, w_gu, w_down, ws_gu, ws_down, ctypes.byref(ws),
+                                  ctypes.byref(plan)))
+    return plan.value, ws.value
+
+
+def moe_prefill_run(plan, x, T, chunk, workspace, workspace_bytes, out, topk_id=None, topk_w=None,
+                    expert_offsets=None, row_token=None, compute=None, copy=None):
+    _check(lib().moe_prefill_run(plan, x, T, chunk, workspace, workspace_bytes, out, topk_id, topk_w,
+                                 expert_offsets, row_token, compute, copy))
+
+
+def moe_prefill_combine(y, w, token_row, s, n, k, H, out, stream=None):
+    _check(lib().moe_prefill_combine(y, w, token_row, s, n, k, H, out, stream))
+
+
+def moe_prefill_check(workspace, stream=None) -> int:
+    """Returns the status (does not raise) so callers can test for device-side errors."""
+    return lib().moe_prefill_check(workspace, stream)
+
+
+def moe_prefill_destroy(plan):
+    lib().moe_prefill_destroy(plan)
+
+
+def moe_prefill_set_profiling(plan, enable: bool):
+    _check(lib().moe_prefill_set_profiling(plan, 1 if enable else 0))
+
+
+def moe_prefill_kernel_times(plan):
+    ms = (ctypes.c_double * KERNEL_KINDS)()
+    n = (ctypes.c_int64 * KERNEL_KINDS)()
+    _check(lib().moe_prefill_kernel_times(plan, ms, n))
+    return {KERNEL_NAMES[i]: (ms[i], n[i]) for i in range(KERNEL_KINDS)}
+
+
+def moe_prefill_launch_count(plan) -> int:
+    return int(lib().moe_prefill_launch_count(plan))
+
+
+def moe_prefill_set_wait_timeout(plan, timeout_ns: int):
+    _check(lib().moe_prefill_set_wait_timeout(plan, timeout_ns))
+
+
+def moe_prefill_run_stats(workspace, stream=None):
+    chunks, band = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().moe_prefill_run_stats(workspace, stream, ctypes.byref(chunks), ctypes.byref(band)))
+    return chunks.value, band.value
+
+
+def moe_prefill_debug_gemm(a, b, c, m, n, k_dim, epilogue, err_word, stall_flag=None, timeout_ns=0, stream=None):
+    _check(lib().moe_prefill_debug_gemm(a, b, c, m, n, k_dim, epilogue, err_word, stall_flag, timeout_ns, stream))
+
+
+# ---------------------------------------------------------------------------------------------------- torch helper
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream or None
+
+
+class MoePrefill:
+    """One MoE layer bound to device weights (torch bf16 tensors), with its workspace.
+
+    weights: dict with w_router [E][H], w_gu [E][2I][H], w_down [E][H][I] and optionally ws_gu [2I_s][H],
+    ws_down [H][I_s], all bf16 CUDA tensors.
+    """
+
+    def __init__(self, weights: dict, top_k: int, max_chunk: int):
+        import torch
+        wr, wgu, wd = weights["w_router"], weights["w_gu"], weights["w_down"]
+        wsg, wsd = weights.get("ws_gu"), weights.get("ws_down")
+        for t in (wr, wgu, wd, wsg, wsd):
+            if t is not None and (t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous()):
+                raise ValueError("weights must be contiguous bf16 CUDA tensors")
+        E, H = wr.shape
+        I = wgu.shape[1] // 2
+        Is = wsg.shape[0] // 2 if wsg is not None else 0
+        self.dims = moe_dims(H, E, I, top_k, Is, 1, max_chunk, 0)
+        self.weights = weights  # keep alive: the plan points at them
+        self.plan, self.workspace_bytes = moe_prefill_plan(self.dims, wr.data_ptr(), wgu.data_ptr(), wd.data_ptr(),
+                                                           _ptr(wsg), _ptr(wsd))
+        self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=wr.device)
+        self.hidden, self.n_experts, self.top_k = H, E, top_k
+
+    def __del__(self):
+        plan = getattr(self, "plan", None)
+        if plan:
+            moe_prefill_destroy(plan)
+            self.plan = None
+
+    def run(self, x, chunk: int, out=None, topk_id=None, topk_w=None, expert_offsets=None, row_token=None,
+            stream=None):
+        import torch
+        if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
+            raise ValueError("x must be a contiguous bf16 CUDA tensor")
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        moe_prefill_run(self.plan, x.data_ptr(), T, chunk, self.workspace.data_ptr(), self.workspace_bytes,
+                        out.data_ptr(), _ptr(topk_id), _ptr(topk_w), _ptr(expert_offsets), _ptr(row_token),
+                        _stream_handle(stream), None)
+        return out
+
+    def check(self, stream=None) -> int:
+        return moe_prefill_check(self.workspace.data_ptr(), _stream_handle(stream))
+
+    def raise_on_device_error(self, stream=None):
+        st = self.check(stream)
+        if st != MOE_OK:
+            raise MoeError(st, moe_prefill_last_error())
+
+    def stats(self, stream=None):
+        return moe_prefill_run_stats(self.workspace.data_ptr(), _stream_handle(stream))

@@ -1,0 +1,332 @@
+// Grouped GEMM on the 5th-generation tensor cores: TMA -> shared memory (128B swizzle) -> tcgen05.mma (TMEM
+// accumulators) -> epilogue from TMEM. One persistent CTA per SM walks a tile list with a static stride.
+//
+// This is the expert-major projection step of the layer: "Flash Next EXL3: exact deep prefill" (introduction) runs
+// each chunk expert by expert, and the maintainer review of the deep-prefill draft names the two expert kernels, a
+// gate/up projection and a down projection, on tiles of expert members. Here a tile is 128 member rows of one expert
+// (or of the shared expert) times up to 256 output columns; the K loop is fixed (64 per stage, 16 per instruction),
+// so every output element is computed with the same accumulation order whatever the tile's row position or the
+// number of members of its expert. That makes each row independent of the chunk size.
+//
+// Warp roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns the TMEM allocation and lane 0 issues the
+// UMMAs; warps 2..5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..+31) and store the outputs.
+// Two TMEM accumulators of 256 columns let the epilogue of one tile overlap the main loop of the next.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+
+namespace moe {
+namespace {
+
+struct TileInfo {
+  int cls, group, n_idx, a_row0, rows, out_row0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+  TileInfo ti;
+  if (p.tiles != nullptr) {
+    const int4 r = __ldg(p.tiles + t);
+    const uint32_t x = static_cast<uint32_t>(r.x);
+    ti.group = static_cast<int>(x & 0x7FFFu);
+    ti.cls = static_cast<int>((x >> 15) & 1u);
+    ti.n_idx = static_cast<int>(x >> 16);
+    ti.a_row0 = r.y;
+    ti.rows = r.z;
+    ti.out_row0 = r.w;
+  } else {
+    const int mt = (p.dense_m + kBlockM - 1) / kBlockM;
+    const int m = t % mt;
+    ti.cls = 0;
+    ti.group = 0;
+    ti.n_idx = t / mt;
+    ti.a_row0 = p.dense_a_row0 + m * kBlockM;
+    ti.rows = min(kBlockM, p.dense_m - m * kBlockM);
+    ti.out_row0 = m * kBlockM;
+  }
+  return ti;
+}
+
+__device__ __forceinline__ int total_tiles(const GemmParams& p) {
+  if (p.tiles != nullptr) return *reinterpret_cast<const volatile int32_t*>(p.num_tiles);
+  return ((p.dense_m + kBlockM - 1) / kBlockM) * p.dense_n_tiles;
+}
+
+__device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* abort_flag, int site) {
+  *abort_flag = 1;
+  atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, site, static_cast<int>(blockIdx.x)));
+}
+
+__device__ __forceinline__ float swiglu(float g, float u) {
+  // silu(g) * u with silu(z) = z / (1 + exp(-z)); IEEE-rounded division and products.
+  const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+  return __fmul_rn(s, u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sB = base + kStages * kStageABytes;
+  const uint32_t bars = sB + kStages * kStageBBytes;
+  uint8_t* bars_ptr = base_ptr + kStages * (kStageABytes + kStageBBytes);
+  // barrier slots: full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain
+  const uint32_t full0 = bars, empty0 = bars + 8u * kStages, tfull0 = bars + 16u * kStages;
+  const uint32_t tempty0 = tfull0 + 16u, drain_bar = tempty0 + 16u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 16 * kStages + 40);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 16 * kStages + 44);
+
+  const int warp = static_cast<int>(threadIdx.x) / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(full0 + 8u * s, 1);
+      ptx::mbar_init(empty0 + 8u * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull0 + 8u * a, 1);
+      ptx::mbar_init(tempty0 + 8u * a, 4 * 32);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&p.tmA[0]);
+    ptx::tma_prefetch_desc(&p.tmB[0]);
+    ptx::tma_prefetch_desc(&p.tmA[1]);
+    ptx::tma_prefetch_desc(&p.tmB[1]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 2 * kMaxN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const int ntiles = total_tiles(p);
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      bool failed = false;
+      if (p.stall_flag != nullptr) {
+        // Test hook: wait (bounded) for a flag in global memory before loading anything.
+        const uint64_t t0 = ptx::globaltimer();
+        while (*reinterpret_cast<const volatile int32_t*>(p.stall_flag) == 0) {
+          if (ptx::globaltimer() - t0 > tmo || *abort_flag) {
+            raise_error(p, abort_flag, kSiteStallFlag);
+            failed = true;
+            break;
+          }
+        }
+      }
+      for (int t = blockIdx.x; !failed && t < ntiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t);
+        const GemmClass& C = p.cls[ti.cls];
+        const void* tA = &p.tmA[ti.cls];
+        const void* tB = &p.tmB[ti.cls];
+        const int nA = (ti.rows + kABoxRows - 1) / kABoxRows;
+        const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
+        const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * 128u;
+        int b_row0, b_row1 = 0;
+        if (EPI == kEpiSwiGLU) {
+          b_row0 = ti.group * C.b_group_rows + ti.n_idx * C.b_box_rows;
+          b_row1 = b_row0 + C.b_up_offset;
+        } else {
+          b_row0 = ti.group * C.b_group_rows + ti.n_idx * C.n_tile;
+        }
+        for (int kb = 0; kb < C.kblocks; ++kb) {
+          if (!ptx::wait_bounded(empty0 + 8u * stage, phase ^ 1u, tmo, abort_flag)) {
+            raise_error(p, abort_flag, kSiteProducerEmpty);
+            failed = true;
+            break;
+          }
+          const uint32_t fb = full0 + 8u * stage;
+          ptx::mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t a_dst = sA + stage * kStageABytes;
+          const uint32_t b_dst = sB + stage * kStageBBytes;
+          const int kc = kb * kBlockK;
+          for (int j = 0; j < nA; ++j)
+            ptx::tma_load_2d(a_dst + j * (kABoxRows * 128), tA, kc, ti.a_row0 + j * kABoxRows, fb);
+          ptx::tma_load_2d(b_dst, tB, kc, b_row0, fb);
+          if (EPI == kEpiSwiGLU) ptx::tma_load_2d(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (failed) {
+        // Wait (bounded) until every load already issued has landed, so no copy targets a CTA that has exited.
+        int no_abort = 0;
+        for (int s = 0; s < kStages; ++s) {
+          const uint32_t cnt = issued / kStages + (static_cast<uint32_t>(s) < issued % kStages ? 1u : 0u);
+          if (cnt == 0) continue;
+          if (!ptx::wait_bounded(full0 + 8u * s, (cnt - 1u) & 1u, tmo, &no_abort))
+            atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, kSiteDrain, static_cast<int>(blockIdx.x)));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      int stage = 0, local = 0;
+      uint32_t phase = 0;
+      bool failed = false, issued_any = false;
+      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+        const TileInfo ti = decode_tile(p, t);
+        const GemmClass& C = p.cls[ti.cls];
+        const int acc = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!ptx::wait_bounded(tempty0 + 8u * acc, (use & 1u) ^ 1u, tmo, abort_flag)) {
+          raise_error(p, abort_flag, kSiteMmaTmemEmpty);
+          failed = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxN);
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, static_cast<uint32_t>(C.n_tile));
+        for (int kb = 0; kb < C.kblocks; ++kb) {
+          if (!ptx::wait_bounded(full0 + 8u * stage, phase, tmo, abort_flag)) {
+            raise_error(p, abort_flag, kSiteMmaFull);
+            failed = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(sA + stage * kStageABytes);
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(sB + stage * kStageBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk) {
+            // advancing K by 16 bf16 = 32 bytes = 2 units of the descriptor's start address
+            ptx::umma_bf16(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          ptx::umma_commit(empty0 + 8u * stage);  // frees the smem stage once these UMMAs have read it
+          issued_any = true;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (failed) break;
+        ptx::umma_commit(tfull0 + 8u * acc);  // accumulator ready for the epilogue
+      }
+      if (failed && issued_any) {
+        int no_abort = 0;
+        ptx::umma_commit(drain_bar);
+        if (!ptx::wait_bounded(drain_bar, 0u, tmo, &no_abort))
+          atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, kSiteDrain, static_cast<int>(blockIdx.x)));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int local = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+      const TileInfo ti = decode_tile(p, t);
+      const GemmClass& C = p.cls[ti.cls];
+      const int acc = local & 1;
+      const uint32_t use = static_cast<uint32_t>(local >> 1);
+      bool ok = ptx::wait_bounded(tfull0 + 8u * acc, use & 1u, tmo, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) raise_error(p, abort_flag, kSiteEpilogueFull);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kMaxN);
+      const bool valid = row < ti.rows;
+      const int64_t orow = static_cast<int64_t>(ti.out_row0) + row;
+      if (EPI == kEpiSwiGLU) {
+        const int half = C.b_box_rows;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(C.out) + orow * C.out_ld + static_cast<int64_t>(ti.n_idx) * half;
+        for (int c = 0; c < half; c += 32) {
+          uint32_t g[32], u[32];
+          ptx::tmem_ld32(tbase + c, g);
+          ptx::tmem_ld32(tbase + half + c, u);
+          ptx::tmem_ld_wait();
+          uint32_t hp[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            hp[i] = pack_bf16(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                              swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+          }
+        }
+      } else {
+        const int col0 = ti.n_idx * C.n_tile;
+        float* out = static_cast<float*>(C.out) + orow * C.out_ld + col0;
+        const bool vec = (C.out_ld % 4) == 0;
+        for (int c = 0; c < C.n_tile; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tbase + c, v);
+          ptx::tmem_ld_wait();
+          if (valid) {
+            if (vec && col0 + c + 32 <= C.out_cols) {
+              float4* dst = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + c + j < C.out_cols) out[c + j] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(tempty0 + 8u * acc);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 2 * kMaxN);
+  }
+}
+
+}  // namespace
+
+cudaError_t prepare_gemm_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kGemmSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kGemmSmemBytes);
+}
+
+cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  if (epilogue == kEpiSwiGLU)
+    grouped_gemm_kernel<kEpiSwiGLU><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  else
+    grouped_gemm_kernel<kEpiF32><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

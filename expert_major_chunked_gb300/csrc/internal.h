@@ -1,0 +1,133 @@
+// Internal declarations shared by the kernels (gemm.cu, route.cu, combine.cu) and the C-ABI (moe_prefill.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// ------------------------------------------------------------------ device error word (workspace header)
+// Low byte: kind; bits 8..15: role/site; bits 16..31: block index (saturated).
+enum DeviceErrorKind : int32_t {
+  kDevErrNone = 0,
+  kDevErrTimeout = 1,   // a bounded wait on an mbarrier gave up
+  kDevErrBounds = 2,    // a device-side bounds check failed (access skipped)
+};
+enum DeviceErrorSite : int32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaTmemEmpty = 2,
+  kSiteMmaFull = 3,
+  kSiteEpilogueFull = 4,
+  kSiteStallFlag = 5,
+  kSiteDrain = 6,
+  kSiteRouting = 7,
+};
+__host__ __device__ inline int32_t dev_error_code(int32_t kind, int32_t site, int32_t block) {
+  return kind | (site << 8) | ((block > 0xFFFF ? 0xFFFF : block) << 16);
+}
+
+// Workspace header (first 256 bytes of the workspace).
+struct WsHeader {
+  int32_t err;                 // device error word for the most recent run
+  int32_t band_tokens;         // tokens whose top-k needed the float64 recheck (this run)
+  int32_t chunks_done;         // chunks processed (this run)
+  int32_t pad0;
+  float wnorm_max;             // max_e ||w_router[e]||_2 (upper bound)
+  int32_t pad[59];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// ------------------------------------------------------------------ grouped GEMM
+constexpr int kBlockM = 128;        // UMMA M (rows of a tile)
+constexpr int kBlockK = 64;         // bf16 elements per 128-byte swizzle row
+constexpr int kStages = 4;          // smem pipeline depth
+constexpr int kMaxN = 256;          // widest UMMA N (TMEM columns per accumulator)
+constexpr int kABoxRows = 32;       // A rows per TMA box (a tile loads ceil(rows/32) boxes)
+constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM alloc, warps 2..5 epilogue
+constexpr int kStageABytes = kBlockM * kBlockK * 2;   // 16 KB
+constexpr int kStageBBytes = kMaxN * kBlockK * 2;     // 32 KB
+constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + 256;
+
+enum Epilogue : int { kEpiF32 = 0, kEpiSwiGLU = 1 };
+
+// One operand class of a grouped GEMM launch (class 0: routed experts, class 1: shared expert).
+struct GemmClass {
+  int32_t kblocks;        // K / 64
+  int32_t n_tile;         // UMMA N = TMEM columns used by a tile
+  int32_t b_box_rows;     // rows per B TMA box (SwiGLU: gate half = up half = n_tile/2; F32: n_tile)
+  int32_t b_group_rows;   // B rows per group (expert): row base of group e is e * b_group_rows
+  int32_t b_up_offset;    // SwiGLU: row offset of the up half inside a group (= I), else 0
+  int32_t out_cols;       // valid output columns (masks a ragged last N tile)
+  int64_t out_ld;         // output row stride in elements
+  void* out;              // F32: float*, SwiGLU: bf16*
+};
+
+// Tile record: x = group | (cls << 15) | (n_idx << 16); y = first A row; z = valid rows (1..128); w = first out row.
+struct GemmParams {
+  CUtensorMap tmA[2];
+  CUtensorMap tmB[2];
+  GemmClass cls[2];
+  const int4* tiles;          // device tile list (nullptr: dense mode)
+  const int32_t* num_tiles;   // device tile count (used when tiles != nullptr)
+  int32_t dense_m;            // dense mode: M rows, tiles = ceil(M/128) x n_tiles, A rows start at dense_a_row0
+  int32_t dense_n_tiles;
+  int32_t dense_a_row0;
+  int32_t pad_;
+  int32_t* err;               // device error word
+  const int32_t* stall_flag;  // test hook: producer waits for *stall_flag != 0 before any load (nullptr: none)
+  uint64_t timeout_ns;        // bound on every mbarrier wait
+};
+
+cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream);
+cudaError_t prepare_gemm_kernels();   // sets the dynamic shared memory attribute (once per device)
+
+// ------------------------------------------------------------------ routing
+struct RouteParams {
+  const float* logits;        // [n][E] fp32 (chunk-local)
+  const uint16_t* x;          // chunk rows of X, bf16 [n][H]
+  const uint16_t* w_router;   // bf16 [E][H]
+  const float* wnorm;         // [E] ||w_e||_2
+  WsHeader* hdr;
+  int32_t n, E, H, k;
+  float tau_coef;             // tau = tau_coef * ||x_t|| * max_e ||w_e||
+  int32_t* topk_id;           // [n][k]
+  float* topk_w;              // [n][k]
+  uint8_t* band_flag;         // [n] 1 when the float64 recheck ran
+};
+cudaError_t launch_router_norms(const uint16_t* w_router, int E, int H, float* wnorm, WsHeader* hdr,
+                                cudaStream_t stream);
+cudaError_t launch_topk(const RouteParams& p, cudaStream_t stream);
+
+struct PermuteParams {
+  const int32_t* topk_id;     // [n][k]
+  const uint8_t* band_flag;   // [n]
+  const uint16_t* x;          // chunk rows of X [n][H]
+  int32_t n, E, H, k, nblk;
+  int64_t token0;             // global id of the chunk's first token
+  uint32_t* masks;            // [nblk][E]
+  int32_t* counts;            // [nblk][E]
+  int32_t* block_band;        // [nblk]
+  int32_t* base;              // [nblk][E]
+  int32_t* offsets;           // [E+1] (workspace)
+  int32_t* offsets_out;       // user [E+1] for this chunk, or nullptr
+  int32_t* token_row;         // [n][k]
+  int32_t* row_token;         // [n*k] (global token ids)
+  uint16_t* xp;               // gathered rows [n*k][H]
+  WsHeader* hdr;
+  // tile lists for the two grouped GEMMs
+  int4* tiles_gu;             // capacity cap_gu
+  int4* tiles_down;           // capacity cap_down
+  int32_t* num_tiles;         // [2]: gu, down
+  int32_t cap_gu, cap_down;
+  int32_t nt_gu, nt_down;     // N tiles per routed expert (GU: I / half, down: H / bn_down)
+  int32_t nt_gu_shared, nt_down_shared;  // N tiles of the shared expert (0 = no shared expert)
+};
+cudaError_t launch_count(const PermuteParams& p, cudaStream_t stream);
+cudaError_t launch_scan_tiles(const PermuteParams& p, cudaStream_t stream);
+cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------------ combine
+cudaError_t launch_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
+                           int k, int H, uint16_t* out, cudaStream_t stream);
+
+}  // namespace moe

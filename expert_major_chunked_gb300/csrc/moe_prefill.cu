@@ -1,0 +1,708 @@
+// Host side of the C ABI declared in include/moe_prefill.h: validation, workspace layout, TMA descriptors and the
+// chunk loop. All arithmetic runs in the kernels of gemm.cu, route.cu and combine.cu.
+#include "../../include/moe_prefill.h"
+#include "internal.h"
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+using namespace moe;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+moe_status fail(moe_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                            \
+  do {                                                                                            \
+    cudaError_t e_ = (expr);                                                                      \
+    if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));   \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ------------------------------------------------------------------ TMA descriptor encoding
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 matrix [rows][cols] (row-major), boxes of box_rows x 64 elements, 128-byte swizzle, zero fill out of range.
+moe_status encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu x %llu] matrix, box %u rows", (int)r,
+                (unsigned long long)rows, (unsigned long long)cols, box_rows);
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ device checks
+moe_status check_device(int* device, int* num_sms) {
+  CUDA_TRY(cudaGetDevice(device));
+  cudaDeviceProp prop;
+  CUDA_TRY(cudaGetDeviceProperties(&prop, *device));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(MOE_ERR_ARCH, "device %d is sm_%d%d; the kernels are built for sm_103a", *device, prop.major,
+                prop.minor);
+  *num_sms = prop.multiProcessorCount;
+  static std::mutex mu;
+  static std::vector<int> prepared;
+  std::lock_guard<std::mutex> lock(mu);
+  if (std::find(prepared.begin(), prepared.end(), *device) == prepared.end()) {
+    cudaError_t e = prepare_gemm_kernels();
+    if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
+      return fail(MOE_ERR_ARCH, "kernels do not load on device %d: %s", *device, cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    prepared.push_back(*device);
+  }
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------------ workspace layout
+struct Layout {
+  size_t hdr, wnorm, logits, topk_id, topk_w, band, masks, counts, base, block_band, offsets, token_row, num_tiles,
+      tiles_gu, tiles_down, xp, h, hs, y, s, total;
+  int cap_gu, cap_down;
+};
+
+struct Shape {
+  int H, E, I, k, Is, C;
+  int gu_half, gu_half_s, bn_down, bn_router;
+  int nt_gu, nt_gu_s, nt_down, nt_router;
+};
+
+Shape make_shape(const moe_dims& d) {
+  Shape s;
+  s.H = d.hidden;
+  s.E = d.n_experts;
+  s.I = d.inter;
+  s.k = d.top_k;
+  s.Is = d.shared_inter;
+  s.C = d.max_chunk;
+  s.gu_half = (s.I % 128 == 0) ? 128 : 64;
+  s.gu_half_s = (s.Is % 128 == 0) ? 128 : 64;
+  s.bn_down = (s.H % 256 == 0) ? 256 : (s.H % 128 == 0 ? 128 : 64);
+  s.bn_router = std::min(256, s.E);
+  s.nt_gu = s.I / s.gu_half;
+  s.nt_gu_s = s.Is > 0 ? s.Is / s.gu_half_s : 0;
+  s.nt_down = s.H / s.bn_down;
+  s.nt_router = (s.E + s.bn_router - 1) / s.bn_router;
+  return s;
+}
+
+Layout make_layout(const Shape& s) {
+  Layout L;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  const size_t C = static_cast<size_t>(s.C), E = s.E, k = s.k, H = s.H, I = s.I, Is = s.Is;
+  const size_t R = C * k;
+  const size_t nblk = (C + 31) / 32;
+  const size_t mts = (C + kBlockM - 1) / kBlockM;
+  const size_t routed_mt = (R + kBlockM - 1) / kBlockM + std::min(E, R);
+  L.cap_gu = static_cast<int>(routed_mt * s.nt_gu + (Is > 0 ? mts * s.nt_gu_s : 0));
+  L.cap_down = static_cast<int>(routed_mt * s.nt_down + (Is > 0 ? mts * s.nt_down : 0));
+  L.hdr = take(sizeof(WsHeader));
+  L.wnorm = take(E * 4);
+  L.logits = take(C * E * 4);
+  L.topk_id = take(C * k * 4);
+  L.topk_w = take(C * k * 4);
+  L.band = take(C);
+  L.masks = take(nblk * E * 4);
+  L.counts = take(nblk * E * 4);
+  L.base = take(nblk * E * 4);
+  L.block_band = take(nblk * 4);
+  L.offsets = take((E + 1) * 4);
+  L.token_row = take(C * k * 4);
+  L.num_tiles = take(16);
+  L.tiles_gu = take(static_cast<size_t>(L.cap_gu) * 16);
+  L.tiles_down = take(static_cast<size_t>(L.cap_down) * 16);
+  L.xp = take(R * H * 2);
+  L.h = take(R * I * 2);
+  L.hs = take(Is > 0 ? C * Is * 2 : 0);
+  L.y = take(R * H * 4);
+  L.s = take(Is > 0 ? C * H * 4 : 0);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+struct moe_plan {
+  moe_dims d;
+  Shape sh;
+  Layout lay;
+  int device, num_sms;
+  const void *w_router, *w_gu, *w_down, *ws_gu, *ws_down;
+  CUtensorMap tm_wr, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
+  // descriptors of workspace-resident activations, cached per workspace pointer
+  const void* ws_cached = nullptr;
+  CUtensorMap tm_xp, tm_h, tm_hs;
+  uint64_t timeout_ns = 2000000000ull;
+  int64_t launches = 0;
+  bool profiling = false;
+  struct Timed {
+    int kind;
+    cudaEvent_t a, b;
+  };
+  std::vector<Timed> pending;
+  std::vector<cudaEvent_t> pool;
+  double ms[MOE_KERNEL_KINDS] = {};
+  int64_t counts[MOE_KERNEL_KINDS] = {};
+};
+
+namespace {
+
+moe_status validate_dims(const moe_dims* d) {
+  if (!d) return fail(MOE_ERR_INVALID_ARG, "dims is NULL");
+  if (d->hidden <= 0 || d->n_experts <= 0 || d->inter <= 0 || d->top_k <= 0 || d->shared_inter < 0 ||
+      d->max_chunk <= 0 || d->offload_slots < 0)
+    return fail(MOE_ERR_INVALID_ARG, "dims must be positive (shared_inter, offload_slots >= 0)");
+  if (d->hidden % 64 || d->inter % 64 || d->shared_inter % 64)
+    return fail(MOE_ERR_UNSUPPORTED, "hidden, inter and shared_inter must be multiples of 64");
+  if (d->n_experts % 16 || d->n_experts > 1024)
+    return fail(MOE_ERR_UNSUPPORTED, "n_experts must be a multiple of 16 and at most 1024 (got %d)", d->n_experts);
+  if (d->top_k > d->n_experts || d->top_k > 32)
+    return fail(MOE_ERR_UNSUPPORTED, "top_k must be at most min(n_experts, 32) (got %d)", d->top_k);
+  if (d->renormalize != 1) return fail(MOE_ERR_UNSUPPORTED, "only renormalize == 1 is implemented");
+  if (d->offload_slots != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "offloaded experts (offload_slots > 0) are not available in this build");
+  const int64_t R = static_cast<int64_t>(d->max_chunk) * d->top_k;
+  if (R >= (1ll << 30) || static_cast<int64_t>(d->n_experts) * d->hidden >= (1ll << 31) ||
+      static_cast<int64_t>(d->n_experts) * 2 * d->inter >= (1ll << 31))
+    return fail(MOE_ERR_UNSUPPORTED, "sizes exceed 32-bit row indices");
+  return MOE_OK;
+}
+
+void record_kernel(moe_plan* p, int kind, cudaStream_t st, bool before) {
+  if (!p->profiling) return;
+  auto take = [&]() {
+    cudaEvent_t e;
+    if (!p->pool.empty()) {
+      e = p->pool.back();
+      p->pool.pop_back();
+    } else if (cudaEventCreate(&e) != cudaSuccess) {
+      e = nullptr;
+    }
+    return e;
+  };
+  if (before) {
+    moe_plan::Timed t{kind, take(), take()};
+    if (t.a) cudaEventRecord(t.a, st);
+    p->pending.push_back(t);
+  } else if (!p->pending.empty() && p->pending.back().b) {
+    cudaEventRecord(p->pending.back().b, st);
+  }
+}
+
+struct LaunchScope {
+  moe_plan* p;
+  int kind;
+  cudaStream_t st;
+  LaunchScope(moe_plan* p_, int kind_, cudaStream_t st_) : p(p_), kind(kind_), st(st_) {
+    record_kernel(p, kind, st, true);
+  }
+  ~LaunchScope() {
+    record_kernel(p, kind, st, false);
+    p->launches += 1;
+  }
+};
+
+moe_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MOE_OK;
+  return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
+                            const void* ws_gu, const void* ws_down, size_t* workspace_bytes, moe_plan_t* plan) {
+  if (plan) *plan = nullptr;
+  moe_status st = validate_dims(dims);
+  if (st != MOE_OK) return st;
+  if (!workspace_bytes || !plan) return fail(MOE_ERR_INVALID_ARG, "workspace_bytes and plan must not be NULL");
+  if (!w_router || !w_gu || !w_down) return fail(MOE_ERR_INVALID_ARG, "weight pointers must not be NULL");
+  if (dims->shared_inter > 0 && (!ws_gu || !ws_down))
+    return fail(MOE_ERR_INVALID_ARG, "shared_inter > 0 needs ws_gu and ws_down");
+  if (dims->shared_inter == 0 && (ws_gu || ws_down))
+    return fail(MOE_ERR_INVALID_ARG, "ws_gu / ws_down given but shared_inter == 0");
+  for (const void* q : {w_router, w_gu, w_down, ws_gu, ws_down})
+    if (q && !aligned16(q)) return fail(MOE_ERR_INVALID_ARG, "weight pointers must be 16-byte aligned");
+  int device = 0, num_sms = 0;
+  st = check_device(&device, &num_sms);
+  if (st != MOE_OK) return st;
+
+  moe_plan* p = new moe_plan();
+  p->d = *dims;
+  p->sh = make_shape(*dims);
+  p->lay = make_layout(p->sh);
+  p->device = device;
+  p->num_sms = num_sms;
+  p->w_router = w_router;
+  p->w_gu = w_gu;
+  p->w_down = w_down;
+  p->ws_gu = ws_gu;
+  p->ws_down = ws_down;
+  const Shape& s = p->sh;
+  st = encode_bf16_2d(&p->tm_wr, w_router, s.E, s.H, s.bn_router);
+  if (st == MOE_OK)
+    st = encode_bf16_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H, s.gu_half);
+  if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
+  if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
+  if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
+  if (st != MOE_OK) {
+    delete p;
+    return st;
+  }
+  *workspace_bytes = p->lay.total;
+  *plan = p;
+  return MOE_OK;
+}
+
+moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void* workspace,
+                           size_t workspace_bytes, void* out, int32_t* topk_id, float* topk_w,
+                           int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute_, moe_stream_t copy) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
+  if (chunk < 1 || chunk > p->d.max_chunk)
+    return fail(MOE_ERR_INVALID_ARG, "chunk must be in [1, max_chunk=%d] (got %d)", p->d.max_chunk, chunk);
+  if (copy) return fail(MOE_ERR_INVALID_ARG, "copy stream must be NULL for resident weights");
+  if (T >= (1ll << 31)) return fail(MOE_ERR_UNSUPPORTED, "T must be below 2^31");
+  if (T == 0) return MOE_OK;
+  if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out must not be NULL");
+  if (!workspace || workspace_bytes < p->lay.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", p->lay.total, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  for (const void* q : {x, static_cast<const void*>(out), static_cast<const void*>(topk_id),
+                        static_cast<const void*>(topk_w), static_cast<const void*>(expert_offsets),
+                        static_cast<const void*>(row_token)})
+    if (q && (reinterpret_cast<uintptr_t>(q) & 3u) != 0) return fail(MOE_ERR_INVALID_ARG, "pointers need 4-byte alignment");
+  if (!aligned16(x) || !aligned16(out)) return fail(MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != p->device) return fail(MOE_ERR_INVALID_ARG, "current device %d differs from the plan's %d", dev, p->device);
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(compute_);
+  const Shape& s = p->sh;
+  const Layout& L = p->lay;
+  char* ws = static_cast<char*>(workspace);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws + L.hdr);
+  float* wnorm = reinterpret_cast<float*>(ws + L.wnorm);
+  float* logits = reinterpret_cast<float*>(ws + L.logits);
+  uint8_t* band = reinterpret_cast<uint8_t*>(ws + L.band);
+  int32_t* token_row = reinterpret_cast<int32_t*>(ws + L.token_row);
+  int32_t* num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
+  uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);
+  uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
+  uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
+  float* y = reinterpret_cast<float*>(ws + L.y);
+  float* sbuf = reinterpret_cast<float*>(ws + L.s);
+
+  // activation descriptors: X per run; workspace-resident ones cached per workspace address
+  CUtensorMap tm_x;
+  moe_status rc = encode_bf16_2d(&tm_x, x, static_cast<uint64_t>(T), s.H, kABoxRows);
+  if (rc != MOE_OK) return rc;
+  if (p->ws_cached != workspace) {
+    const uint64_t R = static_cast<uint64_t>(s.C) * s.k;
+    rc = encode_bf16_2d(&p->tm_xp, xp, R, s.H, kABoxRows);
+    if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_h, h, R, s.I, kABoxRows);
+    if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(&p->tm_hs, hs, s.C, s.Is, kABoxRows);
+    if (rc != MOE_OK) {
+      p->ws_cached = nullptr;
+      return rc;
+    }
+    p->ws_cached = workspace;
+  }
+
+  {
+    LaunchScope ls(p, MOE_KERNEL_NORMS, st);
+    rc = cuda_status(launch_router_norms(static_cast<const uint16_t*>(p->w_router), s.E, s.H, wnorm, hdr, st),
+                     "router norms launch");
+  }
+  if (rc != MOE_OK) return rc;
+
+  const float tau_coef = static_cast<float>(s.H / 16 + 1) * 0x1p-22f;
+  int64_t chunk_idx = 0;
+  for (int64_t c0 = 0; c0 < T; c0 += chunk, ++chunk_idx) {
+    const int n = static_cast<int>(std::min<int64_t>(chunk, T - c0));
+    const int nblk = (n + 31) / 32;
+    const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * s.H;
+    int32_t* ids = topk_id ? topk_id + c0 * s.k : reinterpret_cast<int32_t*>(ws + L.topk_id);
+    float* wts = topk_w ? topk_w + c0 * s.k : reinterpret_cast<float*>(ws + L.topk_w);
+
+    // 1. router GEMM: logits [n][E] fp32
+    GemmParams g;
+    memset(&g, 0, sizeof g);
+    g.tmA[0] = g.tmA[1] = tm_x;
+    g.tmB[0] = g.tmB[1] = p->tm_wr;
+    GemmClass rc0;
+    rc0.kblocks = s.H / kBlockK;
+    rc0.n_tile = s.bn_router;
+    rc0.b_box_rows = s.bn_router;
+    rc0.b_group_rows = 0;
+    rc0.b_up_offset = 0;
+    rc0.out_cols = s.E;
+    rc0.out_ld = s.E;
+    rc0.out = logits;
+    g.cls[0] = g.cls[1] = rc0;
+    g.tiles = nullptr;
+    g.num_tiles = nullptr;
+    g.dense_m = n;
+    g.dense_n_tiles = s.nt_router;
+    g.dense_a_row0 = static_cast<int32_t>(c0);
+    g.err = &hdr->err;
+    g.stall_flag = nullptr;
+    g.timeout_ns = p->timeout_ns;
+    {
+      const int tiles = ((n + kBlockM - 1) / kBlockM) * s.nt_router;
+      LaunchScope ls(p, MOE_KERNEL_ROUTER, st);
+      rc = cuda_status(launch_grouped_gemm(g, kEpiF32, std::min(p->num_sms, tiles), st), "router GEMM launch");
+    }
+    if (rc != MOE_OK) return rc;
+
+    // 2. top-k + weights
+    RouteParams r;
+    r.logits = logits;
+    r.x = xc;
+    r.w_router = static_cast<const uint16_t*>(p->w_router);
+    r.wnorm = wnorm;
+    r.hdr = hdr;
+    r.n = n;
+    r.E = s.E;
+    r.H = s.H;
+    r.k = s.k;
+    r.tau_coef = tau_coef;
+    r.topk_id = ids;
+    r.topk_w = wts;
+    r.band_flag = band;
+    {
+      LaunchScope ls(p, MOE_KERNEL_TOPK, st);
+      rc = cuda_status(launch_topk(r, st), "top-k launch");
+    }
+    if (rc != MOE_OK) return rc;
+
+    // 3-5. member lists and tile lists
+    PermuteParams q;
+    q.topk_id = ids;
+    q.band_flag = band;
+    q.x = xc;
+    q.n = n;
+    q.E = s.E;
+    q.H = s.H;
+    q.k = s.k;
+    q.nblk = nblk;
+    q.token0 = c0;
+    q.masks = reinterpret_cast<uint32_t*>(ws + L.masks);
+    q.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+    q.block_band = reinterpret_cast<int32_t*>(ws + L.block_band);
+    q.base = reinterpret_cast<int32_t*>(ws + L.base);
+    q.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    q.offsets_out = expert_offsets ? expert_offsets + chunk_idx * (s.E + 1) : nullptr;
+    q.token_row = token_row;
+    q.row_token = row_token ? row_token + c0 * s.k : nullptr;
+    q.xp = xp;
+    q.hdr = hdr;
+    q.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu);
+    q.tiles_down = reinterpret_cast<int4*>(ws + L.tiles_down);
+    q.num_tiles = num_tiles;
+    q.cap_gu = L.cap_gu;
+    q.cap_down = L.cap_down;
+    q.nt_gu = s.nt_gu;
+    q.nt_down = s.nt_down;
+    q.nt_gu_shared = s.nt_gu_s;
+    q.nt_down_shared = s.Is > 0 ? s.nt_down : 0;
+    {
+      LaunchScope ls(p, MOE_KERNEL_COUNT, st);
+      rc = cuda_status(launch_count(q, st), "count launch");
+    }
+    if (rc != MOE_OK) return rc;
+    {
+      LaunchScope ls(p, MOE_KERNEL_SCAN, st);
+      rc = cuda_status(launch_scan_tiles(q, st), "scan launch");
+    }
+    if (rc != MOE_OK) return rc;
+    {
+      LaunchScope ls(p, MOE_KERNEL_PERMUTE, st);
+      rc = cuda_status(launch_permute(q, st), "permute launch");
+    }
+    if (rc != MOE_OK) return rc;
+
+    // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
+    GemmParams gu;
+    memset(&gu, 0, sizeof gu);
+    gu.tmA[0] = p->tm_xp;
+    gu.tmB[0] = p->tm_wgu;
+    GemmClass c_r;
+    c_r.kblocks = s.H / kBlockK;
+    c_r.n_tile = 2 * s.gu_half;
+    c_r.b_box_rows = s.gu_half;
+    c_r.b_group_rows = 2 * s.I;
+    c_r.b_up_offset = s.I;
+    c_r.out_cols = s.I;
+    c_r.out_ld = s.I;
+    c_r.out = h;
+    gu.cls[0] = c_r;
+    if (s.Is > 0) {
+      gu.tmA[1] = tm_x;
+      gu.tmB[1] = p->tm_wsgu;
+      GemmClass c_s;
+      c_s.kblocks = s.H / kBlockK;
+      c_s.n_tile = 2 * s.gu_half_s;
+      c_s.b_box_rows = s.gu_half_s;
+      c_s.b_group_rows = 0;
+      c_s.b_up_offset = s.Is;
+      c_s.out_cols = s.Is;
+      c_s.out_ld = s.Is;
+      c_s.out = hs;
+      gu.cls[1] = c_s;
+    } else {
+      gu.tmA[1] = gu.tmA[0];
+      gu.tmB[1] = gu.tmB[0];
+      gu.cls[1] = c_r;
+    }
+    gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu);
+    gu.num_tiles = num_tiles;
+    gu.err = &hdr->err;
+    gu.timeout_ns = p->timeout_ns;
+    {
+      LaunchScope ls(p, MOE_KERNEL_GATE_UP, st);
+      rc = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st), "gate/up launch");
+    }
+    if (rc != MOE_OK) return rc;
+
+    // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s)
+    GemmParams dn;
+    memset(&dn, 0, sizeof dn);
+    dn.tmA[0] = p->tm_h;
+    dn.tmB[0] = p->tm_wdown;
+    GemmClass d_r;
+    d_r.kblocks = s.I / kBlockK;
+    d_r.n_tile = s.bn_down;
+    d_r.b_box_rows = s.bn_down;
+    d_r.b_group_rows = s.H;
+    d_r.b_up_offset = 0;
+    d_r.out_cols = s.H;
+    d_r.out_ld = s.H;
+    d_r.out = y;
+    dn.cls[0] = d_r;
+    if (s.Is > 0) {
+      dn.tmA[1] = p->tm_hs;
+      dn.tmB[1] = p->tm_wsdown;
+      GemmClass d_s = d_r;
+      d_s.kblocks = s.Is / kBlockK;
+      d_s.b_group_rows = 0;
+      d_s.out = sbuf;
+      dn.cls[1] = d_s;
+    } else {
+      dn.tmA[1] = dn.tmA[0];
+      dn.tmB[1] = dn.tmB[0];
+      dn.cls[1] = d_r;
+    }
+    dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down);
+    dn.num_tiles = num_tiles + 1;
+    dn.err = &hdr->err;
+    dn.timeout_ns = p->timeout_ns;
+    {
+      LaunchScope ls(p, MOE_KERNEL_DOWN, st);
+      rc = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
+    }
+    if (rc != MOE_OK) return rc;
+
+    // 8. canonical combine
+    {
+      LaunchScope ls(p, MOE_KERNEL_COMBINE, st);
+      rc = cuda_status(launch_combine(y, wts, token_row, s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
+                                      static_cast<uint16_t*>(out) + c0 * s.H, st),
+                       "combine launch");
+    }
+    if (rc != MOE_OK) return rc;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_prefill_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
+                               int32_t k, int32_t H, void* out, moe_stream_t stream) {
+  if (n < 0 || k < 1 || k > 32 || H <= 0 || H % 4 != 0)
+    return fail(MOE_ERR_INVALID_ARG, "need n >= 0, 1 <= k <= 32, H a positive multiple of 4");
+  if (n >= (1ll << 31)) return fail(MOE_ERR_UNSUPPORTED, "n must be below 2^31");
+  if (n == 0) return MOE_OK;
+  if (!y || !w || !token_row || !out) return fail(MOE_ERR_INVALID_ARG, "y, w, token_row and out must not be NULL");
+  if (!aligned16(y) || !aligned16(out) || (s && !aligned16(s)))
+    return fail(MOE_ERR_INVALID_ARG, "y, s and out must be 16-byte aligned");
+  return cuda_status(launch_combine(y, w, token_row, s, n, k, H, static_cast<uint16_t*>(out),
+                                    reinterpret_cast<cudaStream_t>(stream)),
+                     "combine launch");
+}
+
+moe_status moe_prefill_check(void* workspace, moe_stream_t stream) {
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  int32_t err = 0;
+  CUDA_TRY(cudaMemcpy(&err, workspace, sizeof err, cudaMemcpyDeviceToHost));
+  if (err == 0) return MOE_OK;
+  const int32_t zero = 0;
+  CUDA_TRY(cudaMemcpy(workspace, &zero, sizeof zero, cudaMemcpyHostToDevice));
+  const int kind = err & 0xFF, site = (err >> 8) & 0xFF, block = (err >> 16) & 0xFFFF;
+  if (kind == kDevErrTimeout)
+    return fail(MOE_ERR_DEVICE_TIMEOUT, "device wait gave up (site %d, block %d, word 0x%08x)", site, block, err);
+  return fail(MOE_ERR_DEVICE_BOUNDS, "device bounds check failed (site %d, index %d, word 0x%08x)", site, block, err);
+}
+
+moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* chunks, int32_t* band_tokens) {
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  WsHeader hdr;
+  CUDA_TRY(cudaMemcpy(&hdr, workspace, sizeof hdr, cudaMemcpyDeviceToHost));
+  if (chunks) *chunks = hdr.chunks_done;
+  if (band_tokens) *band_tokens = hdr.band_tokens;
+  return MOE_OK;
+}
+
+void moe_prefill_destroy(moe_plan_t p) {
+  if (!p) return;
+  for (auto& t : p->pending) {
+    if (t.a) cudaEventDestroy(t.a);
+    if (t.b) cudaEventDestroy(t.b);
+  }
+  for (cudaEvent_t e : p->pool) cudaEventDestroy(e);
+  delete p;
+}
+
+const char* moe_prefill_last_error(void) { return g_last_error.c_str(); }
+
+moe_status moe_prefill_set_profiling(moe_plan_t p, int32_t enable) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  p->profiling = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_prefill_kernel_times(moe_plan_t p, double* ms, int64_t* launches) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  moe_status st = MOE_OK;
+  for (auto& t : p->pending) {
+    if (t.a && t.b) {
+      cudaError_t e = cudaEventSynchronize(t.b);
+      float el = 0.0f;
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&el, t.a, t.b);
+      if (e != cudaSuccess && st == MOE_OK) st = fail(MOE_ERR_CUDA, "event timing: %s", cudaGetErrorString(e));
+      p->ms[t.kind] += el;
+      p->counts[t.kind] += 1;
+    }
+    if (t.a) p->pool.push_back(t.a);
+    if (t.b) p->pool.push_back(t.b);
+  }
+  p->pending.clear();
+  for (int i = 0; i < MOE_KERNEL_KINDS; ++i) {
+    if (ms) ms[i] = p->ms[i];
+    if (launches) launches[i] = p->counts[i];
+    p->ms[i] = 0.0;
+    p->counts[i] = 0;
+  }
+  return st;
+}
+
+int64_t moe_prefill_launch_count(moe_plan_t p) { return p ? p->launches : 0; }
+
+moe_status moe_prefill_set_wait_timeout(moe_plan_t p, uint64_t timeout_ns) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (timeout_ns == 0) return fail(MOE_ERR_INVALID_ARG, "timeout must be positive");
+  p->timeout_ns = timeout_ns;
+  return MOE_OK;
+}
+
+moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t m, int32_t n, int32_t k_dim,
+                                  int32_t epilogue, int32_t* err_word, const int32_t* stall_flag,
+                                  uint64_t timeout_ns, moe_stream_t stream) {
+  if (!a || !b || !c || !err_word) return fail(MOE_ERR_INVALID_ARG, "a, b, c and err_word must not be NULL");
+  if (m < 1 || n < 1 || k_dim < 64 || k_dim % 64) return fail(MOE_ERR_INVALID_ARG, "need m, n >= 1, k_dim % 64 == 0");
+  if (epilogue != kEpiF32 && epilogue != kEpiSwiGLU) return fail(MOE_ERR_INVALID_ARG, "epilogue must be 0 or 1");
+  if (epilogue == kEpiF32 && n % 16) return fail(MOE_ERR_UNSUPPORTED, "epilogue 0 needs n % 16 == 0");
+  if (epilogue == kEpiSwiGLU && n % 64) return fail(MOE_ERR_UNSUPPORTED, "epilogue 1 needs n % 64 == 0");
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c)) return fail(MOE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  int device = 0, num_sms = 0;
+  moe_status st = check_device(&device, &num_sms);
+  if (st != MOE_OK) return st;
+  GemmParams g;
+  memset(&g, 0, sizeof g);
+  GemmClass cl;
+  cl.kblocks = k_dim / kBlockK;
+  cl.b_group_rows = 0;
+  cl.out_cols = n;
+  cl.out_ld = n;
+  cl.out = c;
+  int n_tiles;
+  if (epilogue == kEpiF32) {
+    cl.n_tile = std::min(256, n);
+    cl.b_box_rows = cl.n_tile;
+    cl.b_up_offset = 0;
+    n_tiles = (n + cl.n_tile - 1) / cl.n_tile;
+    st = encode_bf16_2d(&g.tmB[0], b, n, k_dim, cl.b_box_rows);
+  } else {
+    const int half = (n % 128 == 0) ? 128 : 64;
+    cl.n_tile = 2 * half;
+    cl.b_box_rows = half;
+    cl.b_up_offset = n;
+    n_tiles = n / half;
+    st = encode_bf16_2d(&g.tmB[0], b, 2ull * n, k_dim, half);
+  }
+  if (st == MOE_OK) st = encode_bf16_2d(&g.tmA[0], a, m, k_dim, kABoxRows);
+  if (st != MOE_OK) return st;
+  g.tmA[1] = g.tmA[0];
+  g.tmB[1] = g.tmB[0];
+  g.cls[0] = g.cls[1] = cl;
+  g.tiles = nullptr;
+  g.dense_m = m;
+  g.dense_n_tiles = n_tiles;
+  g.dense_a_row0 = 0;
+  g.err = err_word;
+  g.stall_flag = stall_flag;
+  g.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+  const int tiles = ((m + kBlockM - 1) / kBlockM) * n_tiles;
+  return cuda_status(launch_grouped_gemm(g, epilogue, std::min(num_sms, tiles), reinterpret_cast<cudaStream_t>(stream)),
+                     "debug GEMM launch");
+}
+
+}  // extern "C"

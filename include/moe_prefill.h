@@ -1,0 +1,187 @@
+/*
+ * moe_prefill.h — C ABI of the expert-major chunked MoE prefill layer for NVIDIA GB300 (sm_103a), one GPU.
+ *
+ * What it computes. The routed-expert (MoE) layer of long-prompt prefill, run expert-major in chunks, as described by
+ * the pull-request pages "EXL3 Flash Next: deep prefill" (draft slice 3 of 7, sections "What" and "Exactness", and
+ * the maintainer review "To land"), "EXL3 Flash Next: deep prefill (3/8)" (sections "What this changes", "Device
+ * results"), "Flash Next EXL3: exact deep prefill" (introduction; "Completed final functional audit") and the
+ * umbrella draft PR #1113 ("What it adds", "Memory and execution split", "Latest prefill efficiency candidate").
+ * For every chunk of consecutive tokens:
+ *   1. router logits l = x . W_router^T (bf16 inputs, fp32 tensor-core accumulation);
+ *   2. top-k experts per token by logit, an exact tie going to the lower expert id; the selection equals the one
+ *      made on the plain float64 logits (ambiguous cases are recomputed in float64); weights = softmax over the k
+ *      selected logits (renormalised);
+ *   3. per-chunk member lists: histogram, exclusive scan and a stable permutation of the (token, slot) pairs into
+ *      expert-major order (no atomics);
+ *   4. grouped gate/up GEMM per touched expert with fused SwiGLU: h = bf16(silu(x.Wg^T) * (x.Wu^T));
+ *   5. grouped down GEMM: y = h . W_down^T (fp32);
+ *   6. the shared expert on every token (same FFN, weight 1);
+ *   7. the canonical combine: out = bf16( (sum over slots in ascending expert id of w*y, in float32, from +0.0f,
+ *      each product and sum rounded separately) + shared ).
+ * The output is bit-identical for every chunk size (including one pass over all tokens) and from run to run.
+ *
+ * Conventions.
+ *   - Every tensor is row-major and dense; bf16 tensors are passed as raw 16-bit patterns (void pointers).
+ *   - Weights are "K-major": W_router [E][H]; W_gu [E][2I][H] with rows 0..I-1 the gate and rows I..2I-1 the up
+ *     projection of each expert; W_down [E][H][I]; shared Ws_gu [2I_s][H]; Ws_down [H][I_s].
+ *   - Pointers marked "device" must point to memory of the current CUDA device, 16-byte aligned.
+ *   - The caller owns every buffer, including the workspace. The library allocates no device memory. A plan holds
+ *     host state only (sizes, TMA descriptors, pointers, optional timing events) and must not outlive the weights.
+ *   - Calls enqueue work on the given stream and return; a status of MOE_OK means "enqueued". Errors found on the
+ *     host are returned at once and leave the stream untouched. Errors found on the device (a bounded wait that
+ *     gave up, a failed bounds check) are written to the workspace error word, which moe_prefill_check() reports.
+ *   - No call throws, exits, aborts or traps. Messages for the last non-OK status of the calling thread come from
+ *     moe_prefill_last_error().
+ *   - Streams are cudaStream_t values; 0 is the legacy default stream.
+ */
+#ifndef MOE_PREFILL_H
+#define MOE_PREFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,    /* null / misaligned pointer, negative size, chunk < 1, ... */
+  MOE_ERR_UNSUPPORTED = -2,    /* dims outside what the kernels handle (see moe_prefill_plan) */
+  MOE_ERR_WORKSPACE = -3,      /* workspace missing or smaller than moe_prefill_plan reported */
+  MOE_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed (message has the CUDA error) */
+  MOE_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up a bounded wait (reported by moe_prefill_check) */
+  MOE_ERR_ARCH = -6,           /* the current device is not sm_103 or the kernels do not load on it */
+  MOE_ERR_DEVICE_BOUNDS = -7   /* a device-side bounds check failed (reported by moe_prefill_check) */
+} moe_status;
+
+typedef struct {
+  int32_t hidden;        /* H: multiple of 64 */
+  int32_t n_experts;     /* E: routed experts, multiple of 16, 16..1024 */
+  int32_t inter;         /* I: routed expert intermediate size, multiple of 64 */
+  int32_t top_k;         /* k: 1..min(E, 32) */
+  int32_t shared_inter;  /* I_s: 0 = no shared expert, else a multiple of 64 */
+  int32_t renormalize;   /* must be 1: weights are the softmax over the selected logits */
+  int32_t max_chunk;     /* largest chunk size (tokens) a run may use; sizes the workspace */
+  int32_t offload_slots; /* must be 0 for moe_prefill_run (weights resident in device memory) */
+} moe_dims;
+
+typedef struct moe_plan* moe_plan_t;
+
+/*
+ * moe_prefill_plan — validate the layer's sizes, bind its weights and build the TMA descriptors.
+ *   dims            in: sizes (see moe_dims for the accepted ranges).
+ *   w_router        device bf16 [E][H].
+ *   w_gu            device bf16 [E][2I][H] (gate rows, then up rows, per expert).
+ *   w_down          device bf16 [E][H][I].
+ *   ws_gu, ws_down  device bf16 [2I_s][H] and [H][I_s]; both NULL when shared_inter == 0.
+ *   workspace_bytes out: bytes of device workspace moe_prefill_run needs for chunks up to max_chunk.
+ *   plan            out: the plan; free it with moe_prefill_destroy.
+ * Requires the current device to be sm_103 (else MOE_ERR_ARCH). Allocates no device memory. Thread-compatible:
+ * one plan must not be used by two threads at once.
+ */
+moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
+                            const void* ws_gu, const void* ws_down, size_t* workspace_bytes, moe_plan_t* plan);
+
+/*
+ * moe_prefill_run — the layer over T tokens, in chunks of `chunk` tokens (the last chunk may be shorter).
+ *   x               device bf16 [T][H].
+ *   T               tokens (T == 0: no-op, MOE_OK).
+ *   chunk           1..max_chunk tokens per chunk; chunk >= T is one single pass.
+ *   workspace       device buffer of at least workspace_bytes (moe_prefill_plan), 256-byte aligned. It holds the
+ *                   device error word of the most recent run; two runs must not share it concurrently.
+ *   out             device bf16 [T][H] (may not alias x).
+ *   topk_id         device int32 [T][k] or NULL: selected expert ids per token, ascending.
+ *   topk_w          device float [T][k] or NULL: their weights (same order).
+ *   expert_offsets  device int32 [n_chunks][E+1] or NULL: per-chunk exclusive offsets of each expert's rows.
+ *   row_token       device int32 [T*k] or NULL: row j of chunk c (chunk-local index) at c*chunk*k + j holds the
+ *                   global id of the token placed in that row (rows ordered by expert, then token).
+ *   compute         stream for all work.
+ *   copy            must be NULL (reserved for the offloaded-expert variant).
+ * Returns after enqueueing; call moe_prefill_check(workspace, compute) for device-side errors.
+ */
+moe_status moe_prefill_run(moe_plan_t plan, const void* x, int64_t T, int32_t chunk, void* workspace,
+                           size_t workspace_bytes, void* out, int32_t* topk_id, float* topk_w,
+                           int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute, moe_stream_t copy);
+
+/*
+ * moe_prefill_combine — the canonical combine alone (the same kernel run uses).
+ *   y          device float [R][H]: per-row expert outputs.
+ *   w          device float [n][k]: weights, slot order = ascending expert id.
+ *   token_row  device int32 [n][k]: row of y for each (token, slot); every value in [0, R).
+ *   s          device float [n][H] or NULL: shared-expert output added last.
+ *   out        device bf16 [n][H].
+ * n >= 0, 1 <= k <= 32, H a positive multiple of 4. Row indices are not range-checked on the device.
+ */
+moe_status moe_prefill_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
+                               int32_t k, int32_t H, void* out, moe_stream_t stream);
+
+/*
+ * moe_prefill_check — wait for `stream`, then read and clear the device error word in the workspace header.
+ * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_CUDA (a failed synchronisation).
+ */
+moe_status moe_prefill_check(void* workspace, moe_stream_t stream);
+
+/* moe_prefill_destroy — free a plan (host memory and its timing events). NULL is ignored. */
+void moe_prefill_destroy(moe_plan_t plan);
+
+/* moe_prefill_last_error — message for the last non-OK status returned on this thread ("" if none). */
+const char* moe_prefill_last_error(void);
+
+/* ------------------------------------------------------------------------------------------------------------
+ * Diagnostics. These are part of the ABI for measurement and tests; the layer needs none of them.
+ * ------------------------------------------------------------------------------------------------------------ */
+
+/* Kernel kinds for moe_prefill_kernel_times, in launch order within a chunk. */
+enum {
+  MOE_KERNEL_NORMS = 0,  /* router row norms + header reset (once per run) */
+  MOE_KERNEL_ROUTER = 1, /* router GEMM */
+  MOE_KERNEL_TOPK = 2,
+  MOE_KERNEL_COUNT = 3,
+  MOE_KERNEL_SCAN = 4,
+  MOE_KERNEL_PERMUTE = 5,
+  MOE_KERNEL_GATE_UP = 6, /* grouped gate/up GEMM + SwiGLU (routed + shared) */
+  MOE_KERNEL_DOWN = 7,    /* grouped down GEMM (routed + shared) */
+  MOE_KERNEL_COMBINE = 8,
+  MOE_KERNEL_KINDS = 9
+};
+
+/* Enable (1) or disable (0) per-kernel CUDA-event timing of later runs of this plan. */
+moe_status moe_prefill_set_profiling(moe_plan_t plan, int32_t enable);
+
+/* Synchronise on the recorded events and return, per kernel kind, the summed device milliseconds and the number
+   of launches timed since the last call (arrays of MOE_KERNEL_KINDS entries; either may be NULL). Clears them. */
+moe_status moe_prefill_kernel_times(moe_plan_t plan, double* ms, int64_t* launches);
+
+/* Total kernels launched by this plan since it was created. */
+int64_t moe_prefill_launch_count(moe_plan_t plan);
+
+/* Bound, in nanoseconds, on every device-side wait of later runs of this plan (default 2e9). */
+moe_status moe_prefill_set_wait_timeout(moe_plan_t plan, uint64_t timeout_ns);
+
+/* Statistics of the most recent run on `workspace` (synchronises `stream`): chunks processed and tokens whose
+   top-k needed the float64 recheck. Either pointer may be NULL. */
+moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* chunks, int32_t* band_tokens);
+
+/*
+ * moe_prefill_debug_gemm — one dense GEMM through the same tcgen05 kernel the layer uses.
+ *   epilogue 0:  c = float [m][n] = a . b^T with a bf16 [m][k_dim], b bf16 [n][k_dim]; n a multiple of 16.
+ *   epilogue 1:  c = bf16 [m][n] = bf16(silu(a . bg^T) * (a . bu^T)) with b bf16 [2n][k_dim] holding the gate rows
+ *                (0..n-1) then the up rows (n..2n-1); n a multiple of 64.
+ *   k_dim a multiple of 64, m >= 1.
+ *   err_word     device int32, must be 0 on entry; set to a non-zero code when a wait gives up.
+ *   stall_flag   device int32 or NULL: when given, the load warp first waits for it to become non-zero (a test of
+ *                the bounded-wait path: pass a zero flag and a short timeout_ns).
+ *   timeout_ns   bound on every device-side wait (0 = default 2e9).
+ */
+moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t m, int32_t n, int32_t k_dim,
+                                  int32_t epilogue, int32_t* err_word, const int32_t* stall_flag,
+                                  uint64_t timeout_ns, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_PREFILL_H */

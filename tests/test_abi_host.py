@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every function that
+include/moe_prefill.h declares, and rejects bad arguments before touching the device."""
+
+import ctypes
+import os
+import re
+import subprocess
+import threading
+
+import pytest
+
+from conftest import ROOT
+
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(HEADER_DIR, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z0-9_]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from expert_major_chunked_gb300 import binding
+    return binding.lib()
+
+
+def test_header_declares_the_layer_entry_points():
+    names = declared_functions()
+    for required in ("moe_prefill_plan", "moe_prefill_run", "moe_prefill_combine", "moe_prefill_check",
+                     "moe_prefill_destroy", "moe_prefill_last_error"):
+        assert required in names
+    assert len(names) >= 12
+
+
+def test_library_exports_every_declared_symbol(L):
+    from expert_major_chunked_gb300 import binding
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/ but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()], capture_output=True, text=True)
+    exported = set(re.findall(r"\s[TW]\s(moe_[a-z0-9_]+)$", out.stdout, flags=re.M))
+    assert set(declared_functions()) <= exported
+    # every exported moe_* symbol is declared (nothing undocumented leaks out of the library)
+    assert exported <= set(declared_functions())
+
+
+def test_plan_rejects_bad_dims_before_device_use(L):
+    from expert_major_chunked_gb300 import binding as b
+    plan = ctypes.c_void_p(None)
+    ws = ctypes.c_size_t(0)
+    assert L.moe_prefill_plan(None, None, None, None, None, None, ctypes.byref(ws), ctypes.byref(plan)) == -1
+    assert b"dims" in L.moe_prefill_last_error()
+    cases = [
+        (b.moe_dims(100, 16, 128, 2, 0, 1, 64, 0), -2),      # hidden not a multiple of 64
+        (b.moe_dims(256, 20, 128, 2, 0, 1, 64, 0), -2),      # experts not a multiple of 16
+        (b.moe_dims(256, 16, 128, 17, 0, 1, 64, 0), -2),     # k > E
+        (b.moe_dims(256, 2048, 128, 2, 0, 1, 64, 0), -2),    # E > 1024
+        (b.moe_dims(256, 64, 128, 33, 0, 1, 64, 0), -2),     # k > 32
+        (b.moe_dims(256, 16, 128, 2, 0, 0, 64, 0), -2),      # renormalize must be 1
+        (b.moe_dims(256, 16, 128, 2, 0, 1, 0, 0), -1),       # max_chunk < 1
+        (b.moe_dims(-256, 16, 128, 2, 0, 1, 64, 0), -1),     # negative size
+        (b.moe_dims(256, 16, 128, 2, 32, 1, 64, 0), -2),     # shared_inter not a multiple of 64
+    ]
+    fake = ctypes.c_void_p(0x1000)
+    for dims, want in cases:
+        st = L.moe_prefill_plan(ctypes.byref(dims), fake, fake, fake, None, None, ctypes.byref(ws),
+                                ctypes.byref(plan))
+        assert st == want, (dims.hidden, dims.n_experts, dims.top_k, st)
+        assert plan.value is None
+        assert L.moe_prefill_last_error()
+    good = b.moe_dims(256, 16, 128, 2, 128, 1, 64, 0)
+    # shared weights missing although shared_inter > 0
+    assert L.moe_prefill_plan(ctypes.byref(good), fake, fake, fake, None, None, ctypes.byref(ws),
+                              ctypes.byref(plan)) == -1
+    # misaligned weight pointer
+    odd = ctypes.c_void_p(0x1001)
+    assert L.moe_prefill_plan(ctypes.byref(good), odd, fake, fake, fake, fake, ctypes.byref(ws),
+                              ctypes.byref(plan)) == -1
+
+
+def test_plan_without_a_gpu_fails_cleanly(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    from expert_major_chunked_gb300 import binding as b
+    plan = ctypes.c_void_p(None)
+    ws = ctypes.c_size_t(0)
+    fake = ctypes.c_void_p(0x1000)
+    dims = b.moe_dims(256, 16, 128, 2, 128, 1, 64, 0)
+    st = L.moe_prefill_plan(ctypes.byref(dims), fake, fake, fake, fake, fake, ctypes.byref(ws), ctypes.byref(plan))
+    assert st in (-4, -6)  # no CUDA device: a CUDA error, never a crash or a fallback
+    assert plan.value is None
+
+
+def test_run_combine_and_misc_reject_bad_arguments(L):
+    assert L.moe_prefill_run(None, None, 0, 1, None, 0, None, None, None, None, None, None, None) == -1
+    fake = ctypes.c_void_p(0x1000)
+    assert L.moe_prefill_combine(fake, fake, fake, None, 4, 0, 64, fake, None) == -1     # k = 0
+    assert L.moe_prefill_combine(fake, fake, fake, None, 4, 33, 64, fake, None) == -1    # k > 32
+    assert L.moe_prefill_combine(fake, fake, fake, None, 4, 2, 62, fake, None) == -1     # H % 4
+    assert L.moe_prefill_combine(fake, fake, fake, None, -1, 2, 64, fake, None) == -1
+    assert L.moe_prefill_combine(None, None, None, None, 0, 2, 64, None, None) == 0      # n == 0: no-op
+    assert L.moe_prefill_check(None, None) == -1
+    assert L.moe_prefill_set_profiling(None, 1) == -1
+    assert L.moe_prefill_kernel_times(None, None, None) == -1
+    assert L.moe_prefill_launch_count(None) == 0
+    assert L.moe_prefill_set_wait_timeout(None, 5) == -1
+    L.moe_prefill_destroy(None)
+    assert L.moe_prefill_debug_gemm(None, None, None, 1, 16, 64, 0, None, None, 0, None) == -1
+    assert L.moe_prefill_debug_gemm(fake, fake, fake, 1, 16, 60, 0, fake, None, 0, None) == -1  # k % 64
+
+
+def test_last_error_is_per_thread(L):
+    L.moe_prefill_combine(None, None, None, None, 4, 0, 64, None, None)
+    main_msg = L.moe_prefill_last_error()
+    assert main_msg
+    seen = {}
+
+    def other():
+        seen["msg"] = L.moe_prefill_last_error()
+
+    t = threading.Thread(target=other)
+    t.start()
+    t.join()
+    assert seen["msg"] == b""
+    assert L.moe_prefill_last_error() == main_msg
