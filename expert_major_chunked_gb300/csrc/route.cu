@@ -219,10 +219,15 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
     }
     pos += __popc(b);
   }
-  if (lane == 0) {
-    p.band_flag[t] = band ? 1 : 0;
-    if (pos != k) atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
+  if (pos < k) {
+    // cannot happen for finite logits; keep every slot a valid expert id so later kernels stay in bounds
+    if (lane >= pos && lane < k) {
+      ids_out[lane] = 0;
+      w_out[lane] = 0.0f;
+    }
+    if (lane == 0) atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
   }
+  if (lane == 0) p.band_flag[t] = band ? 1 : 0;
 }
 
 // Histogram of a block of 32 tokens: for every expert, a bit mask of the block's tokens that selected it.
@@ -362,9 +367,17 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteParams p) {
   for (int i = warp; i < nt; i += 8) {
     const int t = t0 + i;
     if (lane < k) {
-      const int e = p.topk_id[static_cast<int64_t>(t) * k + lane];
+      int e = p.topk_id[static_cast<int64_t>(t) * k + lane];
+      if (e < 0 || e >= E) {
+        atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
+        e = 0;
+      }
       const int64_t be = static_cast<int64_t>(b) * E + e;
-      const int row = p.base[be] + __popc(p.masks[be] & ((1u << i) - 1u));
+      int row = p.base[be] + __popc(p.masks[be] & ((1u << i) - 1u));
+      if (row < 0 || row >= p.n * k) {
+        atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
+        row = 0;
+      }
       rows_sm[warp][lane] = row;
       p.token_row[static_cast<int64_t>(t) * k + lane] = row;
       if (p.row_token) p.row_token[row] = static_cast<int32_t>(p.token0 + t);

@@ -49,7 +49,8 @@ def test_debug_gemm_float_inputs_close_to_float64(B):
     ref = a.double() @ b.double().T
     c = torch.empty((m, n), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.moe_prefill_debug_gemm(a.cuda().data_ptr(), b.cuda().data_ptr(), c.data_ptr(), m, n, k, 0, err.data_ptr())
+    da, db = a.cuda(), b.cuda()   # keep the device copies alive until the kernel has run
+    B.moe_prefill_debug_gemm(da.data_ptr(), db.data_ptr(), c.data_ptr(), m, n, k, 0, err.data_ptr())
     torch.cuda.synchronize()
     assert err.item() == 0
     scale = a.double().abs() @ b.double().abs().T
@@ -70,7 +71,8 @@ def test_debug_gemm_swiglu_epilogue(B, oracle_lib, m, n, k):
     h_ref = oracle_lib.bf16_to_double(oracle_lib.bf16_from_double(g / (1 + np.exp(-g)) * u))
     c = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    B.moe_prefill_debug_gemm(a.cuda().data_ptr(), b.cuda().data_ptr(), c.data_ptr(), m, n, k, 1, err.data_ptr())
+    da, db = a.cuda(), b.cuda()
+    B.moe_prefill_debug_gemm(da.data_ptr(), db.data_ptr(), c.data_ptr(), m, n, k, 1, err.data_ptr())
     torch.cuda.synchronize()
     assert err.item() == 0
     got = c.cpu().double().numpy()
