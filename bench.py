@@ -44,6 +44,7 @@ def parse_args():
     ap.add_argument("--chunk", type=int, default=0, help="chunk size (default: the workload's first chunk size)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single-pass", action="store_true", help="also time chunk = T (one pass over all tokens)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling runs)")
     return ap.parse_args()
 
 
@@ -167,7 +168,7 @@ def load_peaks() -> dict:
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for rel in ("expert_major_chunked_gb300/csrc/gemm.cu", "expert_major_chunked_gb300/csrc/ptx.cuh",
-                "expert_major_chunked_gb300/csrc/internal.h"):
+                "expert_major_chunked_gb300/csrc/internal.h", "expert_major_chunked_gb300/csrc/route.cu"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -291,6 +292,8 @@ def run_ours(args, dist: Dist):
     assert torch.cuda.is_available(), "the benchmark needs a CUDA device"
     torch.cuda.set_device(dist.local_rank)
     wl = workloads.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.with_(tokens=args.tokens)
     chunk = args.chunk or wl.chunks[0]
     T = wl.tokens
     inp = workloads.generate(wl)
@@ -427,7 +430,7 @@ def run_ours(args, dist: Dist):
                   "gate_up_hbm_frac": b1 / g_s / 1e9 / peaks["hbm_gbs"]}
         layer.raise_on_device_error()
 
-    chunks_done, band_tokens = layer.stats()
+    route_stats = layer.stats()
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
@@ -440,7 +443,7 @@ def run_ours(args, dist: Dist):
                 "config": workload_config(wl, chunk, dist.world),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
                 "clocks": clocks_info, "grouped_gemm": grouped,
-                "routing": {"float64_recheck_tokens_last_run": band_tokens, "chunks_last_run": chunks_done}}
+                "routing_last_run": route_stats}
         if single is not None:
             line["single_pass"] = single
         print(json.dumps(line), flush=True)

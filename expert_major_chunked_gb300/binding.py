@@ -48,7 +48,7 @@ _SIGS = {
     "moe_prefill_kernel_times": ([_P, _P, _P], ctypes.c_int),
     "moe_prefill_launch_count": ([_P], ctypes.c_int64),
     "moe_prefill_set_wait_timeout": ([_P, ctypes.c_uint64], ctypes.c_int),
-    "moe_prefill_run_stats": ([_P, _P, _P, _P], ctypes.c_int),
+    "moe_prefill_run_stats": ([_P, _P, _P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_debug_gemm": ([_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                 ctypes.c_uint64, _P], ctypes.c_int),
 }
@@ -130,10 +130,13 @@ def moe_prefill_set_wait_timeout(plan, timeout_ns: int):
     _check(lib().moe_prefill_set_wait_timeout(plan, timeout_ns))
 
 
-def moe_prefill_run_stats(workspace, stream=None):
-    chunks, band = ctypes.c_int32(0), ctypes.c_int32(0)
-    _check(lib().moe_prefill_run_stats(workspace, stream, ctypes.byref(chunks), ctypes.byref(band)))
-    return chunks.value, band.value
+STATS_NAMES = ["chunks", "flagged", "by_float", "by_double", "by_sequential", "by_many"]
+
+
+def moe_prefill_run_stats(workspace, stream=None) -> dict:
+    arr = (ctypes.c_int32 * len(STATS_NAMES))()
+    _check(lib().moe_prefill_run_stats(workspace, stream, arr, len(STATS_NAMES)))
+    return dict(zip(STATS_NAMES, arr))
 
 
 def moe_prefill_debug_gemm(a, b, c, m, n, k_dim, epilogue, err_word, stall_flag=None, timeout_ns=0, stream=None):

@@ -35,13 +35,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
   __syncthreads();
   for (int c = threadIdx.x * 4; c < H; c += kCombineThreads * 4) {
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int slot = 0; slot < k; ++slot) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(rows[slot]) * H + c));
-      const float ws = wts[slot];
-      acc.x = __fadd_rn(acc.x, __fmul_rn(ws, v.x));
-      acc.y = __fadd_rn(acc.y, __fmul_rn(ws, v.y));
-      acc.z = __fadd_rn(acc.z, __fmul_rn(ws, v.z));
-      acc.w = __fadd_rn(acc.w, __fmul_rn(ws, v.w));
+    // slots in groups of 8: issue the group's loads first (memory-level parallelism), then add them in order
+    for (int s0 = 0; s0 < k; s0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < k) v[j] = __ldg(reinterpret_cast<const float4*>(y + static_cast<int64_t>(rows[s0 + j]) * H + c));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < k) {
+          const float ws = wts[s0 + j];
+          acc.x = __fadd_rn(acc.x, __fmul_rn(ws, v[j].x));
+          acc.y = __fadd_rn(acc.y, __fmul_rn(ws, v[j].y));
+          acc.z = __fadd_rn(acc.z, __fmul_rn(ws, v[j].z));
+          acc.w = __fadd_rn(acc.w, __fmul_rn(ws, v[j].w));
+        }
+      }
     }
     if (s != nullptr) {
       const float4 v = __ldg(reinterpret_cast<const float4*>(s + t * H + c));

@@ -20,7 +20,7 @@ namespace moe {
 namespace {
 
 struct TileInfo {
-  int cls, group, n_idx, a_row0, rows, out_row0;
+  int cls, group, n_idx, a_row0, rows, out_row0, stream;
 };
 
 __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
@@ -30,7 +30,8 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
     const uint32_t x = static_cast<uint32_t>(r.x);
     ti.group = static_cast<int>(x & 0x7FFFu);
     ti.cls = static_cast<int>((x >> 15) & 1u);
-    ti.n_idx = static_cast<int>(x >> 16);
+    ti.n_idx = static_cast<int>((x >> 16) & 0x7FFFu);
+    ti.stream = static_cast<int>(x >> 31);
     ti.a_row0 = r.y;
     ti.rows = r.z;
     ti.out_row0 = r.w;
@@ -40,6 +41,7 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
     ti.cls = 0;
     ti.group = 0;
     ti.n_idx = t / mt;
+    ti.stream = 0;
     ti.a_row0 = p.dense_a_row0 + m * kBlockM;
     ti.rows = min(kBlockM, p.dense_m - m * kBlockM);
     ti.out_row0 = m * kBlockM;
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool failed = false;
+      const uint64_t pol_stream = ptx::make_policy_evict_first();
       if (p.stall_flag != nullptr) {
         // Test hook: wait (bounded) for a flag in global memory before loading anything.
         const uint64_t t0 = ptx::globaltimer();
@@ -162,8 +165,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const int kc = kb * kBlockK;
           for (int j = 0; j < nA; ++j)
             ptx::tma_load_2d(a_dst + j * (kABoxRows * 128), tA, kc, ti.a_row0 + j * kABoxRows, fb);
-          ptx::tma_load_2d(b_dst, tB, kc, b_row0, fb);
-          if (EPI == kEpiSwiGLU) ptx::tma_load_2d(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb);
+          if (C.b_stream && ti.stream) {
+            ptx::tma_load_2d_hint(b_dst, tB, kc, b_row0, fb, pol_stream);
+            if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb, pol_stream);
+          } else {
+            ptx::tma_load_2d(b_dst, tB, kc, b_row0, fb);
+            if (EPI == kEpiSwiGLU) ptx::tma_load_2d(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb);
+          }
           ++issued;
           if (++stage == kStages) {
             stage = 0;

@@ -33,7 +33,8 @@ struct WsHeader {
   int32_t chunks_done;         // chunks processed (this run)
   int32_t pad0;
   float wnorm_max;             // max_e ||w_router[e]||_2 (upper bound)
-  int32_t pad[59];
+  int32_t band_levels[4];      // flagged tokens decided by: float sums, double sums, sequential sums, many-candidate path
+  int32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -58,11 +59,15 @@ struct GemmClass {
   int32_t b_group_rows;   // B rows per group (expert): row base of group e is e * b_group_rows
   int32_t b_up_offset;    // SwiGLU: row offset of the up half inside a group (= I), else 0
   int32_t out_cols;       // valid output columns (masks a ragged last N tile)
+  int32_t b_stream;       // 1: honour the tile's stream bit (expert weights); 0: never use the evict-first policy
+  int32_t pad_;
   int64_t out_ld;         // output row stride in elements
   void* out;              // F32: float*, SwiGLU: bf16*
 };
 
-// Tile record: x = group | (cls << 15) | (n_idx << 16); y = first A row; z = valid rows (1..128); w = first out row.
+// Tile record: x = group | (cls << 15) | (n_idx << 16) | (stream << 31); y = first A row; z = valid rows (1..128);
+// w = first out row. stream = 1 marks a tile whose B tile no other tile of the launch reads (its expert has one M
+// tile): the B loads then use an evict-first L2 policy.
 struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
@@ -93,10 +98,12 @@ struct RouteParams {
   int32_t* topk_id;           // [n][k]
   float* topk_w;              // [n][k]
   uint8_t* band_flag;         // [n] 1 when the float64 recheck ran
+  double4* band_info;         // [n] (tau, v_k, v_{k+1}, -) of tokens left to band_kernel
+  int32_t band_grid;          // CTAs of band_kernel (one per SM)
 };
 cudaError_t launch_router_norms(const uint16_t* w_router, int E, int H, float* wnorm, WsHeader* hdr,
                                 cudaStream_t stream);
-cudaError_t launch_topk(const RouteParams& p, cudaStream_t stream);
+cudaError_t launch_topk(const RouteParams& p, cudaStream_t stream);  // top-k kernel + band kernel (2 launches)
 
 struct PermuteParams {
   const int32_t* topk_id;     // [n][k]

@@ -97,15 +97,19 @@ moe_status check_device(int* device, int* num_sms) {
 
 // ------------------------------------------------------------------ workspace layout
 struct Layout {
-  size_t hdr, wnorm, logits, topk_id, topk_w, band, masks, counts, base, block_band, offsets, token_row, num_tiles,
+  size_t hdr, wnorm, logits, topk_id, topk_w, band, band_info, masks, counts, base, block_band, offsets, token_row, num_tiles,
       tiles_gu, tiles_down, xp, h, hs, y, s, total;
   int cap_gu, cap_down;
 };
 
+// Routing (router GEMM, top-k, float64 recheck) is per token, so it runs once per span of whole chunks, up to
+// kRouteSpan tokens (or max_chunk when larger); the expert-major GEMMs and the combine run per chunk.
+constexpr int kRouteSpan = 16384;
+
 struct Shape {
-  int H, E, I, k, Is, C;
-  int gu_half, gu_half_s, bn_down, bn_router;
-  int nt_gu, nt_gu_s, nt_down, nt_router;
+  int H, E, I, k, Is, C, span_cap;
+  int gu_half, gu_half_s, bn_down, bn_router_narrow, bn_router_wide;
+  int nt_gu, nt_gu_s, nt_down;
 };
 
 Shape make_shape(const moe_dims& d) {
@@ -116,14 +120,15 @@ Shape make_shape(const moe_dims& d) {
   s.k = d.top_k;
   s.Is = d.shared_inter;
   s.C = d.max_chunk;
+  s.span_cap = std::max(s.C, kRouteSpan);
   s.gu_half = (s.I % 128 == 0) ? 128 : 64;
   s.gu_half_s = (s.Is % 128 == 0) ? 128 : 64;
   s.bn_down = (s.H % 256 == 0) ? 256 : (s.H % 128 == 0 ? 128 : 64);
-  s.bn_router = std::min(256, s.E);
+  s.bn_router_narrow = std::min(64, s.E);  // short spans: narrow N tiles give more CTAs
+  s.bn_router_wide = std::min(256, s.E);   // long spans: wide N tiles read each X tile fewer times
   s.nt_gu = s.I / s.gu_half;
   s.nt_gu_s = s.Is > 0 ? s.Is / s.gu_half_s : 0;
   s.nt_down = s.H / s.bn_down;
-  s.nt_router = (s.E + s.bn_router - 1) / s.bn_router;
   return s;
 }
 
@@ -136,6 +141,7 @@ Layout make_layout(const Shape& s) {
     return at;
   };
   const size_t C = static_cast<size_t>(s.C), E = s.E, k = s.k, H = s.H, I = s.I, Is = s.Is;
+  const size_t SP = static_cast<size_t>(s.span_cap);
   const size_t R = C * k;
   const size_t nblk = (C + 31) / 32;
   const size_t mts = (C + kBlockM - 1) / kBlockM;
@@ -144,10 +150,11 @@ Layout make_layout(const Shape& s) {
   L.cap_down = static_cast<int>(routed_mt * s.nt_down + (Is > 0 ? mts * s.nt_down : 0));
   L.hdr = take(sizeof(WsHeader));
   L.wnorm = take(E * 4);
-  L.logits = take(C * E * 4);
-  L.topk_id = take(C * k * 4);
-  L.topk_w = take(C * k * 4);
-  L.band = take(C);
+  L.logits = take(SP * E * 4);
+  L.topk_id = take(SP * k * 4);
+  L.topk_w = take(SP * k * 4);
+  L.band = take(SP);
+  L.band_info = take(SP * 32);
   L.masks = take(nblk * E * 4);
   L.counts = take(nblk * E * 4);
   L.base = take(nblk * E * 4);
@@ -174,7 +181,7 @@ struct moe_plan {
   Layout lay;
   int device, num_sms;
   const void *w_router, *w_gu, *w_down, *ws_gu, *ws_down;
-  CUtensorMap tm_wr, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
+  CUtensorMap tm_wr_narrow, tm_wr_wide, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
   // descriptors of workspace-resident activations, cached per workspace pointer
   const void* ws_cached = nullptr;
   CUtensorMap tm_xp, tm_h, tm_hs;
@@ -235,16 +242,19 @@ void record_kernel(moe_plan* p, int kind, cudaStream_t st, bool before) {
   }
 }
 
+// Brackets the launches of one kernel kind (timing events when profiling) and counts the kernels launched.
 struct LaunchScope {
   moe_plan* p;
   int kind;
   cudaStream_t st;
-  LaunchScope(moe_plan* p_, int kind_, cudaStream_t st_) : p(p_), kind(kind_), st(st_) {
+  int kernels;
+  LaunchScope(moe_plan* p_, int kind_, cudaStream_t st_, int kernels_ = 1)
+      : p(p_), kind(kind_), st(st_), kernels(kernels_) {
     record_kernel(p, kind, st, true);
   }
   ~LaunchScope() {
     record_kernel(p, kind, st, false);
-    p->launches += 1;
+    p->launches += kernels;
   }
 };
 
@@ -286,7 +296,8 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   p->ws_gu = ws_gu;
   p->ws_down = ws_down;
   const Shape& s = p->sh;
-  st = encode_bf16_2d(&p->tm_wr, w_router, s.E, s.H, s.bn_router);
+  st = encode_bf16_2d(&p->tm_wr_narrow, w_router, s.E, s.H, s.bn_router_narrow);
+  if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wr_wide, w_router, s.E, s.H, s.bn_router_wide);
   if (st == MOE_OK)
     st = encode_bf16_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H, s.gu_half);
   if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
@@ -364,201 +375,220 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   }
   if (rc != MOE_OK) return rc;
 
-  const float tau_coef = static_cast<float>(s.H / 16 + 1) * 0x1p-22f;
+  // |fp32 tensor-core logit - exact| <= one ulp per 16-wide K step of a partial sum bounded by ||x|| ||w||
+  const float tau_coef = static_cast<float>(s.H / 16 + 1) * 0x1p-23f;
+  const int64_t span = static_cast<int64_t>(chunk) * std::max(1, s.span_cap / chunk);
   int64_t chunk_idx = 0;
-  for (int64_t c0 = 0; c0 < T; c0 += chunk, ++chunk_idx) {
-    const int n = static_cast<int>(std::min<int64_t>(chunk, T - c0));
-    const int nblk = (n + 31) / 32;
-    const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * s.H;
-    int32_t* ids = topk_id ? topk_id + c0 * s.k : reinterpret_cast<int32_t*>(ws + L.topk_id);
-    float* wts = topk_w ? topk_w + c0 * s.k : reinterpret_cast<float*>(ws + L.topk_w);
+  for (int64_t s0 = 0; s0 < T; s0 += span) {
+    // ---------------------------------------------------------------- routing of the span's tokens
+    const int ns = static_cast<int>(std::min<int64_t>(span, T - s0));
+    int32_t* span_ids = topk_id ? topk_id + s0 * s.k : reinterpret_cast<int32_t*>(ws + L.topk_id);
+    float* span_w = topk_w ? topk_w + s0 * s.k : reinterpret_cast<float*>(ws + L.topk_w);
 
-    // 1. router GEMM: logits [n][E] fp32
+    // 1. router GEMM: logits [ns][E] fp32
+    const bool wide = ns >= 4096;
+    const int bn_router = wide ? s.bn_router_wide : s.bn_router_narrow;
+    const int nt_router = (s.E + bn_router - 1) / bn_router;
     GemmParams g;
     memset(&g, 0, sizeof g);
     g.tmA[0] = g.tmA[1] = tm_x;
-    g.tmB[0] = g.tmB[1] = p->tm_wr;
+    g.tmB[0] = g.tmB[1] = wide ? p->tm_wr_wide : p->tm_wr_narrow;
     GemmClass rc0;
     rc0.kblocks = s.H / kBlockK;
-    rc0.n_tile = s.bn_router;
-    rc0.b_box_rows = s.bn_router;
+    rc0.n_tile = bn_router;
+    rc0.b_box_rows = bn_router;
     rc0.b_group_rows = 0;
     rc0.b_up_offset = 0;
     rc0.out_cols = s.E;
+    rc0.b_stream = 0;
     rc0.out_ld = s.E;
     rc0.out = logits;
     g.cls[0] = g.cls[1] = rc0;
     g.tiles = nullptr;
     g.num_tiles = nullptr;
-    g.dense_m = n;
-    g.dense_n_tiles = s.nt_router;
-    g.dense_a_row0 = static_cast<int32_t>(c0);
+    g.dense_m = ns;
+    g.dense_n_tiles = nt_router;
+    g.dense_a_row0 = static_cast<int32_t>(s0);
     g.err = &hdr->err;
     g.stall_flag = nullptr;
     g.timeout_ns = p->timeout_ns;
     {
-      const int tiles = ((n + kBlockM - 1) / kBlockM) * s.nt_router;
+      const int tiles = ((ns + kBlockM - 1) / kBlockM) * nt_router;
       LaunchScope ls(p, MOE_KERNEL_ROUTER, st);
       rc = cuda_status(launch_grouped_gemm(g, kEpiF32, std::min(p->num_sms, tiles), st), "router GEMM launch");
     }
     if (rc != MOE_OK) return rc;
 
-    // 2. top-k + weights
+    // 2. top-k + weights (and the float64 recheck of tokens whose fp32 selection is not certain)
     RouteParams r;
     r.logits = logits;
-    r.x = xc;
+    r.x = static_cast<const uint16_t*>(x) + s0 * s.H;
     r.w_router = static_cast<const uint16_t*>(p->w_router);
     r.wnorm = wnorm;
     r.hdr = hdr;
-    r.n = n;
+    r.n = ns;
     r.E = s.E;
     r.H = s.H;
     r.k = s.k;
     r.tau_coef = tau_coef;
-    r.topk_id = ids;
-    r.topk_w = wts;
+    r.topk_id = span_ids;
+    r.topk_w = span_w;
     r.band_flag = band;
+    r.band_info = reinterpret_cast<double4*>(ws + L.band_info);
+    r.band_grid = p->num_sms;
     {
-      LaunchScope ls(p, MOE_KERNEL_TOPK, st);
+      LaunchScope ls(p, MOE_KERNEL_TOPK, st, 2);  // top-k, then the float64 recheck of flagged tokens
       rc = cuda_status(launch_topk(r, st), "top-k launch");
     }
     if (rc != MOE_OK) return rc;
 
-    // 3-5. member lists and tile lists
-    PermuteParams q;
-    q.topk_id = ids;
-    q.band_flag = band;
-    q.x = xc;
-    q.n = n;
-    q.E = s.E;
-    q.H = s.H;
-    q.k = s.k;
-    q.nblk = nblk;
-    q.token0 = c0;
-    q.masks = reinterpret_cast<uint32_t*>(ws + L.masks);
-    q.counts = reinterpret_cast<int32_t*>(ws + L.counts);
-    q.block_band = reinterpret_cast<int32_t*>(ws + L.block_band);
-    q.base = reinterpret_cast<int32_t*>(ws + L.base);
-    q.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
-    q.offsets_out = expert_offsets ? expert_offsets + chunk_idx * (s.E + 1) : nullptr;
-    q.token_row = token_row;
-    q.row_token = row_token ? row_token + c0 * s.k : nullptr;
-    q.xp = xp;
-    q.hdr = hdr;
-    q.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu);
-    q.tiles_down = reinterpret_cast<int4*>(ws + L.tiles_down);
-    q.num_tiles = num_tiles;
-    q.cap_gu = L.cap_gu;
-    q.cap_down = L.cap_down;
-    q.nt_gu = s.nt_gu;
-    q.nt_down = s.nt_down;
-    q.nt_gu_shared = s.nt_gu_s;
-    q.nt_down_shared = s.Is > 0 ? s.nt_down : 0;
-    {
-      LaunchScope ls(p, MOE_KERNEL_COUNT, st);
-      rc = cuda_status(launch_count(q, st), "count launch");
-    }
-    if (rc != MOE_OK) return rc;
-    {
-      LaunchScope ls(p, MOE_KERNEL_SCAN, st);
-      rc = cuda_status(launch_scan_tiles(q, st), "scan launch");
-    }
-    if (rc != MOE_OK) return rc;
-    {
-      LaunchScope ls(p, MOE_KERNEL_PERMUTE, st);
-      rc = cuda_status(launch_permute(q, st), "permute launch");
-    }
-    if (rc != MOE_OK) return rc;
+    for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
+      const int n = static_cast<int>(std::min<int64_t>(chunk, T - c0));
+      const int nblk = (n + 31) / 32;
+      const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * s.H;
+      int32_t* ids = span_ids + (c0 - s0) * s.k;
+      float* wts = span_w + (c0 - s0) * s.k;
 
-    // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
-    GemmParams gu;
-    memset(&gu, 0, sizeof gu);
-    gu.tmA[0] = p->tm_xp;
-    gu.tmB[0] = p->tm_wgu;
-    GemmClass c_r;
-    c_r.kblocks = s.H / kBlockK;
-    c_r.n_tile = 2 * s.gu_half;
-    c_r.b_box_rows = s.gu_half;
-    c_r.b_group_rows = 2 * s.I;
-    c_r.b_up_offset = s.I;
-    c_r.out_cols = s.I;
-    c_r.out_ld = s.I;
-    c_r.out = h;
-    gu.cls[0] = c_r;
-    if (s.Is > 0) {
-      gu.tmA[1] = tm_x;
-      gu.tmB[1] = p->tm_wsgu;
-      GemmClass c_s;
-      c_s.kblocks = s.H / kBlockK;
-      c_s.n_tile = 2 * s.gu_half_s;
-      c_s.b_box_rows = s.gu_half_s;
-      c_s.b_group_rows = 0;
-      c_s.b_up_offset = s.Is;
-      c_s.out_cols = s.Is;
-      c_s.out_ld = s.Is;
-      c_s.out = hs;
-      gu.cls[1] = c_s;
-    } else {
-      gu.tmA[1] = gu.tmA[0];
-      gu.tmB[1] = gu.tmB[0];
-      gu.cls[1] = c_r;
-    }
-    gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu);
-    gu.num_tiles = num_tiles;
-    gu.err = &hdr->err;
-    gu.timeout_ns = p->timeout_ns;
-    {
-      LaunchScope ls(p, MOE_KERNEL_GATE_UP, st);
-      rc = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st), "gate/up launch");
-    }
-    if (rc != MOE_OK) return rc;
+      // 3-5. member lists and tile lists
+      PermuteParams q;
+      q.topk_id = ids;
+      q.band_flag = band + (c0 - s0);
+      q.x = xc;
+      q.n = n;
+      q.E = s.E;
+      q.H = s.H;
+      q.k = s.k;
+      q.nblk = nblk;
+      q.token0 = c0;
+      q.masks = reinterpret_cast<uint32_t*>(ws + L.masks);
+      q.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+      q.block_band = reinterpret_cast<int32_t*>(ws + L.block_band);
+      q.base = reinterpret_cast<int32_t*>(ws + L.base);
+      q.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+      q.offsets_out = expert_offsets ? expert_offsets + chunk_idx * (s.E + 1) : nullptr;
+      q.token_row = token_row;
+      q.row_token = row_token ? row_token + c0 * s.k : nullptr;
+      q.xp = xp;
+      q.hdr = hdr;
+      q.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu);
+      q.tiles_down = reinterpret_cast<int4*>(ws + L.tiles_down);
+      q.num_tiles = num_tiles;
+      q.cap_gu = L.cap_gu;
+      q.cap_down = L.cap_down;
+      q.nt_gu = s.nt_gu;
+      q.nt_down = s.nt_down;
+      q.nt_gu_shared = s.nt_gu_s;
+      q.nt_down_shared = s.Is > 0 ? s.nt_down : 0;
+      {
+        LaunchScope ls(p, MOE_KERNEL_COUNT, st);
+        rc = cuda_status(launch_count(q, st), "count launch");
+      }
+      if (rc != MOE_OK) return rc;
+      {
+        LaunchScope ls(p, MOE_KERNEL_SCAN, st);
+        rc = cuda_status(launch_scan_tiles(q, st), "scan launch");
+      }
+      if (rc != MOE_OK) return rc;
+      {
+        LaunchScope ls(p, MOE_KERNEL_PERMUTE, st);
+        rc = cuda_status(launch_permute(q, st), "permute launch");
+      }
+      if (rc != MOE_OK) return rc;
 
-    // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s)
-    GemmParams dn;
-    memset(&dn, 0, sizeof dn);
-    dn.tmA[0] = p->tm_h;
-    dn.tmB[0] = p->tm_wdown;
-    GemmClass d_r;
-    d_r.kblocks = s.I / kBlockK;
-    d_r.n_tile = s.bn_down;
-    d_r.b_box_rows = s.bn_down;
-    d_r.b_group_rows = s.H;
-    d_r.b_up_offset = 0;
-    d_r.out_cols = s.H;
-    d_r.out_ld = s.H;
-    d_r.out = y;
-    dn.cls[0] = d_r;
-    if (s.Is > 0) {
-      dn.tmA[1] = p->tm_hs;
-      dn.tmB[1] = p->tm_wsdown;
-      GemmClass d_s = d_r;
-      d_s.kblocks = s.Is / kBlockK;
-      d_s.b_group_rows = 0;
-      d_s.out = sbuf;
-      dn.cls[1] = d_s;
-    } else {
-      dn.tmA[1] = dn.tmA[0];
-      dn.tmB[1] = dn.tmB[0];
-      dn.cls[1] = d_r;
-    }
-    dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down);
-    dn.num_tiles = num_tiles + 1;
-    dn.err = &hdr->err;
-    dn.timeout_ns = p->timeout_ns;
-    {
-      LaunchScope ls(p, MOE_KERNEL_DOWN, st);
-      rc = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
-    }
-    if (rc != MOE_OK) return rc;
+      // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
+      GemmParams gu;
+      memset(&gu, 0, sizeof gu);
+      gu.tmA[0] = p->tm_xp;
+      gu.tmB[0] = p->tm_wgu;
+      GemmClass c_r;
+      c_r.kblocks = s.H / kBlockK;
+      c_r.n_tile = 2 * s.gu_half;
+      c_r.b_box_rows = s.gu_half;
+      c_r.b_group_rows = 2 * s.I;
+      c_r.b_up_offset = s.I;
+      c_r.out_cols = s.I;
+      c_r.b_stream = 1;
+      c_r.out_ld = s.I;
+      c_r.out = h;
+      gu.cls[0] = c_r;
+      if (s.Is > 0) {
+        gu.tmA[1] = tm_x;
+        gu.tmB[1] = p->tm_wsgu;
+        GemmClass c_s;
+        c_s.kblocks = s.H / kBlockK;
+        c_s.n_tile = 2 * s.gu_half_s;
+        c_s.b_box_rows = s.gu_half_s;
+        c_s.b_group_rows = 0;
+        c_s.b_up_offset = s.Is;
+        c_s.out_cols = s.Is;
+        c_s.b_stream = 0;
+        c_s.out_ld = s.Is;
+        c_s.out = hs;
+        gu.cls[1] = c_s;
+      } else {
+        gu.tmA[1] = gu.tmA[0];
+        gu.tmB[1] = gu.tmB[0];
+        gu.cls[1] = c_r;
+      }
+      gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu);
+      gu.num_tiles = num_tiles;
+      gu.err = &hdr->err;
+      gu.timeout_ns = p->timeout_ns;
+      {
+        LaunchScope ls(p, MOE_KERNEL_GATE_UP, st);
+        rc = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st), "gate/up launch");
+      }
+      if (rc != MOE_OK) return rc;
 
-    // 8. canonical combine
-    {
-      LaunchScope ls(p, MOE_KERNEL_COMBINE, st);
-      rc = cuda_status(launch_combine(y, wts, token_row, s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
-                                      static_cast<uint16_t*>(out) + c0 * s.H, st),
-                       "combine launch");
+      // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s)
+      GemmParams dn;
+      memset(&dn, 0, sizeof dn);
+      dn.tmA[0] = p->tm_h;
+      dn.tmB[0] = p->tm_wdown;
+      GemmClass d_r;
+      d_r.kblocks = s.I / kBlockK;
+      d_r.n_tile = s.bn_down;
+      d_r.b_box_rows = s.bn_down;
+      d_r.b_group_rows = s.H;
+      d_r.b_up_offset = 0;
+      d_r.out_cols = s.H;
+      d_r.b_stream = 1;
+      d_r.out_ld = s.H;
+      d_r.out = y;
+      dn.cls[0] = d_r;
+      if (s.Is > 0) {
+        dn.tmA[1] = p->tm_hs;
+        dn.tmB[1] = p->tm_wsdown;
+        GemmClass d_s = d_r;
+        d_s.kblocks = s.Is / kBlockK;
+        d_s.b_group_rows = 0;
+        d_s.b_stream = 0;
+        d_s.out = sbuf;
+        dn.cls[1] = d_s;
+      } else {
+        dn.tmA[1] = dn.tmA[0];
+        dn.tmB[1] = dn.tmB[0];
+        dn.cls[1] = d_r;
+      }
+      dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down);
+      dn.num_tiles = num_tiles + 1;
+      dn.err = &hdr->err;
+      dn.timeout_ns = p->timeout_ns;
+      {
+        LaunchScope ls(p, MOE_KERNEL_DOWN, st);
+        rc = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
+      }
+      if (rc != MOE_OK) return rc;
+
+      // 8. canonical combine
+      {
+        LaunchScope ls(p, MOE_KERNEL_COMBINE, st);
+        rc = cuda_status(launch_combine(y, wts, token_row, s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
+                                        static_cast<uint16_t*>(out) + c0 * s.H, st),
+                         "combine launch");
+      }
+      if (rc != MOE_OK) return rc;
     }
-    if (rc != MOE_OK) return rc;
   }
   return MOE_OK;
 }
@@ -591,13 +621,15 @@ moe_status moe_prefill_check(void* workspace, moe_stream_t stream) {
   return fail(MOE_ERR_DEVICE_BOUNDS, "device bounds check failed (site %d, index %d, word 0x%08x)", site, block, err);
 }
 
-moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* chunks, int32_t* band_tokens) {
+moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* stats, int32_t n_stats) {
   if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  if (n_stats < 0 || (n_stats > 0 && !stats)) return fail(MOE_ERR_INVALID_ARG, "stats array missing");
   CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
   WsHeader hdr;
   CUDA_TRY(cudaMemcpy(&hdr, workspace, sizeof hdr, cudaMemcpyDeviceToHost));
-  if (chunks) *chunks = hdr.chunks_done;
-  if (band_tokens) *band_tokens = hdr.band_tokens;
+  const int32_t all[MOE_STATS_COUNT] = {hdr.chunks_done,     hdr.band_tokens,     hdr.band_levels[0],
+                                        hdr.band_levels[1], hdr.band_levels[2], hdr.band_levels[3]};
+  for (int32_t i = 0; i < n_stats; ++i) stats[i] = i < MOE_STATS_COUNT ? all[i] : 0;
   return MOE_OK;
 }
 
@@ -671,6 +703,7 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
   cl.kblocks = k_dim / kBlockK;
   cl.b_group_rows = 0;
   cl.out_cols = n;
+  cl.b_stream = 0;
   cl.out_ld = n;
   cl.out = c;
   int n_tiles;

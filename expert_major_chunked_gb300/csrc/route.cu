@@ -9,6 +9,7 @@
 
 #include <cuda_bf16.h>
 #include <cfloat>
+#include <algorithm>
 #include <climits>
 
 namespace moe {
@@ -68,6 +69,130 @@ __device__ double exact_logit(const uint16_t* x, const uint16_t* w, int H) {
   return acc;
 }
 
+// Scratch of one warp for the float64 recheck of the ambiguous places of one token.
+constexpr int kMaxCand = 64;
+struct BandScratch {
+  double val[kMaxCand];
+  double sabs[kMaxCand];
+  int32_t id[kMaxCand];
+  int32_t chosen[kMaxCand];
+};
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// bf16 -> double by bit manipulation on the integer pipe (GB300's fp64 pipe is 1/64 of fp32): exact for every bf16.
+__device__ __forceinline__ double bf16_bits_to_double(uint32_t b16) {
+  const uint32_t sign = b16 >> 15, ex = (b16 >> 7) & 0xFFu, man = b16 & 0x7Fu;
+  if (ex == 0u) return static_cast<double>(__uint_as_float(b16 << 16));  // zero / subnormal: rare, exact cast
+  if (ex == 0xFFu) return static_cast<double>(__uint_as_float(b16 << 16));
+  const uint64_t bits = (static_cast<uint64_t>(sign) << 63) | (static_cast<uint64_t>(ex - 127u + 1023u) << 52) |
+                        (static_cast<uint64_t>(man) << 45);
+  return __longlong_as_double(static_cast<long long>(bits));
+}
+
+template <typename T>
+__device__ __forceinline__ T bf16_as(uint32_t b16);
+template <>
+__device__ __forceinline__ float bf16_as<float>(uint32_t b16) {
+  return __uint_as_float(b16 << 16);
+}
+template <>
+__device__ __forceinline__ double bf16_as<double>(uint32_t b16) {
+  return bf16_bits_to_double(b16);
+}
+
+// Logits of the candidates in precision T (float or double), the whole warp on one candidate at a time. Lane l
+// owns elements 256 m + 8 l + j (j < 8, m = 0, 1, ...); slot j keeps its own running sum over m (fused multiply-
+// add of exact products), the 8 slot sums are added pairwise, then a butterfly adds the 32 lanes. Every bf16 x bf16
+// product is exact in float and in double, so each value differs from the exact dot product by at most
+// depth * u * S, depth = ceil(H/256) + 8 roundings on any path and S = sum |x_i w_i| (returned in B.sabs as a
+// float sum, which the bound inflates by 1%). All loads of a row segment are issued before its arithmetic.
+template <typename T>
+__device__ void band_values(BandScratch& B, int ncand, const uint16_t* xrow, const uint16_t* w_router, int H,
+                            int lane, bool with_sabs) {
+  for (int c = 0; c < ncand; ++c) {
+    const uint16_t* wrow = w_router + static_cast<int64_t>(B.id[c]) * H;
+    T acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = T(0);
+    float sab = 0.0f;
+    for (int i0 = lane * 8; i0 < H; i0 += 256 * 8) {
+      uint4 xa[8], wa[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int i = i0 + 256 * m;
+        if (i < H) {
+          xa[m] = __ldg(reinterpret_cast<const uint4*>(xrow + i));
+          wa[m] = __ldg(reinterpret_cast<const uint4*>(wrow + i));
+        } else {
+          xa[m] = make_uint4(0, 0, 0, 0);
+          wa[m] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const uint32_t aw[4] = {xa[m].x, xa[m].y, xa[m].z, xa[m].w};
+        const uint32_t bw[4] = {wa[m].x, wa[m].y, wa[m].z, wa[m].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const T x0 = bf16_as<T>(aw[q] & 0xFFFFu), x1 = bf16_as<T>(aw[q] >> 16);
+          const T w0 = bf16_as<T>(bw[q] & 0xFFFFu), w1 = bf16_as<T>(bw[q] >> 16);
+          acc[2 * q] = fma(x0, w0, acc[2 * q]);
+          acc[2 * q + 1] = fma(x1, w1, acc[2 * q + 1]);
+          if (with_sabs) {
+            sab += fabsf(bf16_lo(aw[q]) * bf16_lo(bw[q]));
+            sab += fabsf(bf16_hi(aw[q]) * bf16_hi(bw[q]));
+          }
+        }
+      }
+    }
+    T v = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (with_sabs) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sab += __shfl_xor_sync(0xffffffffu, sab, o);
+    }
+    if (lane == 0) {
+      B.val[c] = static_cast<double>(v);
+      if (with_sabs) B.sabs[c] = static_cast<double>(sab) * 1.01;
+    }
+  }
+  __syncwarp();
+}
+
+// Lane 0 only: marks the `need` best candidates by (value desc, id asc) in B.chosen. When beta >= 0 the values are
+// estimates within beta of the sequential float64 sums (per candidate: beta_c = bound * S_c, bound passed in), and
+// the function returns 1 only when the choice provably equals the choice on those sums: the worst chosen estimate
+// beats the best unchosen one by more than twice the largest beta.
+__device__ int band_select(BandScratch& B, int ncand, int need, double bound) {
+  for (int c = 0; c < ncand; ++c) B.chosen[c] = 0;
+  double worst_in = DBL_MAX;
+  for (int r = 0; r < need; ++r) {
+    int best = -1;
+    for (int c = 0; c < ncand; ++c) {
+      if (B.chosen[c]) continue;
+      if (best < 0 || B.val[c] > B.val[best] || (B.val[c] == B.val[best] && B.id[c] < B.id[best])) best = c;
+    }
+    if (best < 0) break;
+    B.chosen[best] = 1;
+    worst_in = fmin(worst_in, B.val[best]);
+  }
+  if (bound < 0.0 || need <= 0 || need >= ncand) return 1;
+  double best_out = -DBL_MAX, smax = 0.0;
+  for (int c = 0; c < ncand; ++c) {
+    smax = fmax(smax, B.sabs[c]);
+    if (!B.chosen[c]) best_out = fmax(best_out, B.val[c]);
+  }
+  // products that underflow float contribute at most 2^-149 each: an absolute term covers them
+  const double beta = bound * smax + 0x1p-140;
+  return (worst_in - best_out > 2.0 * beta) ? 1 : 0;
+}
+
 __global__ void __launch_bounds__(256) router_norms_kernel(const uint16_t* w, int E, int H, float* wnorm,
                                                            WsHeader* hdr) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -76,6 +201,7 @@ __global__ void __launch_bounds__(256) router_norms_kernel(const uint16_t* w, in
     hdr->err = 0;
     hdr->band_tokens = 0;
     hdr->chunks_done = 0;
+    for (int i = 0; i < 4; ++i) hdr->band_levels[i] = 0;
   }
   if (e >= E) return;
   const float ss = row_sumsq(w + static_cast<int64_t>(e) * H, H, lane);
@@ -83,32 +209,24 @@ __global__ void __launch_bounds__(256) router_norms_kernel(const uint16_t* w, in
   if (lane == 0) wnorm[e] = sqrtf(ss) * 1.001f;
 }
 
-// Top-k of one token per warp. Selection follows the float64 logits: the fp32 tensor-core logits are trusted only
-// when the gap between the k-th and (k+1)-th value exceeds twice the error bound tau; otherwise the experts inside
-// the ambiguity band are recomputed in float64 (the same sum the CPU reference uses) and decide the last places.
+// Top-k selection of one token per warp. The selection follows the float64 logits: the fp32 tensor-core logits are
+// trusted only when the gap between the k-th and (k+1)-th largest exceeds twice the error bound tau; otherwise the
+// token is flagged and band_kernel decides its last places (see there). Both kernels write the outputs the same way.
 template <int EPL>
-__global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= p.n) return;
-  const int E = p.E, k = p.k, H = p.H;
-  const float* lrow = p.logits + static_cast<int64_t>(t) * E;
-  float v[EPL];
+__device__ __forceinline__ void load_logits(const float* lrow, int E, int lane, float (&v)[EPL]) {
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = j * 32 + lane;
     v[j] = (e < E) ? lrow[e] : -FLT_MAX;
   }
-  const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
-  const float xnorm = sqrtf(row_sumsq(xrow, H, lane)) * 1.001f;
-  float wm = 0.0f;
-  for (int e = lane; e < E; e += 32) wm = fmaxf(wm, p.wnorm[e]);
-  wm = warp_max(wm);
-  const double tau = static_cast<double>(p.tau_coef) * static_cast<double>(xnorm) * static_cast<double>(wm);
+}
 
-  // (k+1) rounds of warp argmax by (value desc, id asc)
-  uint32_t sel = 0;
-  float vk = 0.0f, vk1 = -FLT_MAX;
+// (rounds) rounds of warp argmax by (value desc, id asc); marks the first k in *sel, returns the k-th and (k+1)-th.
+template <int EPL>
+__device__ __forceinline__ void select_top(const float (&v)[EPL], int E, int k, int lane, uint32_t* sel, float* vk,
+                                           float* vk1) {
+  uint32_t s = 0;
+  float a = 0.0f, b = -FLT_MAX;
   const int rounds = (k + 1 < E) ? k + 1 : E;
   for (int r = 0; r < rounds; ++r) {
     float bv = -FLT_MAX;
@@ -116,7 +234,7 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
       const int e = j * 32 + lane;
-      if (e < E && !((sel >> j) & 1u) && (bid == INT_MAX || v[j] > bv)) {
+      if (e < E && !((s >> j) & 1u) && (bid == INT_MAX || v[j] > bv)) {
         bv = v[j];
         bid = e;
       }
@@ -131,64 +249,23 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
       }
     }
     if (r < k) {
-      if (bid != INT_MAX && (bid & 31) == lane) sel |= 1u << (bid >> 5);
-      if (r == k - 1) vk = bv;
+      if (bid != INT_MAX && (bid & 31) == lane) s |= 1u << (bid >> 5);
+      if (r == k - 1) a = bv;
     } else {
-      vk1 = bv;
+      b = bv;
     }
   }
+  *sel = s;
+  *vk = a;
+  *vk1 = b;
+}
 
-  bool band = false;
-  if (k < E) band = !(static_cast<double>(vk) - static_cast<double>(vk1) > 2.0 * tau);
-  if (band) {
-    const double hi = static_cast<double>(vk1) + 2.0 * tau;  // above: certainly among the k largest
-    const double lo = static_cast<double>(vk) - 2.0 * tau;   // below: certainly not
-    uint32_t sure = 0, cand = 0;
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-      const int e = j * 32 + lane;
-      if (e >= E) continue;
-      const double dv = static_cast<double>(v[j]);
-      if (dv > hi)
-        sure |= 1u << j;
-      else if (dv >= lo)
-        cand |= 1u << j;
-    }
-    const int need = k - warp_sum_i(__popc(sure));
-    double d[EPL];
-#pragma unroll
-    for (int j = 0; j < EPL; ++j) {
-      d[j] = 0.0;
-      if ((cand >> j) & 1u) d[j] = exact_logit(xrow, p.w_router + static_cast<int64_t>(j * 32 + lane) * H, H);
-    }
-    uint32_t chosen = 0;
-    for (int r = 0; r < need; ++r) {
-      double bv = -DBL_MAX;
-      int bid = INT_MAX;
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        if (((cand & ~chosen) >> j) & 1u) {
-          if (bid == INT_MAX || d[j] > bv) {
-            bv = d[j];
-            bid = j * 32 + lane;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-        if (ov > bv || (ov == bv && oid < bid)) {
-          bv = ov;
-          bid = oid;
-        }
-      }
-      if (bid != INT_MAX && (bid & 31) == lane) chosen |= 1u << (bid >> 5);
-    }
-    sel = sure | chosen;
-  }
-
-  // weights: softmax over the selected fp32 logits (= full softmax renormalised over the selection)
+// Ids of the selected experts in ascending order and their weights: softmax over the selected fp32 logits (equal to
+// the full softmax renormalised over the selection).
+template <int EPL>
+__device__ __forceinline__ void write_selection(const RouteParams& p, int t, int lane, uint32_t sel,
+                                                const float (&v)[EPL]) {
+  const int k = p.k;
   float fmax_sel = -FLT_MAX;
 #pragma unroll
   for (int j = 0; j < EPL; ++j)
@@ -219,7 +296,7 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
     }
     pos += __popc(b);
   }
-  if (pos < k) {
+  if (pos != k) {
     // cannot happen for finite logits; keep every slot a valid expert id so later kernels stay in bounds
     if (lane >= pos && lane < k) {
       ids_out[lane] = 0;
@@ -227,36 +304,215 @@ __global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
     }
     if (lane == 0) atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
   }
-  if (lane == 0) p.band_flag[t] = band ? 1 : 0;
 }
 
-// Histogram of a block of 32 tokens: for every expert, a bit mask of the block's tokens that selected it.
-__global__ void __launch_bounds__(256) count_kernel(PermuteParams p) {
-  __shared__ int32_t ids[32 * 32];
-  const int b = blockIdx.x;
-  const int t0 = b * 32;
-  const int nt = min(32, p.n - t0);
-  const int k = p.k, E = p.E;
-  for (int i = threadIdx.x; i < 32 * k; i += blockDim.x) {
-    const int tok = i / k;
-    ids[i] = (tok < nt) ? p.topk_id[static_cast<int64_t>(t0 + tok) * k + (i % k)] : -1;
+// Candidates of a flagged token: experts whose fp32 logit lies in [v_k - 2 tau, v_{k+1} + 2 tau]. Those above the
+// band are certainly among the k largest float64 logits, those below certainly not. Fills B.id in ascending id order
+// (when at most kMaxCand) and returns the number of candidates; *need = places left for them.
+template <int EPL>
+__device__ __forceinline__ int band_candidates(const float (&v)[EPL], int E, int k, int lane, double tau, double vk,
+                                               double vk1, BandScratch& B, uint32_t* sure_out, uint32_t* cand_out,
+                                               int (&cidx)[EPL], int* need) {
+  const double hi = vk1 + 2.0 * tau;
+  const double lo = vk - 2.0 * tau;
+  uint32_t sure = 0, cand = 0;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const int e = j * 32 + lane;
+    if (e >= E) continue;
+    const double dv = static_cast<double>(v[j]);
+    if (dv > hi)
+      sure |= 1u << j;
+    else if (dv >= lo)
+      cand |= 1u << j;
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    uint32_t m = 0;
-    for (int tok = 0; tok < nt; ++tok) {
-      const int32_t* r = ids + tok * k;
-      for (int s = 0; s < k; ++s)
-        if (r[s] == e) m |= 1u << tok;
+  *need = k - warp_sum_i(__popc(sure));
+  int ncand = 0;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) {
+    const bool mine = (cand >> j) & 1u;
+    const uint32_t b = __ballot_sync(0xffffffffu, mine);
+    cidx[j] = ncand + __popc(b & ((1u << lane) - 1u));
+    ncand += __popc(b);
+  }
+  if (ncand <= kMaxCand) {
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if ((cand >> j) & 1u) B.id[cidx[j]] = j * 32 + lane;
+  }
+  __syncwarp();
+  *sure_out = sure;
+  *cand_out = cand;
+  return ncand;
+}
+
+template <int EPL>
+__device__ __forceinline__ uint32_t chosen_mask(const BandScratch& B, uint32_t cand, const int (&cidx)[EPL]) {
+  uint32_t chosen = 0;
+#pragma unroll
+  for (int j = 0; j < EPL; ++j)
+    if (((cand >> j) & 1u) && B.chosen[cidx[j]]) chosen |= 1u << j;
+  return chosen;
+}
+
+// Bounds of the band estimates: an estimate summed with tree depth d is within d u S of the exact dot product and the
+// sequential float64 sum within (H - 1) u64 S of it (S = sum |x_i w_i|); 1% covers the rounding of S itself.
+__device__ __forceinline__ double band_bound(int H, double u) {
+  const double depth = static_cast<double>((H + 255) / 256 + 8);
+  return 1.01 * (depth * u + static_cast<double>(H) * 0x1p-53);
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256, 2) topk_kernel(RouteParams p) {
+  __shared__ BandScratch band_scratch[8];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= p.n) return;
+  const int E = p.E, k = p.k, H = p.H;
+  float v[EPL];
+  load_logits(p.logits + static_cast<int64_t>(t) * E, E, lane, v);
+  const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
+  const float xnorm = sqrtf(row_sumsq(xrow, H, lane)) * 1.001f;
+  float wm = 0.0f;
+  for (int e = lane; e < E; e += 32) wm = fmaxf(wm, p.wnorm[e]);
+  wm = warp_max(wm);
+  const double tau = static_cast<double>(p.tau_coef) * static_cast<double>(xnorm) * static_cast<double>(wm);
+  uint32_t sel;
+  float vk, vk1;
+  select_top(v, E, k, lane, &sel, &vk, &vk1);
+  int flag = 0;
+  if ((k < E) && !(static_cast<double>(vk) - static_cast<double>(vk1) > 2.0 * tau)) {
+    // not certain: try to decide the last places on float sums of the exact products
+    BandScratch& B = band_scratch[warp];
+    uint32_t sure, cand;
+    int cidx[EPL];
+    int need;
+    const int ncand = band_candidates(v, E, k, lane, tau, vk, vk1, B, &sure, &cand, cidx, &need);
+    int certified = 0;
+    if (ncand <= kMaxCand) {
+      band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);
+      if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-24));
+      certified = __shfl_sync(0xffffffffu, certified, 0);
     }
-    p.masks[static_cast<int64_t>(b) * E + e] = m;
-    p.counts[static_cast<int64_t>(b) * E + e] = __popc(m);
+    if (certified) {
+      sel = sure | chosen_mask(B, cand, cidx);
+      flag = 1;
+      if (lane == 0) atomicAdd(&p.hdr->band_levels[0], 1);  // diagnostic counter only
+    } else {
+      flag = 2;  // band_kernel decides this token
+      if (lane == 0) p.band_info[t] = make_double4(tau, static_cast<double>(vk), static_cast<double>(vk1), 0.0);
+    }
+    __syncwarp();
   }
-  if (threadIdx.x < 32) {
-    const int f = (static_cast<int>(threadIdx.x) < nt) ? p.band_flag[t0 + threadIdx.x] : 0;
-    const uint32_t bb = __ballot_sync(0xffffffffu, f != 0);
-    if (threadIdx.x == 0) p.block_band[b] = __popc(bb);
+  if (flag != 2) write_selection(p, t, lane, sel, v);
+  if (lane == 0) p.band_flag[t] = static_cast<uint8_t>(flag);
+}
+
+// Tokens the float sums could not decide (flag 2), on double sums and, when those cannot separate the last places
+// either, on the sequential float64 sums themselves (the reference definition, bit for bit). A grid of one CTA per
+// SM strides over the chunk's tokens.
+template <int EPL>
+__global__ void __launch_bounds__(256) band_kernel(RouteParams p) {
+  __shared__ BandScratch band_scratch[8];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int E = p.E, k = p.k, H = p.H;
+  for (int t = blockIdx.x * 8 + warp; t < p.n; t += gridDim.x * 8) {
+    if (p.band_flag[t] != 2) continue;
+    float v[EPL];
+    load_logits(p.logits + static_cast<int64_t>(t) * E, E, lane, v);
+    const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
+    const double4 bi = p.band_info[t];
+    BandScratch& B = band_scratch[warp];
+    uint32_t sure, cand;
+    int cidx[EPL];
+    int need;
+    const int ncand = band_candidates(v, E, k, lane, bi.x, bi.y, bi.z, B, &sure, &cand, cidx, &need);
+    uint32_t chosen = 0;
+    if (ncand <= kMaxCand) {
+      band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);  // S for the bounds
+      band_values<double>(B, ncand, xrow, p.w_router, H, lane, false);
+      int certified = 0;
+      if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-53));
+      certified = __shfl_sync(0xffffffffu, certified, 0);
+      int level = 1;
+      if (!certified) {
+        level = 2;
+        for (int c = lane; c < ncand; c += 32)
+          B.val[c] = exact_logit(xrow, p.w_router + static_cast<int64_t>(B.id[c]) * H, H);
+        __syncwarp();
+        if (lane == 0) band_select(B, ncand, need, -1.0);
+      }
+      __syncwarp();
+      if (lane == 0) atomicAdd(&p.hdr->band_levels[level], 1);  // diagnostic counter only
+      chosen = chosen_mask(B, cand, cidx);
+    } else {
+      // more candidates than the scratch list holds (e.g. all-zero tokens): sequential float64 sums per lane
+      if (lane == 0) atomicAdd(&p.hdr->band_levels[3], 1);  // diagnostic counter only
+      double d[EPL];
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) {
+        d[j] = 0.0;
+        if ((cand >> j) & 1u) d[j] = exact_logit(xrow, p.w_router + static_cast<int64_t>(j * 32 + lane) * H, H);
+      }
+      for (int r = 0; r < need; ++r) {
+        double bv = -DBL_MAX;
+        int bid = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < EPL; ++j) {
+          if (((cand & ~chosen) >> j) & 1u) {
+            if (bid == INT_MAX || d[j] > bv) {
+              bv = d[j];
+              bid = j * 32 + lane;
+            }
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+          const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+          if (ov > bv || (ov == bv && oid < bid)) {
+            bv = ov;
+            bid = oid;
+          }
+        }
+        if (bid != INT_MAX && (bid & 31) == lane) chosen |= 1u << (bid >> 5);
+      }
+    }
+    write_selection(p, t, lane, sure | chosen, v);
+    __syncwarp();
   }
+}
+
+// Histogram of 32-token blocks, one warp per block: for every expert, the bit mask of the block's tokens that
+// selected it. Slot by slot, __match_any_sync groups the lanes (tokens) that picked the same expert and the
+// group's lowest lane ORs the group into that expert's mask; the experts of one slot are distinct writers, so the
+// masks need no atomics and do not depend on timing.
+constexpr int kCountWarps = 8;
+__global__ void __launch_bounds__(kCountWarps * 32) count_kernel(PermuteParams p) {
+  extern __shared__ uint32_t cmask[];  // [kCountWarps][E]
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int E = p.E, k = p.k;
+  const int b = blockIdx.x * kCountWarps + warp;
+  if (b >= p.nblk) return;
+  uint32_t* m = cmask + warp * E;
+  for (int e = lane; e < E; e += 32) m[e] = 0;
+  __syncwarp();
+  const int t = b * 32 + lane;
+  const bool valid = t < p.n;
+  for (int s = 0; s < k; ++s) {
+    int e = valid ? p.topk_id[static_cast<int64_t>(t) * k + s] : -1;
+    if (e >= E) e = -1;
+    const uint32_t g = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(g) - 1) m[e] |= g;
+    __syncwarp();
+  }
+  for (int e = lane; e < E; e += 32) {
+    const uint32_t v = m[e];
+    p.masks[static_cast<int64_t>(b) * E + e] = v;
+    p.counts[static_cast<int64_t>(b) * E + e] = __popc(v);
+  }
+  const uint32_t bb = __ballot_sync(0xffffffffu, valid && p.band_flag[valid ? t : 0] != 0);
+  if (lane == 0) p.block_band[b] = __popc(bb);
 }
 
 // Exclusive scan across a block of 1024 threads; returns the thread's exclusive prefix, *total gets the sum.
@@ -295,19 +551,34 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(PermuteParams p) {
   __shared__ int sm[33];
   const int e = threadIdx.x;
   const int E = p.E, nblk = p.nblk;
+  // pass 1: per-expert totals; thread e reads column e of counts[nblk][E] (coalesced across the warp), 16 blocks
+  // per batch so that 16 loads are in flight per thread
   int total = 0;
-  if (e < E)
-    for (int b = 0; b < nblk; ++b) total += p.counts[static_cast<int64_t>(b) * E + e];
+  if (e < E) {
+    for (int b0 = 0; b0 < nblk; b0 += 16) {
+      int c[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? p.counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) total += c[j];
+    }
+  }
   int R = 0;
   const int off = block_exclusive_scan(e < E ? total : 0, &R, sm);
   if (e < E) {
     p.offsets[e] = off;
     if (p.offsets_out) p.offsets_out[e] = off;
+    // pass 2: row base of every (block, expert)
     int run = off;
-    for (int b = 0; b < nblk; ++b) {
-      const int64_t i = static_cast<int64_t>(b) * E + e;
-      p.base[i] = run;
-      run += p.counts[i];
+    for (int b0 = 0; b0 < nblk; b0 += 16) {
+      int c[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? p.counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        if (b0 + j < nblk) p.base[static_cast<int64_t>(b0 + j) * E + e] = run;
+        run += c[j];
+      }
     }
   }
   if (e == 0) {
@@ -323,14 +594,16 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(PermuteParams p) {
   const int n_dn_all = n_dn + (p.nt_down_shared > 0 ? mts * p.nt_down_shared : 0);
   const bool fits = n_gu_all <= p.cap_gu && n_dn_all <= p.cap_down;
   if (fits && e < E) {
+    // an expert with a single M tile is the only reader of its weight tiles: mark them for streaming
+    const int stream = (mt == 1) ? static_cast<int>(1u << 31) : 0;
     for (int nn = 0; nn < p.nt_gu; ++nn)
       for (int m = 0; m < mt; ++m)
-        p.tiles_gu[gu_base + nn * mt + m] =
-            make_int4(e | (nn << 16), off + m * kBlockM, min(kBlockM, total - m * kBlockM), off + m * kBlockM);
+        p.tiles_gu[gu_base + nn * mt + m] = make_int4(e | (nn << 16) | stream, off + m * kBlockM,
+                                                      min(kBlockM, total - m * kBlockM), off + m * kBlockM);
     for (int nn = 0; nn < p.nt_down; ++nn)
       for (int m = 0; m < mt; ++m)
-        p.tiles_down[dn_base + nn * mt + m] =
-            make_int4(e | (nn << 16), off + m * kBlockM, min(kBlockM, total - m * kBlockM), off + m * kBlockM);
+        p.tiles_down[dn_base + nn * mt + m] = make_int4(e | (nn << 16) | stream, off + m * kBlockM,
+                                                        min(kBlockM, total - m * kBlockM), off + m * kBlockM);
   }
   if (fits) {
     // shared expert (class 1): gate/up reads the chunk's rows of X, down reads the shared h rows
@@ -349,47 +622,47 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(PermuteParams p) {
     p.num_tiles[0] = fits ? n_gu_all : 0;
     p.num_tiles[1] = fits ? n_dn_all : 0;
     if (!fits) atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, 0));
-    int band = 0;
-    for (int b = 0; b < nblk; ++b) band += p.block_band[b];
-    p.hdr->band_tokens += band;
     p.hdr->chunks_done += 1;
   }
+  int nb_band = 0;
+  for (int b = threadIdx.x; b < nblk; b += blockDim.x) nb_band += p.block_band[b];
+  int band_total = 0;
+  (void)block_exclusive_scan(nb_band, &band_total, sm);
+  if (threadIdx.x == 0) p.hdr->band_tokens += band_total;
 }
 
 // Row index of every (token, slot), the inverse map, and the gathered copy of X in expert-major row order.
-__global__ void __launch_bounds__(256) permute_kernel(PermuteParams p) {
-  const int b = blockIdx.x;
+// One warp per token: lane s < k computes the row of slot s from the block's row base of its expert plus the
+// number of earlier tokens of the block that selected the same expert (popcount of the mask below the token).
+constexpr int kPermuteWarps = 8;
+__global__ void __launch_bounds__(kPermuteWarps * 32) permute_kernel(PermuteParams p) {
+  __shared__ int32_t rows_sm[kPermuteWarps][32];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int t0 = b * 32;
-  const int nt = min(32, p.n - t0);
+  const int t = blockIdx.x * kPermuteWarps + warp;
+  if (t >= p.n) return;
   const int k = p.k, E = p.E, H = p.H;
-  __shared__ int32_t rows_sm[8][32];
-  for (int i = warp; i < nt; i += 8) {
-    const int t = t0 + i;
-    if (lane < k) {
-      int e = p.topk_id[static_cast<int64_t>(t) * k + lane];
-      if (e < 0 || e >= E) {
-        atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
-        e = 0;
-      }
-      const int64_t be = static_cast<int64_t>(b) * E + e;
-      int row = p.base[be] + __popc(p.masks[be] & ((1u << i) - 1u));
-      if (row < 0 || row >= p.n * k) {
-        atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
-        row = 0;
-      }
-      rows_sm[warp][lane] = row;
-      p.token_row[static_cast<int64_t>(t) * k + lane] = row;
-      if (p.row_token) p.row_token[row] = static_cast<int32_t>(p.token0 + t);
+  const int b = t >> 5, i = t & 31;
+  if (lane < k) {
+    int e = p.topk_id[static_cast<int64_t>(t) * k + lane];
+    if (e < 0 || e >= E) {
+      atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
+      e = 0;
     }
-    __syncwarp();
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(t) * H);
-    for (int c = lane; c < H / 8; c += 32) {
-      const uint4 val = __ldg(src + c);
-      for (int s = 0; s < k; ++s)
-        reinterpret_cast<uint4*>(p.xp + static_cast<int64_t>(rows_sm[warp][s]) * H)[c] = val;
+    const int64_t be = static_cast<int64_t>(b) * E + e;
+    int row = p.base[be] + __popc(p.masks[be] & ((1u << i) - 1u));
+    if (row < 0 || row >= p.n * k) {
+      atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
+      row = 0;
     }
-    __syncwarp();
+    rows_sm[warp][lane] = row;
+    p.token_row[static_cast<int64_t>(t) * k + lane] = row;
+    if (p.row_token) p.row_token[row] = static_cast<int32_t>(p.token0 + t);
+  }
+  __syncwarp();
+  const uint4* src = reinterpret_cast<const uint4*>(p.x + static_cast<int64_t>(t) * H);
+  for (int c = lane; c < H / 8; c += 32) {
+    const uint4 val = __ldg(src + c);
+    for (int s = 0; s < k; ++s) reinterpret_cast<uint4*>(p.xp + static_cast<int64_t>(rows_sm[warp][s]) * H)[c] = val;
   }
 }
 
@@ -401,27 +674,30 @@ cudaError_t launch_router_norms(const uint16_t* w_router, int E, int H, float* w
   return cudaGetLastError();
 }
 
+template <int EPL>
+cudaError_t launch_topk_epl(const RouteParams& p, int grid, cudaStream_t stream) {
+  topk_kernel<EPL><<<grid, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  band_kernel<EPL><<<std::min(grid, p.band_grid), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const RouteParams& p, cudaStream_t stream) {
   if (p.n <= 0) return cudaSuccess;
   const int grid = (p.n + 7) / 8;
   const int epl = (p.E + 31) / 32;
-  if (epl <= 1)
-    topk_kernel<1><<<grid, 256, 0, stream>>>(p);
-  else if (epl <= 2)
-    topk_kernel<2><<<grid, 256, 0, stream>>>(p);
-  else if (epl <= 4)
-    topk_kernel<4><<<grid, 256, 0, stream>>>(p);
-  else if (epl <= 8)
-    topk_kernel<8><<<grid, 256, 0, stream>>>(p);
-  else if (epl <= 16)
-    topk_kernel<16><<<grid, 256, 0, stream>>>(p);
-  else
-    topk_kernel<32><<<grid, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  if (epl <= 1) return launch_topk_epl<1>(p, grid, stream);
+  if (epl <= 2) return launch_topk_epl<2>(p, grid, stream);
+  if (epl <= 4) return launch_topk_epl<4>(p, grid, stream);
+  if (epl <= 8) return launch_topk_epl<8>(p, grid, stream);
+  if (epl <= 16) return launch_topk_epl<16>(p, grid, stream);
+  return launch_topk_epl<32>(p, grid, stream);
 }
 
 cudaError_t launch_count(const PermuteParams& p, cudaStream_t stream) {
-  count_kernel<<<p.nblk, 256, 0, stream>>>(p);
+  const size_t smem = static_cast<size_t>(kCountWarps) * p.E * sizeof(uint32_t);
+  count_kernel<<<(p.nblk + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -431,7 +707,7 @@ cudaError_t launch_scan_tiles(const PermuteParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream) {
-  permute_kernel<<<p.nblk, 256, 0, stream>>>(p);
+  permute_kernel<<<(p.n + kPermuteWarps - 1) / kPermuteWarps, kPermuteWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

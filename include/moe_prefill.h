@@ -139,7 +139,7 @@ const char* moe_prefill_last_error(void);
 enum {
   MOE_KERNEL_NORMS = 0,  /* router row norms + header reset (once per run) */
   MOE_KERNEL_ROUTER = 1, /* router GEMM */
-  MOE_KERNEL_TOPK = 2,
+  MOE_KERNEL_TOPK = 2,    /* top-k selection + float64 recheck of ambiguous tokens (2 kernels) */
   MOE_KERNEL_COUNT = 3,
   MOE_KERNEL_SCAN = 4,
   MOE_KERNEL_PERMUTE = 5,
@@ -162,9 +162,18 @@ int64_t moe_prefill_launch_count(moe_plan_t plan);
 /* Bound, in nanoseconds, on every device-side wait of later runs of this plan (default 2e9). */
 moe_status moe_prefill_set_wait_timeout(moe_plan_t plan, uint64_t timeout_ns);
 
-/* Statistics of the most recent run on `workspace` (synchronises `stream`): chunks processed and tokens whose
-   top-k needed the float64 recheck. Either pointer may be NULL. */
-moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* chunks, int32_t* band_tokens);
+/* Statistics of the most recent run on `workspace` (synchronises `stream`), in this order: */
+enum {
+  MOE_STATS_CHUNKS = 0,       /* chunks processed */
+  MOE_STATS_FLAGGED = 1,      /* tokens whose fp32 top-k was not certain and went to the float64 recheck */
+  MOE_STATS_BY_FLOAT = 2,     /* ... decided by float sums of the exact products */
+  MOE_STATS_BY_DOUBLE = 3,    /* ... decided by double sums */
+  MOE_STATS_BY_SEQUENTIAL = 4,/* ... decided by the sequential float64 sums */
+  MOE_STATS_BY_MANY = 5,      /* ... with more candidates than the recheck list holds (sequential sums) */
+  MOE_STATS_COUNT = 6
+};
+/* Writes min(n_stats, ...) entries of the list above to stats (entries past MOE_STATS_COUNT are 0). */
+moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* stats, int32_t n_stats);
 
 /*
  * moe_prefill_debug_gemm — one dense GEMM through the same tcgen05 kernel the layer uses.

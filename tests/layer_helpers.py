@@ -69,7 +69,7 @@ def tau_bound(x_bf16: torch.Tensor, w_router_bf16: torch.Tensor) -> np.ndarray:
     H = x_bf16.shape[1]
     xn = np.linalg.norm(x_bf16.double().numpy(), axis=1)
     wn = np.linalg.norm(w_router_bf16.double().numpy(), axis=1).max()
-    return (H // 16 + 1) * 2.0 ** -22 * xn * wn
+    return (H // 16 + 1) * 2.0 ** -23 * xn * wn
 
 
 def sample_tokens(T: int, chunks, extra: int, seed: int = 0):
