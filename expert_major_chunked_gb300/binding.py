@@ -49,6 +49,7 @@ _SIGS = {
     "moe_prefill_launch_count": ([_P], ctypes.c_int64),
     "moe_prefill_set_wait_timeout": ([_P, ctypes.c_uint64], ctypes.c_int),
     "moe_prefill_run_stats": ([_P, _P, _P, ctypes.c_int32], ctypes.c_int),
+    "moe_prefill_run_noalloc": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_prefill_debug_gemm": ([_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                 ctypes.c_uint64, _P], ctypes.c_int),
 }
@@ -96,6 +97,13 @@ def moe_prefill_run(plan, x, T, chunk, workspace, workspace_bytes, out, topk_id=
                     expert_offsets=None, row_token=None, compute=None, copy=None):
     _check(lib().moe_prefill_run(plan, x, T, chunk, workspace, workspace_bytes, out, topk_id, topk_w,
                                  expert_offsets, row_token, compute, copy))
+
+
+def moe_prefill_run_noalloc(plan, x, T, chunk, out, topk_id=None, topk_w=None, expert_offsets=None, row_token=None,
+                            device_status=None, stream=None):
+    """moe_prefill_run with the library's built-in scratch array instead of a caller workspace (see the header)."""
+    _check(lib().moe_prefill_run_noalloc(plan, x, T, chunk, out, topk_id, topk_w, expert_offsets, row_token,
+                                         device_status, stream))
 
 
 def moe_prefill_combine(y, w, token_row, s, n, k, H, out, stream=None):

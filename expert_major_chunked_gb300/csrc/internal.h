@@ -137,4 +137,7 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
                            int k, int H, uint16_t* out, cudaStream_t stream);
 
+// ------------------------------------------------------------------ host helpers shared with noalloc.cu
+void set_last_error(const char* msg);
+
 }  // namespace moe

@@ -265,6 +265,12 @@ moe_status cuda_status(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace moe {
+// Helpers for noalloc.cu (internal linkage names, not part of the C ABI).
+size_t plan_workspace_bytes(moe_plan_t plan) { return plan ? plan->lay.total : 0; }
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace moe
+
 extern "C" {
 
 moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,

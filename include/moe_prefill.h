@@ -131,6 +131,35 @@ void moe_prefill_destroy(moe_plan_t plan);
 /* moe_prefill_last_error — message for the last non-OK status returned on this thread ("" if none). */
 const char* moe_prefill_last_error(void);
 
+/*
+ * moe_prefill_run_noalloc — moe_prefill_run for callers that cannot allocate device memory.
+ * No counterpart in the pages this layer follows: it is a convenience of this library.
+ *
+ * Who needs it: callers that must not call cudaMalloc where they run the layer — code whose device memory belongs
+ * to another allocator or pool (an allocation behind its back breaks its accounting and can fail once the pool has
+ * reserved the GPU), serving loops that forbid allocation after start-up (cudaMalloc/cudaFree synchronise the
+ * device), and plug-ins that are only handed input and output pointers. It computes exactly what moe_prefill_run
+ * computes (same kernels, same bytes out) but keeps its scratch in a fixed array of MOE_NOALLOC_WORKSPACE_BYTES
+ * inside the library, so it allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *   plan, x, T, chunk, out, topk_id, topk_w, expert_offsets, row_token, stream: as for moe_prefill_run.
+ *   device_status   device int32 or NULL: receives the run's device error word once the run's work has finished on
+ *                   `stream` (0 = no device-side error; otherwise the code moe_prefill_check would decode).
+ * Limits and behaviour:
+ *   - The plan's workspace_bytes must be at most MOE_NOALLOC_WORKSPACE_BYTES; larger plans get MOE_ERR_WORKSPACE
+ *     with a message (use a smaller max_chunk, or moe_prefill_run).
+ *   - Every GPU that loads the library holds the array until the process exits.
+ *   - The array is shared by all calls on a device and keeps the last call's contents. Each run first clears the
+ *     part that must start at zero (error word, counters) and writes every other byte whose value reaches an
+ *     output before reading it. Calls whose work overlaps on the GPU (e.g. on different streams) race on the
+ *     array: serialise them.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture.
+ */
+#define MOE_NOALLOC_WORKSPACE_BYTES ((size_t)64 << 20)
+moe_status moe_prefill_run_noalloc(moe_plan_t plan, const void* x, int64_t T, int32_t chunk, void* out,
+                                   int32_t* topk_id, float* topk_w, int32_t* expert_offsets, int32_t* row_token,
+                                   int32_t* device_status, moe_stream_t stream);
+
 /* ------------------------------------------------------------------------------------------------------------
  * Diagnostics. These are part of the ABI for measurement and tests; the layer needs none of them.
  * ------------------------------------------------------------------------------------------------------------ */
