@@ -87,6 +87,11 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cud
 cudaError_t prepare_gemm_kernels();   // sets the dynamic shared memory attribute (once per device)
 
 // ------------------------------------------------------------------ routing
+// Left for band_kernel by topk_kernel for a token it could not decide: the bound and the k-th / (k+1)-th logits.
+struct BandInfo {
+  double tau, vk, vk1, pad;
+};
+
 struct RouteParams {
   const float* logits;        // [n][E] fp32 (chunk-local)
   const uint16_t* x;          // chunk rows of X, bf16 [n][H]
@@ -98,7 +103,7 @@ struct RouteParams {
   int32_t* topk_id;           // [n][k]
   float* topk_w;              // [n][k]
   uint8_t* band_flag;         // [n] 1 when the float64 recheck ran
-  double4* band_info;         // [n] (tau, v_k, v_{k+1}, -) of tokens left to band_kernel
+  BandInfo* band_info;        // [n] of tokens left to band_kernel
   int32_t band_grid;          // CTAs of band_kernel (one per SM)
 };
 cudaError_t launch_router_norms(const uint16_t* w_router, int E, int H, float* wnorm, WsHeader* hdr,

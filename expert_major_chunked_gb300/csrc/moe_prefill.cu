@@ -97,8 +97,10 @@ moe_status check_device(int* device, int* num_sms) {
 
 // ------------------------------------------------------------------ workspace layout
 struct Layout {
-  size_t hdr, wnorm, logits, topk_id, topk_w, band, band_info, masks, counts, base, block_band, offsets, token_row, num_tiles,
-      tiles_gu, tiles_down, xp, h, hs, y, s, total;
+  size_t hdr, wnorm, logits, topk_id, topk_w, band, band_info, masks, counts, base, block_band, offsets, h, hs, y, s,
+      total;
+  // two sets (chunk parity): the member lists of chunk c+1 are built while chunk c's GEMMs still read chunk c's
+  size_t token_row[2], num_tiles[2], tiles_gu[2], tiles_down[2], xp[2];
   int cap_gu, cap_down;
 };
 
@@ -160,11 +162,13 @@ Layout make_layout(const Shape& s) {
   L.base = take(nblk * E * 4);
   L.block_band = take(nblk * 4);
   L.offsets = take((E + 1) * 4);
-  L.token_row = take(C * k * 4);
-  L.num_tiles = take(16);
-  L.tiles_gu = take(static_cast<size_t>(L.cap_gu) * 16);
-  L.tiles_down = take(static_cast<size_t>(L.cap_down) * 16);
-  L.xp = take(R * H * 2);
+  for (int b = 0; b < 2; ++b) {
+    L.token_row[b] = take(C * k * 4);
+    L.num_tiles[b] = take(16);
+    L.tiles_gu[b] = take(static_cast<size_t>(L.cap_gu) * 16);
+    L.tiles_down[b] = take(static_cast<size_t>(L.cap_down) * 16);
+    L.xp[b] = take(R * H * 2);
+  }
   L.h = take(R * I * 2);
   L.hs = take(Is > 0 ? C * Is * 2 : 0);
   L.y = take(R * H * 4);
@@ -184,7 +188,12 @@ struct moe_plan {
   CUtensorMap tm_wr_narrow, tm_wr_wide, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
   // descriptors of workspace-resident activations, cached per workspace pointer
   const void* ws_cached = nullptr;
-  CUtensorMap tm_xp, tm_h, tm_hs;
+  CUtensorMap tm_xp[2], tm_h, tm_hs;
+  // Each chunk's member lists (count, scan, permute) run on a side stream so that they overlap the previous chunk's
+  // GEMMs; events order the two streams (see moe_prefill_run).
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_span = nullptr, ev_join = nullptr, ev_ready[2] = {}, ev_down = nullptr,
+              ev_comb = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int64_t launches = 0;
   bool profiling = false;
@@ -309,8 +318,18 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
+  if (st == MOE_OK) {
+    int lo = 0, hi = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, hi);
+    cudaEvent_t* evs[] = {&p->ev_fork, &p->ev_span, &p->ev_join, &p->ev_ready[0], &p->ev_ready[1], &p->ev_down,
+                          &p->ev_comb};
+    for (cudaEvent_t* ev : evs)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) st = fail(MOE_ERR_CUDA, "stream/event creation: %s", cudaGetErrorString(e));
+  }
   if (st != MOE_OK) {
-    delete p;
+    moe_prefill_destroy(p);
     return st;
   }
   *workspace_bytes = p->lay.total;
@@ -350,9 +369,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   float* wnorm = reinterpret_cast<float*>(ws + L.wnorm);
   float* logits = reinterpret_cast<float*>(ws + L.logits);
   uint8_t* band = reinterpret_cast<uint8_t*>(ws + L.band);
-  int32_t* token_row = reinterpret_cast<int32_t*>(ws + L.token_row);
-  int32_t* num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles);
-  uint16_t* xp = reinterpret_cast<uint16_t*>(ws + L.xp);
+  cudaStream_t side = p->side;
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
   uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
   float* y = reinterpret_cast<float*>(ws + L.y);
@@ -364,7 +381,8 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   if (rc != MOE_OK) return rc;
   if (p->ws_cached != workspace) {
     const uint64_t R = static_cast<uint64_t>(s.C) * s.k;
-    rc = encode_bf16_2d(&p->tm_xp, xp, R, s.H, kABoxRows);
+    rc = encode_bf16_2d(&p->tm_xp[0], ws + L.xp[0], R, s.H, kABoxRows);
+    if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_xp[1], ws + L.xp[1], R, s.H, kABoxRows);
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_h, h, R, s.I, kABoxRows);
     if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(&p->tm_hs, hs, s.C, s.Is, kABoxRows);
     if (rc != MOE_OK) {
@@ -374,12 +392,22 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     p->ws_cached = workspace;
   }
 
+  // The side stream starts after everything the caller enqueued on `compute` before this call, and every return
+  // after this point first makes `compute` wait for all side work (join), so the run is one unit on `compute`.
+  rc = cuda_status(cudaEventRecord(p->ev_fork, st), "fork event");
+  if (rc == MOE_OK) rc = cuda_status(cudaStreamWaitEvent(side, p->ev_fork, 0), "fork wait");
+  if (rc != MOE_OK) return rc;
+  auto join = [&](moe_status r) {
+    if (cudaEventRecord(p->ev_join, side) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
+    return r;
+  };
+
   {
     LaunchScope ls(p, MOE_KERNEL_NORMS, st);
     rc = cuda_status(launch_router_norms(static_cast<const uint16_t*>(p->w_router), s.E, s.H, wnorm, hdr, st),
                      "router norms launch");
   }
-  if (rc != MOE_OK) return rc;
+  if (rc != MOE_OK) return join(rc);
 
   // |fp32 tensor-core logit - exact| <= one ulp per 16-wide K step of a partial sum bounded by ||x|| ||w||
   const float tau_coef = static_cast<float>(s.H / 16 + 1) * 0x1p-23f;
@@ -390,6 +418,10 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     const int ns = static_cast<int>(std::min<int64_t>(span, T - s0));
     int32_t* span_ids = topk_id ? topk_id + s0 * s.k : reinterpret_cast<int32_t*>(ws + L.topk_id);
     float* span_w = topk_w ? topk_w + s0 * s.k : reinterpret_cast<float*>(ws + L.topk_w);
+
+    // the previous span's combines and member lists read this span's buffers (logits, top-k): wait for them
+    rc = cuda_status(cudaStreamWaitEvent(st, p->ev_comb, 0), "span start wait");
+    if (rc != MOE_OK) return join(rc);
 
     // 1. router GEMM: logits [ns][E] fp32
     const bool wide = ns >= 4096;
@@ -423,7 +455,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       LaunchScope ls(p, MOE_KERNEL_ROUTER, st);
       rc = cuda_status(launch_grouped_gemm(g, kEpiF32, std::min(p->num_sms, tiles), st), "router GEMM launch");
     }
-    if (rc != MOE_OK) return rc;
+    if (rc != MOE_OK) return join(rc);
 
     // 2. top-k + weights (and the float64 recheck of tokens whose fp32 selection is not certain)
     RouteParams r;
@@ -440,71 +472,79 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     r.topk_id = span_ids;
     r.topk_w = span_w;
     r.band_flag = band;
-    r.band_info = reinterpret_cast<double4*>(ws + L.band_info);
+    r.band_info = reinterpret_cast<BandInfo*>(ws + L.band_info);
     r.band_grid = p->num_sms;
     {
       LaunchScope ls(p, MOE_KERNEL_TOPK, st, 2);  // top-k, then the float64 recheck of flagged tokens
       rc = cuda_status(launch_topk(r, st), "top-k launch");
     }
-    if (rc != MOE_OK) return rc;
+    if (rc == MOE_OK) rc = cuda_status(cudaEventRecord(p->ev_span, st), "span event");
+    if (rc != MOE_OK) return join(rc);
 
-    for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
+    // Per chunk c: member lists L(c) on the side stream, GEMMs G(c) on `compute`, combine C(c) on the side stream.
+    // Enqueue order: L(first); then for each chunk G(c), L(c+1), C(c). On the GPU, L(c+1) and C(c) overlap G(c)
+    // and G(c+1). Buffer set c%2 (gathered rows, tile lists, token_row) is reused by chunk c+2: L(c+2) follows
+    // C(c) on the side stream, and C(c) waits for G(c). The down GEMM of chunk c waits for C(c-1) (y, s reuse).
+    auto lists = [&](int64_t c0, int64_t cidx) -> moe_status {
       const int n = static_cast<int>(std::min<int64_t>(chunk, T - c0));
-      const int nblk = (n + 31) / 32;
-      const uint16_t* xc = static_cast<const uint16_t*>(x) + c0 * s.H;
-      int32_t* ids = span_ids + (c0 - s0) * s.k;
-      float* wts = span_w + (c0 - s0) * s.k;
-
-      // 3-5. member lists and tile lists
+      const int par = static_cast<int>(cidx & 1);
       PermuteParams q;
-      q.topk_id = ids;
+      q.topk_id = span_ids + (c0 - s0) * s.k;
       q.band_flag = band + (c0 - s0);
-      q.x = xc;
+      q.x = static_cast<const uint16_t*>(x) + c0 * s.H;
       q.n = n;
       q.E = s.E;
       q.H = s.H;
       q.k = s.k;
-      q.nblk = nblk;
+      q.nblk = (n + 31) / 32;
       q.token0 = c0;
       q.masks = reinterpret_cast<uint32_t*>(ws + L.masks);
       q.counts = reinterpret_cast<int32_t*>(ws + L.counts);
       q.block_band = reinterpret_cast<int32_t*>(ws + L.block_band);
       q.base = reinterpret_cast<int32_t*>(ws + L.base);
       q.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
-      q.offsets_out = expert_offsets ? expert_offsets + chunk_idx * (s.E + 1) : nullptr;
-      q.token_row = token_row;
+      q.offsets_out = expert_offsets ? expert_offsets + cidx * (s.E + 1) : nullptr;
+      q.token_row = reinterpret_cast<int32_t*>(ws + L.token_row[par]);
       q.row_token = row_token ? row_token + c0 * s.k : nullptr;
-      q.xp = xp;
+      q.xp = reinterpret_cast<uint16_t*>(ws + L.xp[par]);
       q.hdr = hdr;
-      q.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu);
-      q.tiles_down = reinterpret_cast<int4*>(ws + L.tiles_down);
-      q.num_tiles = num_tiles;
+      q.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu[par]);
+      q.tiles_down = reinterpret_cast<int4*>(ws + L.tiles_down[par]);
+      q.num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles[par]);
       q.cap_gu = L.cap_gu;
       q.cap_down = L.cap_down;
       q.nt_gu = s.nt_gu;
       q.nt_down = s.nt_down;
       q.nt_gu_shared = s.nt_gu_s;
       q.nt_down_shared = s.Is > 0 ? s.nt_down : 0;
+      moe_status r2;
       {
-        LaunchScope ls(p, MOE_KERNEL_COUNT, st);
-        rc = cuda_status(launch_count(q, st), "count launch");
+        LaunchScope ls(p, MOE_KERNEL_COUNT, side);
+        r2 = cuda_status(launch_count(q, side), "count launch");
       }
-      if (rc != MOE_OK) return rc;
+      if (r2 != MOE_OK) return r2;
       {
-        LaunchScope ls(p, MOE_KERNEL_SCAN, st);
-        rc = cuda_status(launch_scan_tiles(q, st), "scan launch");
+        LaunchScope ls(p, MOE_KERNEL_SCAN, side);
+        r2 = cuda_status(launch_scan_tiles(q, side), "scan launch");
       }
-      if (rc != MOE_OK) return rc;
+      if (r2 != MOE_OK) return r2;
       {
-        LaunchScope ls(p, MOE_KERNEL_PERMUTE, st);
-        rc = cuda_status(launch_permute(q, st), "permute launch");
+        LaunchScope ls(p, MOE_KERNEL_PERMUTE, side);
+        r2 = cuda_status(launch_permute(q, side), "permute launch");
       }
-      if (rc != MOE_OK) return rc;
+      if (r2 != MOE_OK) return r2;
+      return cuda_status(cudaEventRecord(p->ev_ready[par], side), "ready event");
+    };
 
+    auto gemms = [&](int64_t cidx) -> moe_status {
+      const int par = static_cast<int>(cidx & 1);
+      const int32_t* num_tiles = reinterpret_cast<const int32_t*>(ws + L.num_tiles[par]);
+      moe_status r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_ready[par], 0), "ready wait");
+      if (r2 != MOE_OK) return r2;
       // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
       GemmParams gu;
       memset(&gu, 0, sizeof gu);
-      gu.tmA[0] = p->tm_xp;
+      gu.tmA[0] = p->tm_xp[par];
       gu.tmB[0] = p->tm_wgu;
       GemmClass c_r;
       c_r.kblocks = s.H / kBlockK;
@@ -536,17 +576,20 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         gu.tmB[1] = gu.tmB[0];
         gu.cls[1] = c_r;
       }
-      gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu);
+      gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu[par]);
       gu.num_tiles = num_tiles;
       gu.err = &hdr->err;
       gu.timeout_ns = p->timeout_ns;
       {
         LaunchScope ls(p, MOE_KERNEL_GATE_UP, st);
-        rc = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st), "gate/up launch");
+        r2 = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st), "gate/up launch");
       }
-      if (rc != MOE_OK) return rc;
+      if (r2 != MOE_OK) return r2;
 
-      // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s)
+      // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s), once the previous chunk's combine
+      // has read y and s
+      r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_comb, 0), "combine wait");
+      if (r2 != MOE_OK) return r2;
       GemmParams dn;
       memset(&dn, 0, sizeof dn);
       dn.tmA[0] = p->tm_h;
@@ -576,27 +619,48 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         dn.tmB[1] = dn.tmB[0];
         dn.cls[1] = d_r;
       }
-      dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down);
+      dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down[par]);
       dn.num_tiles = num_tiles + 1;
       dn.err = &hdr->err;
       dn.timeout_ns = p->timeout_ns;
       {
         LaunchScope ls(p, MOE_KERNEL_DOWN, st);
-        rc = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
+        r2 = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
       }
-      if (rc != MOE_OK) return rc;
+      if (r2 != MOE_OK) return r2;
+      return cuda_status(cudaEventRecord(p->ev_down, st), "down event");
+    };
 
+    auto combine = [&](int64_t c0, int64_t cidx) -> moe_status {
+      const int n = static_cast<int>(std::min<int64_t>(chunk, T - c0));
+      const int par = static_cast<int>(cidx & 1);
+      moe_status r2 = cuda_status(cudaStreamWaitEvent(side, p->ev_down, 0), "down wait");
+      if (r2 != MOE_OK) return r2;
       // 8. canonical combine
       {
-        LaunchScope ls(p, MOE_KERNEL_COMBINE, st);
-        rc = cuda_status(launch_combine(y, wts, token_row, s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
-                                        static_cast<uint16_t*>(out) + c0 * s.H, st),
+        LaunchScope ls(p, MOE_KERNEL_COMBINE, side);
+        r2 = cuda_status(launch_combine(y, span_w + (c0 - s0) * s.k,
+                                        reinterpret_cast<const int32_t*>(ws + L.token_row[par]),
+                                        s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
+                                        static_cast<uint16_t*>(out) + c0 * s.H, side),
                          "combine launch");
       }
-      if (rc != MOE_OK) return rc;
+      if (r2 != MOE_OK) return r2;
+      return cuda_status(cudaEventRecord(p->ev_comb, side), "combine event");
+    };
+
+    rc = cuda_status(cudaStreamWaitEvent(side, p->ev_span, 0), "span wait");
+    if (rc == MOE_OK) rc = lists(s0, chunk_idx);
+    if (rc != MOE_OK) return join(rc);
+    for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
+      rc = gemms(chunk_idx);
+      if (rc == MOE_OK && c0 + chunk < s0 + ns) rc = lists(c0 + chunk, chunk_idx + 1);
+      if (rc == MOE_OK) rc = combine(c0, chunk_idx);
+      if (rc != MOE_OK) return join(rc);
     }
   }
-  return MOE_OK;
+  // The side stream's last combine joins `compute` here: the run ends after all of its work.
+  return join(MOE_OK);
 }
 
 moe_status moe_prefill_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
@@ -641,6 +705,9 @@ moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* 
 
 void moe_prefill_destroy(moe_plan_t p) {
   if (!p) return;
+  for (cudaEvent_t e : {p->ev_fork, p->ev_span, p->ev_join, p->ev_ready[0], p->ev_ready[1], p->ev_down, p->ev_comb})
+    if (e) cudaEventDestroy(e);
+  if (p->side) cudaStreamDestroy(p->side);
   for (auto& t : p->pending) {
     if (t.a) cudaEventDestroy(t.a);
     if (t.b) cudaEventDestroy(t.b);

@@ -78,12 +78,6 @@ struct BandScratch {
   int32_t chosen[kMaxCand];
 };
 
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // bf16 -> double by bit manipulation on the integer pipe (GB300's fp64 pipe is 1/64 of fp32): exact for every bf16.
 __device__ __forceinline__ double bf16_bits_to_double(uint32_t b16) {
   const uint32_t sign = b16 >> 15, ex = (b16 >> 7) & 0xFFu, man = b16 & 0x7Fu;
@@ -400,7 +394,7 @@ __global__ void __launch_bounds__(256, 2) topk_kernel(RouteParams p) {
       if (lane == 0) atomicAdd(&p.hdr->band_levels[0], 1);  // diagnostic counter only
     } else {
       flag = 2;  // band_kernel decides this token
-      if (lane == 0) p.band_info[t] = make_double4(tau, static_cast<double>(vk), static_cast<double>(vk1), 0.0);
+      if (lane == 0) p.band_info[t] = BandInfo{tau, static_cast<double>(vk), static_cast<double>(vk1), 0.0};
     }
     __syncwarp();
   }
@@ -421,12 +415,12 @@ __global__ void __launch_bounds__(256) band_kernel(RouteParams p) {
     float v[EPL];
     load_logits(p.logits + static_cast<int64_t>(t) * E, E, lane, v);
     const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
-    const double4 bi = p.band_info[t];
+    const BandInfo bi = p.band_info[t];
     BandScratch& B = band_scratch[warp];
     uint32_t sure, cand;
     int cidx[EPL];
     int need;
-    const int ncand = band_candidates(v, E, k, lane, bi.x, bi.y, bi.z, B, &sure, &cand, cidx, &need);
+    const int ncand = band_candidates(v, E, k, lane, bi.tau, bi.vk, bi.vk1, B, &sure, &cand, cidx, &need);
     uint32_t chosen = 0;
     if (ncand <= kMaxCand) {
       band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);  // S for the bounds
