@@ -167,20 +167,24 @@ class MoePrefill:
     """One MoE layer bound to device weights (torch bf16 tensors), with its workspace.
 
     weights: dict with w_router [E][H], w_gu [E][2I][H], w_down [E][H][I] and optionally ws_gu [2I_s][H],
-    ws_down [H][I_s], all bf16 CUDA tensors.
+    ws_down [H][I_s], all bf16 CUDA tensors; with offload_slots > 0, w_gu and w_down are pinned CPU tensors.
     """
 
-    def __init__(self, weights: dict, top_k: int, max_chunk: int):
+    def __init__(self, weights: dict, top_k: int, max_chunk: int, offload_slots: int = 0):
         import torch
         wr, wgu, wd = weights["w_router"], weights["w_gu"], weights["w_down"]
         wsg, wsd = weights.get("ws_gu"), weights.get("ws_down")
-        for t in (wr, wgu, wd, wsg, wsd):
+        for t in (wr, wsg, wsd) + (() if offload_slots else (wgu, wd)):
             if t is not None and (t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous()):
                 raise ValueError("weights must be contiguous bf16 CUDA tensors")
+        if offload_slots:
+            for t in (wgu, wd):
+                if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+                    raise ValueError("offloaded expert banks must be contiguous pinned bf16 CPU tensors")
         E, H = wr.shape
         I = wgu.shape[1] // 2
         Is = wsg.shape[0] // 2 if wsg is not None else 0
-        self.dims = moe_dims(H, E, I, top_k, Is, 1, max_chunk, 0)
+        self.dims = moe_dims(H, E, I, top_k, Is, 1, max_chunk, offload_slots)
         self.weights = weights  # keep alive: the plan points at them
         self.plan, self.workspace_bytes = moe_prefill_plan(self.dims, wr.data_ptr(), wgu.data_ptr(), wd.data_ptr(),
                                                            _ptr(wsg), _ptr(wsd))
@@ -194,7 +198,7 @@ class MoePrefill:
             self.plan = None
 
     def run(self, x, chunk: int, out=None, topk_id=None, topk_w=None, expert_offsets=None, row_token=None,
-            stream=None):
+            stream=None, copy_stream=None):
         import torch
         if x.dtype != torch.bfloat16 or not x.is_cuda or not x.is_contiguous():
             raise ValueError("x must be a contiguous bf16 CUDA tensor")
@@ -203,7 +207,7 @@ class MoePrefill:
             out = torch.empty_like(x)
         moe_prefill_run(self.plan, x.data_ptr(), T, chunk, self.workspace.data_ptr(), self.workspace_bytes,
                         out.data_ptr(), _ptr(topk_id), _ptr(topk_w), _ptr(expert_offsets), _ptr(row_token),
-                        _stream_handle(stream), None)
+                        _stream_handle(stream), copy_stream.cuda_stream if copy_stream is not None else None)
         return out
 
     def check(self, stream=None) -> int:

@@ -54,6 +54,16 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p) {
   return ((p.dense_m + kBlockM - 1) / kBlockM) * p.dense_n_tiles;
 }
 
+// First tile of this launch and the end of its range: the whole list, or [*range_lo, *range_hi) of it.
+__device__ __forceinline__ int2 tile_range(const GemmParams& p) {
+  int lo = 0, hi = total_tiles(p);
+  if (p.range_lo != nullptr) {
+    lo = max(0, *reinterpret_cast<const volatile int32_t*>(p.range_lo));
+    hi = min(hi, *reinterpret_cast<const volatile int32_t*>(p.range_hi));
+  }
+  return make_int2(lo, hi);
+}
+
 __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* abort_flag, int site) {
   *abort_flag = 1;
   atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, site, static_cast<int>(blockIdx.x)));
@@ -116,7 +126,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
-  const int ntiles = total_tiles(p);
+  const int2 trange = tile_range(p);
+  const int tfirst = trange.x + static_cast<int>(blockIdx.x);
+  const int ntiles = trange.y;
   const uint64_t tmo = p.timeout_ns;
 
   if (warp == 0) {
@@ -137,7 +149,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           }
         }
       }
-      for (int t = blockIdx.x; !failed && t < ntiles; t += gridDim.x) {
+      for (int t = tfirst; !failed && t < ntiles; t += gridDim.x) {
         const TileInfo ti = decode_tile(p, t);
         const GemmClass& C = p.cls[ti.cls];
         const void* tA = &p.tmA[ti.cls];
@@ -146,11 +158,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
         const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * 128u;
         int b_row0, b_row1 = 0;
+        const int slot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
         if (EPI == kEpiSwiGLU) {
-          b_row0 = ti.group * C.b_group_rows + ti.n_idx * C.b_box_rows;
+          b_row0 = slot * C.b_group_rows + ti.n_idx * C.b_box_rows;
           b_row1 = b_row0 + C.b_up_offset;
         } else {
-          b_row0 = ti.group * C.b_group_rows + ti.n_idx * C.n_tile;
+          b_row0 = slot * C.b_group_rows + ti.n_idx * C.n_tile;
         }
         for (int kb = 0; kb < C.kblocks; ++kb) {
           if (!ptx::wait_bounded(empty0 + 8u * stage, phase ^ 1u, tmo, abort_flag)) {
@@ -197,7 +210,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       int stage = 0, local = 0;
       uint32_t phase = 0;
       bool failed = false, issued_any = false;
-      for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+      for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
         const TileInfo ti = decode_tile(p, t);
         const GemmClass& C = p.cls[ti.cls];
         const int acc = local & 1;
@@ -247,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     const int q = warp & 3;
     const int row = q * 32 + lane;
     int local = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++local) {
+    for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
       const TileInfo ti = decode_tile(p, t);
       const GemmClass& C = p.cls[ti.cls];
       const int acc = local & 1;

@@ -60,7 +60,7 @@ struct GemmClass {
   int32_t b_up_offset;    // SwiGLU: row offset of the up half inside a group (= I), else 0
   int32_t out_cols;       // valid output columns (masks a ragged last N tile)
   int32_t b_stream;       // 1: honour the tile's stream bit (expert weights); 0: never use the evict-first policy
-  int32_t pad_;
+  int32_t b_group_mod;    // > 0: B holds a ring of b_group_mod groups and group e lives in slot e % b_group_mod
   int64_t out_ld;         // output row stride in elements
   void* out;              // F32: float*, SwiGLU: bf16*
 };
@@ -74,6 +74,8 @@ struct GemmParams {
   GemmClass cls[2];
   const int4* tiles;          // device tile list (nullptr: dense mode)
   const int32_t* num_tiles;   // device tile count (used when tiles != nullptr)
+  const int32_t* range_lo;    // optional device bounds: only tiles [*range_lo, *range_hi) of the list run
+  const int32_t* range_hi;
   int32_t dense_m;            // dense mode: M rows, tiles = ceil(M/128) x n_tiles, A rows start at dense_a_row0
   int32_t dense_n_tiles;
   int32_t dense_a_row0;
@@ -130,6 +132,7 @@ struct PermuteParams {
   int4* tiles_gu;             // capacity cap_gu
   int4* tiles_down;           // capacity cap_down
   int32_t* num_tiles;         // [2]: gu, down
+  int32_t* tile_base;         // [2][E+1]: first gate/up and first down tile of each expert ([E] = routed total)
   int32_t cap_gu, cap_down;
   int32_t nt_gu, nt_down;     // N tiles per routed expert (GU: I / half, down: H / bn_down)
   int32_t nt_gu_shared, nt_down_shared;  // N tiles of the shared expert (0 = no shared expert)

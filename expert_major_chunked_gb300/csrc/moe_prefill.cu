@@ -100,7 +100,8 @@ struct Layout {
   size_t hdr, wnorm, logits, topk_id, topk_w, band, band_info, masks, counts, base, block_band, offsets, h, hs, y, s,
       total;
   // two sets (chunk parity): the member lists of chunk c+1 are built while chunk c's GEMMs still read chunk c's
-  size_t token_row[2], num_tiles[2], tiles_gu[2], tiles_down[2], xp[2];
+  size_t token_row[2], num_tiles[2], tiles_gu[2], tiles_down[2], xp[2], tile_base[2];
+  size_t ring_gu, ring_down;  // offloaded experts: the HBM ring of expert slots
   int cap_gu, cap_down;
 };
 
@@ -109,7 +110,7 @@ struct Layout {
 constexpr int kRouteSpan = 16384;
 
 struct Shape {
-  int H, E, I, k, Is, C, span_cap;
+  int H, E, I, k, Is, C, span_cap, slots, window;
   int gu_half, gu_half_s, bn_down, bn_router_narrow, bn_router_wide;
   int nt_gu, nt_gu_s, nt_down;
 };
@@ -123,6 +124,8 @@ Shape make_shape(const moe_dims& d) {
   s.Is = d.shared_inter;
   s.C = d.max_chunk;
   s.span_cap = std::max(s.C, kRouteSpan);
+  s.slots = d.offload_slots;
+  s.window = d.offload_slots / 2;
   s.gu_half = (s.I % 128 == 0) ? 128 : 64;
   s.gu_half_s = (s.Is % 128 == 0) ? 128 : 64;
   s.bn_down = (s.H % 256 == 0) ? 256 : (s.H % 128 == 0 ? 128 : 64);
@@ -168,7 +171,11 @@ Layout make_layout(const Shape& s) {
     L.tiles_gu[b] = take(static_cast<size_t>(L.cap_gu) * 16);
     L.tiles_down[b] = take(static_cast<size_t>(L.cap_down) * 16);
     L.xp[b] = take(R * H * 2);
+    L.tile_base[b] = take(2 * (E + 1) * 4);
   }
+  const size_t S = static_cast<size_t>(s.slots);
+  L.ring_gu = take(S * 2 * I * H * 2);
+  L.ring_down = take(S * H * I * 2);
   L.h = take(R * I * 2);
   L.hs = take(Is > 0 ? C * Is * 2 : 0);
   L.y = take(R * H * 4);
@@ -188,7 +195,11 @@ struct moe_plan {
   CUtensorMap tm_wr_narrow, tm_wr_wide, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
   // descriptors of workspace-resident activations, cached per workspace pointer
   const void* ws_cached = nullptr;
-  CUtensorMap tm_xp[2], tm_h, tm_hs;
+  CUtensorMap tm_xp[2], tm_h, tm_hs, tm_ring_gu, tm_ring_down;
+  // offloaded experts: w_gu / w_down are pinned host banks; the copy stream fills the ring (see moe_prefill_run)
+  bool offload = false;
+  cudaStream_t own_copy = nullptr;
+  cudaEvent_t ev_copy[2] = {}, ev_rel[2] = {};
   // Each chunk's member lists (count, scan, permute) run on a side stream so that they overlap the previous chunk's
   // GEMMs; events order the two streams (see moe_prefill_run).
   cudaStream_t side = nullptr;
@@ -221,8 +232,12 @@ moe_status validate_dims(const moe_dims* d) {
   if (d->top_k > d->n_experts || d->top_k > 32)
     return fail(MOE_ERR_UNSUPPORTED, "top_k must be at most min(n_experts, 32) (got %d)", d->top_k);
   if (d->renormalize != 1) return fail(MOE_ERR_UNSUPPORTED, "only renormalize == 1 is implemented");
-  if (d->offload_slots != 0)
-    return fail(MOE_ERR_UNSUPPORTED, "offloaded experts (offload_slots > 0) are not available in this build");
+  if (d->offload_slots != 0) {
+    const int S = d->offload_slots;
+    if (S < 2 || S % 2 || S > d->n_experts || d->n_experts % (S / 2))
+      return fail(MOE_ERR_UNSUPPORTED,
+                  "offload_slots must be even, at most n_experts, and half of it must divide n_experts (got %d)", S);
+  }
   const int64_t R = static_cast<int64_t>(d->max_chunk) * d->top_k;
   if (R >= (1ll << 30) || static_cast<int64_t>(d->n_experts) * d->hidden >= (1ll << 31) ||
       static_cast<int64_t>(d->n_experts) * 2 * d->inter >= (1ll << 31))
@@ -311,19 +326,34 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   p->ws_gu = ws_gu;
   p->ws_down = ws_down;
   const Shape& s = p->sh;
+  p->offload = dims->offload_slots > 0;
+  if (p->offload) {
+    // the expert banks stay in host memory: they must be page-locked so the copy engines can read them
+    for (const void* q : {w_gu, w_down}) {
+      cudaPointerAttributes a;
+      if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        delete p;
+        return fail(MOE_ERR_INVALID_ARG, "offload_slots > 0 needs w_gu and w_down in pinned host memory");
+      }
+    }
+  }
   st = encode_bf16_2d(&p->tm_wr_narrow, w_router, s.E, s.H, s.bn_router_narrow);
   if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wr_wide, w_router, s.E, s.H, s.bn_router_wide);
-  if (st == MOE_OK)
+  if (st == MOE_OK && !p->offload)
     st = encode_bf16_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H, s.gu_half);
-  if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
+  if (st == MOE_OK && !p->offload)
+    st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
   if (st == MOE_OK) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, hi);
-    cudaEvent_t* evs[] = {&p->ev_fork, &p->ev_span, &p->ev_join, &p->ev_ready[0], &p->ev_ready[1], &p->ev_down,
-                          &p->ev_comb};
+    if (e == cudaSuccess && p->offload) e = cudaStreamCreateWithFlags(&p->own_copy, cudaStreamNonBlocking);
+    cudaEvent_t* evs[] = {&p->ev_fork,    &p->ev_span,    &p->ev_join,    &p->ev_ready[0], &p->ev_ready[1],
+                          &p->ev_down,    &p->ev_comb,    &p->ev_copy[0], &p->ev_copy[1], &p->ev_rel[0],
+                          &p->ev_rel[1]};
     for (cudaEvent_t* ev : evs)
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) st = fail(MOE_ERR_CUDA, "stream/event creation: %s", cudaGetErrorString(e));
@@ -344,7 +374,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
   if (chunk < 1 || chunk > p->d.max_chunk)
     return fail(MOE_ERR_INVALID_ARG, "chunk must be in [1, max_chunk=%d] (got %d)", p->d.max_chunk, chunk);
-  if (copy) return fail(MOE_ERR_INVALID_ARG, "copy stream must be NULL for resident weights");
+  if (copy && !p->offload) return fail(MOE_ERR_INVALID_ARG, "copy stream must be NULL for resident weights");
   if (T >= (1ll << 31)) return fail(MOE_ERR_UNSUPPORTED, "T must be below 2^31");
   if (T == 0) return MOE_OK;
   if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "x and out must not be NULL");
@@ -370,6 +400,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   float* logits = reinterpret_cast<float*>(ws + L.logits);
   uint8_t* band = reinterpret_cast<uint8_t*>(ws + L.band);
   cudaStream_t side = p->side;
+  cudaStream_t cp = copy ? reinterpret_cast<cudaStream_t>(copy) : p->own_copy;  // offloaded experts only
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + L.h);
   uint16_t* hs = reinterpret_cast<uint16_t*>(ws + L.hs);
   float* y = reinterpret_cast<float*>(ws + L.y);
@@ -385,6 +416,10 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_xp[1], ws + L.xp[1], R, s.H, kABoxRows);
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_h, h, R, s.I, kABoxRows);
     if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(&p->tm_hs, hs, s.C, s.Is, kABoxRows);
+    if (rc == MOE_OK && p->offload)
+      rc = encode_bf16_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
+    if (rc == MOE_OK && p->offload)
+      rc = encode_bf16_2d(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I, s.bn_down);
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;
@@ -396,9 +431,11 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   // after this point first makes `compute` wait for all side work (join), so the run is one unit on `compute`.
   rc = cuda_status(cudaEventRecord(p->ev_fork, st), "fork event");
   if (rc == MOE_OK) rc = cuda_status(cudaStreamWaitEvent(side, p->ev_fork, 0), "fork wait");
+  if (rc == MOE_OK && p->offload) rc = cuda_status(cudaStreamWaitEvent(cp, p->ev_fork, 0), "fork wait");
   if (rc != MOE_OK) return rc;
   auto join = [&](moe_status r) {
     if (cudaEventRecord(p->ev_join, side) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
+    if (p->offload && cudaEventRecord(p->ev_join, cp) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
     return r;
   };
 
@@ -439,6 +476,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     rc0.b_up_offset = 0;
     rc0.out_cols = s.E;
     rc0.b_stream = 0;
+    rc0.b_group_mod = 0;
     rc0.out_ld = s.E;
     rc0.out = logits;
     g.cls[0] = g.cls[1] = rc0;
@@ -511,6 +549,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       q.tiles_gu = reinterpret_cast<int4*>(ws + L.tiles_gu[par]);
       q.tiles_down = reinterpret_cast<int4*>(ws + L.tiles_down[par]);
       q.num_tiles = reinterpret_cast<int32_t*>(ws + L.num_tiles[par]);
+      q.tile_base = reinterpret_cast<int32_t*>(ws + L.tile_base[par]);
       q.cap_gu = L.cap_gu;
       q.cap_down = L.cap_down;
       q.nt_gu = s.nt_gu;
@@ -536,16 +575,44 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       return cuda_status(cudaEventRecord(p->ev_ready[par], side), "ready event");
     };
 
-    auto gemms = [&](int64_t cidx) -> moe_status {
+    // Offloaded experts: the ring's halves hold windows of W consecutive experts; window [e0, e0 + W) goes to slots
+    // e0 % S ... (one copy for its gate/up weights, one for its down weights) once the copy stream has seen the
+    // release of the window that last used those slots.
+    auto copy_window = [&](int e0) -> moe_status {
+      const int hb = (e0 / s.window) & 1;
+      const size_t slot0 = static_cast<size_t>(e0 % s.slots);
+      const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H * 2, dn_bytes = static_cast<size_t>(s.H) * s.I * 2;
+      moe_status r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[hb], 0), "slot release wait");
+      if (r2 == MOE_OK)
+        r2 = cuda_status(cudaMemcpyAsync(ws + L.ring_gu + slot0 * gu_bytes,
+                                         static_cast<const char*>(p->w_gu) + static_cast<size_t>(e0) * gu_bytes,
+                                         gu_bytes * s.window, cudaMemcpyHostToDevice, cp),
+                         "expert gate/up copy");
+      if (r2 == MOE_OK)
+        r2 = cuda_status(cudaMemcpyAsync(ws + L.ring_down + slot0 * dn_bytes,
+                                         static_cast<const char*>(p->w_down) + static_cast<size_t>(e0) * dn_bytes,
+                                         dn_bytes * s.window, cudaMemcpyHostToDevice, cp),
+                         "expert down copy");
+      if (r2 == MOE_OK) r2 = cuda_status(cudaEventRecord(p->ev_copy[hb], cp), "copy event");
+      return r2;
+    };
+
+    // The grouped GEMMs of experts [e0, e1) of a chunk (all experts when the weights are resident); the range
+    // of the last experts also covers the shared expert's tiles, which follow the routed ones in the lists.
+    auto gemms = [&](int64_t cidx, int e0, int e1) -> moe_status {
       const int par = static_cast<int>(cidx & 1);
       const int32_t* num_tiles = reinterpret_cast<const int32_t*>(ws + L.num_tiles[par]);
+      const int32_t* tbase = reinterpret_cast<const int32_t*>(ws + L.tile_base[par]);
+      const bool windowed = p->offload;
+      const int hb = windowed ? (e0 / s.window) & 1 : 0;
       moe_status r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_ready[par], 0), "ready wait");
+      if (r2 == MOE_OK && windowed) r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_copy[hb], 0), "copy wait");
       if (r2 != MOE_OK) return r2;
       // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
       GemmParams gu;
       memset(&gu, 0, sizeof gu);
       gu.tmA[0] = p->tm_xp[par];
-      gu.tmB[0] = p->tm_wgu;
+      gu.tmB[0] = windowed ? p->tm_ring_gu : p->tm_wgu;
       GemmClass c_r;
       c_r.kblocks = s.H / kBlockK;
       c_r.n_tile = 2 * s.gu_half;
@@ -554,6 +621,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       c_r.b_up_offset = s.I;
       c_r.out_cols = s.I;
       c_r.b_stream = 1;
+      c_r.b_group_mod = windowed ? s.slots : 0;
       c_r.out_ld = s.I;
       c_r.out = h;
       gu.cls[0] = c_r;
@@ -568,6 +636,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         c_s.b_up_offset = s.Is;
         c_s.out_cols = s.Is;
         c_s.b_stream = 0;
+        c_s.b_group_mod = 0;
         c_s.out_ld = s.Is;
         c_s.out = hs;
         gu.cls[1] = c_s;
@@ -578,6 +647,10 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       }
       gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu[par]);
       gu.num_tiles = num_tiles;
+      if (windowed) {
+        gu.range_lo = tbase + e0;
+        gu.range_hi = (e1 >= s.E) ? num_tiles : tbase + e1;
+      }
       gu.err = &hdr->err;
       gu.timeout_ns = p->timeout_ns;
       {
@@ -593,7 +666,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       GemmParams dn;
       memset(&dn, 0, sizeof dn);
       dn.tmA[0] = p->tm_h;
-      dn.tmB[0] = p->tm_wdown;
+      dn.tmB[0] = windowed ? p->tm_ring_down : p->tm_wdown;
       GemmClass d_r;
       d_r.kblocks = s.I / kBlockK;
       d_r.n_tile = s.bn_down;
@@ -602,6 +675,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       d_r.b_up_offset = 0;
       d_r.out_cols = s.H;
       d_r.b_stream = 1;
+      d_r.b_group_mod = windowed ? s.slots : 0;
       d_r.out_ld = s.H;
       d_r.out = y;
       dn.cls[0] = d_r;
@@ -612,6 +686,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         d_s.kblocks = s.Is / kBlockK;
         d_s.b_group_rows = 0;
         d_s.b_stream = 0;
+        d_s.b_group_mod = 0;
         d_s.out = sbuf;
         dn.cls[1] = d_s;
       } else {
@@ -621,6 +696,10 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       }
       dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down[par]);
       dn.num_tiles = num_tiles + 1;
+      if (windowed) {
+        dn.range_lo = tbase + (s.E + 1) + e0;
+        dn.range_hi = (e1 >= s.E) ? num_tiles + 1 : tbase + (s.E + 1) + e1;
+      }
       dn.err = &hdr->err;
       dn.timeout_ns = p->timeout_ns;
       {
@@ -628,6 +707,10 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         r2 = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
       }
       if (r2 != MOE_OK) return r2;
+      if (windowed) {
+        r2 = cuda_status(cudaEventRecord(p->ev_rel[hb], st), "slot release event");
+        if (r2 != MOE_OK) return r2;
+      }
       return cuda_status(cudaEventRecord(p->ev_down, st), "down event");
     };
 
@@ -653,7 +736,14 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     if (rc == MOE_OK) rc = lists(s0, chunk_idx);
     if (rc != MOE_OK) return join(rc);
     for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
-      rc = gemms(chunk_idx);
+      if (!p->offload) {
+        rc = gemms(chunk_idx, 0, s.E);
+      } else {
+        for (int e0 = 0; rc == MOE_OK && e0 < s.E; e0 += s.window) {
+          rc = copy_window(e0);
+          if (rc == MOE_OK) rc = gemms(chunk_idx, e0, e0 + s.window);
+        }
+      }
       if (rc == MOE_OK && c0 + chunk < s0 + ns) rc = lists(c0 + chunk, chunk_idx + 1);
       if (rc == MOE_OK) rc = combine(c0, chunk_idx);
       if (rc != MOE_OK) return join(rc);
@@ -705,9 +795,11 @@ moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* 
 
 void moe_prefill_destroy(moe_plan_t p) {
   if (!p) return;
-  for (cudaEvent_t e : {p->ev_fork, p->ev_span, p->ev_join, p->ev_ready[0], p->ev_ready[1], p->ev_down, p->ev_comb})
+  for (cudaEvent_t e : {p->ev_fork, p->ev_span, p->ev_join, p->ev_ready[0], p->ev_ready[1], p->ev_down, p->ev_comb,
+                        p->ev_copy[0], p->ev_copy[1], p->ev_rel[0], p->ev_rel[1]})
     if (e) cudaEventDestroy(e);
   if (p->side) cudaStreamDestroy(p->side);
+  if (p->own_copy) cudaStreamDestroy(p->own_copy);
   for (auto& t : p->pending) {
     if (t.a) cudaEventDestroy(t.a);
     if (t.b) cudaEventDestroy(t.b);
@@ -777,6 +869,7 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
   cl.b_group_rows = 0;
   cl.out_cols = n;
   cl.b_stream = 0;
+  cl.b_group_mod = 0;
   cl.out_ld = n;
   cl.out = c;
   int n_tiles;

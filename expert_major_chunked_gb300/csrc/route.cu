@@ -587,6 +587,14 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(PermuteParams p) {
   const int n_gu_all = n_gu + (p.nt_gu_shared > 0 ? mts * p.nt_gu_shared : 0);
   const int n_dn_all = n_dn + (p.nt_down_shared > 0 ? mts * p.nt_down_shared : 0);
   const bool fits = n_gu_all <= p.cap_gu && n_dn_all <= p.cap_down;
+  if (e < E) {
+    p.tile_base[e] = gu_base;
+    p.tile_base[E + 1 + e] = dn_base;
+  }
+  if (threadIdx.x == 0) {
+    p.tile_base[E] = n_gu;
+    p.tile_base[E + 1 + E] = n_dn;
+  }
   if (fits && e < E) {
     // an expert with a single M tile is the only reader of its weight tiles: mark them for streaming
     const int stream = (mt == 1) ? static_cast<int>(1u << 31) : 0;

@@ -66,7 +66,9 @@ typedef struct {
   int32_t shared_inter;  /* I_s: 0 = no shared expert, else a multiple of 64 */
   int32_t renormalize;   /* must be 1: weights are the softmax over the selected logits */
   int32_t max_chunk;     /* largest chunk size (tokens) a run may use; sizes the workspace */
-  int32_t offload_slots; /* must be 0 for moe_prefill_run (weights resident in device memory) */
+  int32_t offload_slots; /* 0: expert weights resident in device memory. S > 0: w_gu / w_down are pinned host
+                            banks, streamed through a ring of S expert slots in the workspace (S even, S <= E,
+                            S/2 divides E) */
 } moe_dims;
 
 typedef struct moe_plan* moe_plan_t;
@@ -78,6 +80,11 @@ typedef struct moe_plan* moe_plan_t;
  *   w_gu            device bf16 [E][2I][H] (gate rows, then up rows, per expert).
  *   w_down          device bf16 [E][H][I].
  *   ws_gu, ws_down  device bf16 [2I_s][H] and [H][I_s]; both NULL when shared_inter == 0.
+ *   With offload_slots = S > 0, w_gu and w_down are page-locked HOST memory (cudaHostAlloc / cudaHostRegister)
+ *   in the same layouts; the router and shared-expert weights stay in device memory. (Offloaded experts follow
+ *   the umbrella PR #1113, "What it adds" / "Memory and execution split": pinned host banks, device expert
+ *   lines, asynchronous host-to-device staging; and the deep-prefill draft, "What": a ring of staged expert
+ *   lines overlapped with compute.)
  *   workspace_bytes out: bytes of device workspace moe_prefill_run needs for chunks up to max_chunk.
  *   plan            out: the plan; free it with moe_prefill_destroy.
  * Requires the current device to be sm_103 (else MOE_ERR_ARCH). Allocates no device memory. Thread-compatible:
@@ -99,8 +106,12 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
  *   expert_offsets  device int32 [n_chunks][E+1] or NULL: per-chunk exclusive offsets of each expert's rows.
  *   row_token       device int32 [T*k] or NULL: row j of chunk c (chunk-local index) at c*chunk*k + j holds the
  *                   global id of the token placed in that row (rows ordered by expert, then token).
- *   compute         stream for all work.
- *   copy            must be NULL (reserved for the offloaded-expert variant).
+ *   compute         stream for all kernels.
+ *   copy            resident weights: must be NULL. Offloaded experts: the stream for the host-to-device expert
+ *                   copies, or NULL for one owned by the plan. For every chunk the experts are staged in windows of
+ *                   S/2 consecutive experts (two copies per window: gate/up and down) into alternate halves of the
+ *                   ring; a window's GEMMs wait for its copies and a copy waits until the GEMMs of the window
+ *                   that last used its half have finished. Every expert is staged for every chunk.
  * Returns after enqueueing; call moe_prefill_check(workspace, compute) for device-side errors.
  */
 moe_status moe_prefill_run(moe_plan_t plan, const void* x, int64_t T, int32_t chunk, void* workspace,

@@ -66,6 +66,9 @@ def test_plan_rejects_bad_dims_before_device_use(L):
         (b.moe_dims(256, 16, 128, 2, 0, 1, 0, 0), -1),       # max_chunk < 1
         (b.moe_dims(-256, 16, 128, 2, 0, 1, 64, 0), -1),     # negative size
         (b.moe_dims(256, 16, 128, 2, 32, 1, 64, 0), -2),     # shared_inter not a multiple of 64
+        (b.moe_dims(256, 16, 128, 2, 0, 1, 64, 3), -2),      # odd ring size
+        (b.moe_dims(256, 16, 128, 2, 0, 1, 64, 6), -2),      # half the ring (3) does not divide 16 experts
+        (b.moe_dims(256, 16, 128, 2, 0, 1, 64, 32), -2),     # ring larger than the expert count
     ]
     fake = ctypes.c_void_p(0x1000)
     for dims, want in cases:
