@@ -176,14 +176,14 @@ def kernel_source_hash() -> str:
 
 def ncu_traffic(workload: str, chunk: int):
     """DRAM bytes per gate/up launch from the committed ncu summary, if it was taken on the current kernel."""
-    path = os.path.join(ROOT, "profiles", f"gate_up_traffic_{workload}_c{chunk}.json")
+    import re
+    path = os.path.join(ROOT, "profiles", f"gate_up_{workload}_c{chunk}.md")
     if not os.path.exists(path):
         return None
-    with open(path) as f:
-        d = json.load(f)
-    if d.get("kernel_source_hash") != kernel_source_hash():
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+kernel_source_hash:\s*([0-9a-f]+)", open(path).read())
+    if not m or m.group(2) != kernel_source_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    return int(m.group(1))
 
 
 # ------------------------------------------------------------------------------------------------ reference arm
