@@ -258,7 +258,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;
-    const int row = q * 32 + lane;
+    uint32_t* stage = reinterpret_cast<uint32_t*>(bars_ptr + 256) + (warp - 2) * (32 * 33);
     int local = 0;
     for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
       const TileInfo ti = decode_tile(p, t);
@@ -273,48 +273,64 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
       ptx::tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kMaxN);
-      const bool valid = row < ti.rows;
-      const int64_t orow = static_cast<int64_t>(ti.out_row0) + row;
+      // Each warp owns a 32-row slab of the tile. A 32-column block of the accumulator arrives one row per lane;
+      // it is staged in shared memory (odd row stride: no bank conflicts) and written back row-contiguously, so
+      // every store instruction covers whole 128-byte lines instead of 32 different rows.
+      const int slab_rows = ti.rows - q * 32;
+      const int64_t slab_row0 = static_cast<int64_t>(ti.out_row0) + q * 32;
       if (EPI == kEpiSwiGLU) {
         const int half = C.b_box_rows;
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(C.out) + orow * C.out_ld + static_cast<int64_t>(ti.n_idx) * half;
+        const int64_t ldw = C.out_ld / 2;  // row stride in 32-bit words (two bf16 each)
+        uint32_t* outw = reinterpret_cast<uint32_t*>(C.out) + (static_cast<int64_t>(ti.n_idx) * half) / 2;
         for (int c = 0; c < half; c += 32) {
           uint32_t g[32], u[32];
           ptx::tmem_ld32(tbase + c, g);
           ptx::tmem_ld32(tbase + half + c, u);
           ptx::tmem_ld_wait();
-          uint32_t hp[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            hp[i] = pack_bf16(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                              swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(out + c);
+            stage[lane * 17 + i] = pack_bf16(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                             swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+          __syncwarp();
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(hp[4 * v], hp[4 * v + 1], hp[4 * v + 2], hp[4 * v + 3]);
+          for (int m = 0; m < 4; ++m) {
+            const int r = m * 8 + (lane >> 2), w0 = (lane & 3) * 4;
+            if (r < slab_rows) {
+              const uint32_t* sr = stage + r * 17 + w0;
+              *reinterpret_cast<uint4*>(outw + (slab_row0 + r) * ldw + c / 2 + w0) = make_uint4(sr[0], sr[1], sr[2], sr[3]);
+            }
           }
+          __syncwarp();
         }
       } else {
         const int col0 = ti.n_idx * C.n_tile;
-        float* out = static_cast<float*>(C.out) + orow * C.out_ld + col0;
+        float* outb = static_cast<float*>(C.out) + col0;
         const bool vec = (C.out_ld % 4) == 0;
         for (int c = 0; c < C.n_tile; c += 32) {
           uint32_t v[32];
           ptx::tmem_ld32(tbase + c, v);
           ptx::tmem_ld_wait();
-          if (valid) {
-            if (vec && col0 + c + 32 <= C.out_cols) {
-              float4* dst = reinterpret_cast<float4*>(out + c);
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-            } else {
+          for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
+          __syncwarp();
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + c + j < C.out_cols) out[c + j] = __uint_as_float(v[j]);
+          for (int m = 0; m < 8; ++m) {
+            const int r = m * 4 + (lane >> 3), cc = (lane & 7) * 4;
+            if (r < slab_rows) {
+              const uint32_t* sr = stage + r * 33 + cc;
+              float* dst = outb + (slab_row0 + r) * C.out_ld + c + cc;
+              const int gc = col0 + c + cc;
+              if (vec && gc + 4 <= C.out_cols) {
+                *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(sr[0]), __uint_as_float(sr[1]),
+                                                              __uint_as_float(sr[2]), __uint_as_float(sr[3]));
+              } else {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                  if (gc + jj < C.out_cols) dst[jj] = __uint_as_float(sr[jj]);
+              }
             }
           }
+          __syncwarp();
         }
       }
       ptx::tc_fence_before();

@@ -47,7 +47,8 @@ constexpr int kABoxRows = 32;       // A rows per TMA box (a tile loads ceil(row
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM alloc, warps 2..5 epilogue
 constexpr int kStageABytes = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBBytes = kMaxN * kBlockK * 2;     // 32 KB
-constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + 256;
+constexpr int kEpiStageBytes = 4 * 32 * 33 * 4;            // epilogue staging: a 32 x 33-word block per warp
+constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + 256 + kEpiStageBytes;
 
 enum Epilogue : int { kEpiF32 = 0, kEpiSwiGLU = 1 };
 
