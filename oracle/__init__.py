@@ -56,9 +56,12 @@ def lib():
             L.oracle_permutation.argtypes = [P, i64, i32, i32, i32, P, P, P]
             L.oracle_combine_f64.argtypes = [P, P, P, P, i64, i32, i32, P, P]
             L.oracle_combine_f32_canonical.argtypes = [P, P, P, P, i64, i32, i32, P]
+            L.oracle_combine_tree_partial_f64.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, P]
+            L.oracle_combine_tree_finish_f64.argtypes = [P, i32, P, i64, i32, P, P]
             for name in ("oracle_bf16_round_array", "oracle_router_logits", "oracle_topk", "oracle_swiglu_ffn",
                          "oracle_moe_forward", "oracle_permutation", "oracle_combine_f64",
-                         "oracle_combine_f32_canonical"):
+                         "oracle_combine_f32_canonical", "oracle_combine_tree_partial_f64",
+                         "oracle_combine_tree_finish_f64"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -203,3 +206,32 @@ def combine_f32_canonical(y, w, token_row, s=None):
     _check(lib().oracle_combine_f32_canonical(_ptr(y), _ptr(w), _ptr(tr), _ptr(s) if s is not None else None,
                                               n, k, H, _ptr(out)), "combine_f32_canonical")
     return out
+
+
+def combine_tree_partial_f64(y, w, token_row, topk_id, n_experts, n_parts=1, part=0):
+    """float64 value of one aligned block of the expert-id tree (part `part` of `n_parts`); [n][H] float64."""
+    y, w, tr, _ = _combine_args(y, w, token_row, None)
+    ids = np.ascontiguousarray(topk_id, dtype=np.int32)
+    n, k = w.shape
+    H = y.shape[1]
+    out = np.empty((n, H), dtype=np.float64)
+    _check(lib().oracle_combine_tree_partial_f64(_ptr(y), _ptr(w), _ptr(tr), _ptr(ids), n, k, H, n_experts, n_parts,
+                                                 part, _ptr(out)), "combine_tree_partial_f64")
+    return out
+
+
+def combine_tree_finish_f64(partials, s=None):
+    """Sum the parts in the tree, add the shared expert, round once to float32, then to bf16: (f32, bf16 bits)."""
+    parts = np.ascontiguousarray(np.stack(list(partials)), dtype=np.float64)
+    R, n, H = parts.shape
+    s = None if s is None else np.ascontiguousarray(s, dtype=np.float32)
+    f32 = np.empty((n, H), dtype=np.float32)
+    bf = np.empty((n, H), dtype=np.uint16)
+    _check(lib().oracle_combine_tree_finish_f64(_ptr(parts), R, _ptr(s) if s is not None else None, n, H, _ptr(f32),
+                                                _ptr(bf)), "combine_tree_finish_f64")
+    return f32, bf
+
+
+def combine_tree_f64(y, w, token_row, topk_id, n_experts, s=None):
+    """The unsplit float64 tree combine: one part, then the finish."""
+    return combine_tree_finish_f64([combine_tree_partial_f64(y, w, token_row, topk_id, n_experts)], s)

@@ -304,3 +304,97 @@ int oracle_combine_f32_canonical(const float* y, const float* w, const int32_t* 
     }
   return 0;
 }
+
+/*
+ * Expert-parallel combine with float64 partials. [DP-b] "What this changes": the tensor-parallel prefill partials
+ * are float64; "Checklist": they are summed in float64 and rounded once, to float32, at the finish, so a two-GPU
+ * split reproduces the one-GPU sum. The pages leave the order inside a partial open. Reading: a complete binary
+ * tree over the expert ids, evaluated densely here (every expert a leaf, +0.0 where the token has no slot), so that
+ * each aligned block of ids is a subtree and a split into such blocks changes no operation.
+ */
+static double tree_sum_f64(const double* v, int64_t len) {
+  if (len == 1) return v[0];
+  const double left = tree_sum_f64(v, len / 2);
+  const double right = tree_sum_f64(v + len / 2, len / 2);
+  return left + right;
+}
+
+static int32_t least_pow2_at_least(int32_t v) {
+  int32_t p = 1;
+  while (p < v) p *= 2;
+  return p;
+}
+
+static int is_pow2(int32_t v) { return v > 0 && (v & (v - 1)) == 0; }
+
+int oracle_combine_tree_partial_f64(const float* y, const float* w, const int32_t* token_row, const int32_t* topk_id,
+                                    int64_t n, int32_t top_k, int32_t hidden, int32_t n_experts, int32_t n_parts,
+                                    int32_t part, double* partial) {
+  if (!w || !topk_id || !partial || n < 0 || top_k < 1 || hidden < 1 || n_experts < 1) return -1;
+  const int32_t Ep = least_pow2_at_least(n_experts);
+  if (!is_pow2(n_parts) || n_parts > Ep || part < 0 || part >= n_parts) return -1;
+  const int32_t block = Ep / n_parts;
+  const int32_t lo = part * block;
+  for (int64_t i = 0; i < n * top_k; ++i)
+    if (topk_id[i] < 0 || topk_id[i] >= n_experts) return -1;
+  for (int64_t t = 0; t < n; ++t)
+    for (int32_t a = 0; a < top_k; ++a)
+      for (int32_t b = a + 1; b < top_k; ++b)
+        if (topk_id[t * top_k + a] == topk_id[t * top_k + b]) return -1;
+  if (n > 0 && !y && block > 0) {
+    for (int64_t i = 0; i < n * top_k; ++i)
+      if (topk_id[i] >= lo && topk_id[i] < lo + block) return -1;
+  }
+  int rc = 0;
+#pragma omp parallel
+  {
+    double* leaves = (double*)malloc(sizeof(double) * (size_t)block);
+    if (!leaves) {
+#pragma omp atomic write
+      rc = -1;
+    }
+#pragma omp for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+      if (!leaves) continue;
+      for (int32_t o = 0; o < hidden; ++o) {
+        for (int32_t e = 0; e < block; ++e) leaves[e] = 0.0;
+        for (int32_t s = 0; s < top_k; ++s) {
+          const int32_t e = topk_id[t * top_k + s];
+          if (e < lo || e >= lo + block) continue;
+          const int64_t row = token_row[t * top_k + s];
+          leaves[e - lo] = (double)w[t * top_k + s] * (double)y[row * hidden + o];
+        }
+        partial[t * hidden + o] = tree_sum_f64(leaves, block);
+      }
+    }
+    free(leaves);
+  }
+  return rc;
+}
+
+int oracle_combine_tree_finish_f64(const double* partials, int32_t n_parts, const float* s_shared, int64_t n,
+                                   int32_t hidden, float* out_f32, uint16_t* out_bf16) {
+  if (!partials || !is_pow2(n_parts) || n < 0 || hidden < 1) return -1;
+  const int64_t plane = n * hidden;
+  int rc = 0;
+#pragma omp parallel
+  {
+    double* parts = (double*)malloc(sizeof(double) * (size_t)n_parts);
+    if (!parts) {
+#pragma omp atomic write
+      rc = -1;
+    }
+#pragma omp for schedule(static)
+    for (int64_t i = 0; i < plane; ++i) {
+      if (!parts) continue;
+      for (int32_t p = 0; p < n_parts; ++p) parts[p] = partials[p * plane + i];
+      double v = tree_sum_f64(parts, n_parts);
+      if (s_shared) v = v + (double)s_shared[i];
+      const float f = (float)v;
+      if (out_f32) out_f32[i] = f;
+      if (out_bf16) out_bf16[i] = oracle_bf16_from_double((double)f);
+    }
+    free(parts);
+  }
+  return rc;
+}

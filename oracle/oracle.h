@@ -18,7 +18,8 @@
  * Parity pins (the tests): bf16 rounding against closed-form midpoint cases and a library conversion; router
  * logits against a library matmul; top-k against routing invariants and planted ties; the FFN against a textbook
  * numpy SwiGLU; the whole layer against a numpy dense masked evaluation (every expert) and a hand-worked example;
- * the permutation against a stable library sort; the fp32 combine against hand-built exact and midpoint cases.
+ * the permutation against a stable library sort; the fp32 combine against hand-built exact and midpoint cases; the
+ * float64 tree combine against a hand-worked example (order, signed zeros, the float32 step) and exact integer sums.
  *
  * Conventions: BF16 values are passed as their uint16 bit patterns and decoded exactly. Row-major layouts.
  * All functions return 0 on success and -1 on a bad argument.
@@ -83,6 +84,27 @@ int oracle_combine_f64(const float* y, const float* w, const int32_t* token_row,
    and add rounded to float32 (no contraction); then acc = acc + s_shared; out = bf16 RNE of acc. */
 int oracle_combine_f32_canonical(const float* y, const float* w, const int32_t* token_row, const float* s_shared,
                                  int64_t n, int32_t top_k, int32_t hidden, uint16_t* out_bf16);
+
+/*
+ * Expert-parallel combine with float64 partials ([DP-b] "What this changes", "Checklist"). The routed contributions
+ * of one output element are the leaves of a complete binary tree over the expert ids 0 .. Ep-1 (Ep = the least power
+ * of two >= n_experts): leaf e = (double)w * (double)y for the slot routed to expert e (exact: a product of two
+ * floats fits in a double), +0.0 for every expert the token did not choose; each inner node = left + right in
+ * float64, round to nearest. An expert-parallel split has n_parts aligned blocks of Ep/n_parts ids (n_parts a power
+ * of two, 1 <= n_parts <= Ep): part p holds the experts [p*Ep/n_parts, (p+1)*Ep/n_parts), i.e. one subtree.
+ *
+ * Partial: partial[t][o] = value of part `part`'s subtree. topk_id [n][k]: the slots' expert ids, distinct within a
+ * token, in any order; token_row is read only for slots whose expert is in the part.
+ */
+int oracle_combine_tree_partial_f64(const float* y, const float* w, const int32_t* token_row, const int32_t* topk_id,
+                                    int64_t n, int32_t top_k, int32_t hidden, int32_t n_experts, int32_t n_parts,
+                                    int32_t part, double* partial);
+
+/* Finish: the parts' values [n_parts][n][H] summed in the same tree (float64), then + s_shared[t][o] (float64),
+   then ONE rounding to float32 (out_f32), then that float rounded to bf16, ties to even (out_bf16). Either output
+   may be NULL; s_shared may be NULL. */
+int oracle_combine_tree_finish_f64(const double* partials, int32_t n_parts, const float* s_shared, int64_t n,
+                                   int32_t hidden, float* out_f32, uint16_t* out_bf16);
 
 #ifdef __cplusplus
 }

@@ -368,3 +368,102 @@ def test_combine_f64_matches_library(oracle_lib):
     ref, _ = oracle_lib.combine_f64(y, w, tr, s)
     exact = np.einsum("nk,nkh->nh", w.astype(np.float64), y[tr].astype(np.float64)) + s
     np.testing.assert_allclose(ref, exact, rtol=1e-14, atol=1e-15)
+
+
+# ---------------------------------------------------------------- float64 tree combine (expert-parallel partials)
+
+def _tree_fixture():
+    fx = read_fixture("hand_worked_tree_combine.txt")
+    n, k, E, H = (int(v) for v in fx["dims"])
+    f = lambda key, dt: np.array(fx[key], dtype=dt)
+    return (n, k, E, H, f("y", np.float32).reshape(n * k, H), f("w", np.float32).reshape(n, k),
+            f("token_row", np.int32).reshape(n, k), f("topk_id", np.int32).reshape(n, k),
+            f("s", np.float32).reshape(n, H), fx)
+
+
+def _same_bits(a, b):
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b, dtype=a.dtype)
+    np.testing.assert_array_equal(a.view(np.uint64 if a.itemsize == 8 else np.uint32),
+                                  b.view(np.uint64 if b.itemsize == 8 else np.uint32))
+
+
+def test_tree_combine_hand_worked_example(oracle_lib):
+    n, k, E, H, y, w, tr, ids, s, fx = _tree_fixture()
+    for part in (0, 1):
+        got = oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E, n_parts=2, part=part)
+        _same_bits(got, np.array(fx[f"part{part}"], dtype=np.float64).reshape(n, H))  # signed zeros included
+    whole = oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E)
+    f32, bf = oracle_lib.combine_tree_finish_f64([whole])
+    _same_bits(f32, np.array(fx["out_f32_no_shared"], dtype=np.float32).reshape(n, H))
+    np.testing.assert_array_equal(bf, np.array(fx["out_bf16_no_shared"], dtype=np.uint16).reshape(n, H))
+    for parts in (1, 2, 4):
+        pieces = [oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E, parts, p) for p in range(parts)]
+        f32, bf = oracle_lib.combine_tree_finish_f64(pieces, s)
+        _same_bits(f32, np.array(fx["out_f32"], dtype=np.float32).reshape(n, H))
+        np.testing.assert_array_equal(bf, np.array(fx["out_bf16"], dtype=np.uint16).reshape(n, H))
+    # the ascending-id float64 sum of the same slots differs in t0 c0: the order is part of the definition
+    ref, _ = oracle_lib.combine_f64(y, w, tr)
+    assert ref[0, 0] == 0.0 and whole[0, 0] == 1.0
+
+
+@pytest.mark.parametrize("E,k", [(48, 6), (64, 8), (16, 1)])
+def test_tree_combine_exact_integer_sums(oracle_lib, E, k):
+    """Integer y and power-of-two weights keep every partial sum exact, so any tree equals the exact sum."""
+    rng = np.random.default_rng(21 + E)
+    n, H = 37, 12
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(n)]).astype(np.int32)
+    w = (2.0 ** rng.integers(-4, 3, size=(n, k))).astype(np.float32)
+    y = rng.integers(-2 ** 20, 2 ** 20, size=(n * k, H)).astype(np.float32)
+    s = rng.integers(-2 ** 20, 2 ** 20, size=(n, H)).astype(np.float32)
+    tr = rng.permutation(n * k).reshape(n, k).astype(np.int32)
+    exact = [[sum(int(y[tr[t, j], o]) * float(w[t, j]) for j in range(k)) for o in range(H)] for t in range(n)]
+    whole = oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E)
+    np.testing.assert_array_equal(whole, np.array(exact))
+    f32, bf = oracle_lib.combine_tree_finish_f64([whole], s)
+    np.testing.assert_array_equal(f32.astype(np.float64), (np.array(exact) + s).astype(np.float32))
+    np.testing.assert_array_equal(oracle_lib.bf16_to_double(bf), _bf16_round_torch(f32.astype(np.float64)))
+    Ep = 1 << (E - 1).bit_length()
+    for parts in (2, Ep):
+        lo = [p * Ep // parts for p in range(parts)]
+        for p in range(parts):
+            got = oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E, parts, p)
+            inside = (ids >= lo[p]) & (ids < lo[p] + Ep // parts)
+            want = np.einsum("nk,nkh->nh", np.where(inside, w, 0).astype(np.float64), y[tr].astype(np.float64))
+            np.testing.assert_array_equal(got, want)
+
+
+def test_tree_combine_split_reproduces_whole(oracle_lib):
+    rng = np.random.default_rng(22)
+    n, k, E, H = 29, 8, 96, 20
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(n)]).astype(np.int32)
+    w = rng.random((n, k)).astype(np.float32)
+    y = (rng.standard_normal((n * k, H)) * 10.0 ** rng.integers(-6, 7, size=(n * k, H))).astype(np.float32)
+    s = rng.standard_normal((n, H)).astype(np.float32)
+    tr = rng.permutation(n * k).reshape(n, k).astype(np.int32)
+    f_whole, b_whole = oracle_lib.combine_tree_f64(y, w, tr, ids, E, s)
+    for parts in (2, 4, 8, 32, 128):
+        pieces = [oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E, parts, p) for p in range(parts)]
+        f32, bf = oracle_lib.combine_tree_finish_f64(pieces, s)
+        _same_bits(f32, f_whole)
+        np.testing.assert_array_equal(bf, b_whole)
+    # within the float64 error bound of the exact sum (math.fsum), then one float32 rounding
+    whole = oracle_lib.combine_tree_partial_f64(y, w, tr, ids, E)
+    depth = 7  # log2(128)
+    for t in range(n):
+        for o in range(H):
+            terms = [float(w[t, j]) * float(y[tr[t, j], o]) for j in range(k)]
+            bound = depth * 2.0 ** -53 * sum(abs(v) for v in terms)
+            assert abs(whole[t, o] - math.fsum(terms)) <= bound
+
+
+def test_tree_combine_rejects_bad_arguments(oracle_lib):
+    y = np.ones((4, 2), np.float32)
+    w = np.ones((2, 2), np.float32)
+    tr = np.array([[0, 1], [2, 3]], np.int32)
+    with pytest.raises(ValueError):
+        oracle_lib.combine_tree_partial_f64(y, w, tr, np.array([[1, 1], [0, 2]], np.int32), 4)   # repeated id
+    with pytest.raises(ValueError):
+        oracle_lib.combine_tree_partial_f64(y, w, tr, np.array([[0, 4], [1, 2]], np.int32), 4)   # id >= E
+    with pytest.raises(ValueError):
+        oracle_lib.combine_tree_partial_f64(y, w, tr, np.array([[0, 1], [1, 2]], np.int32), 4, 3, 0)  # 3 parts
