@@ -41,6 +41,13 @@ _SIGS = {
     "moe_prefill_run": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
     "moe_prefill_combine": ([_P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
+    "moe_prefill_combine_partial_f64": ([_P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
+    "moe_prefill_combine_finish_f64": ([_P, ctypes.c_int32, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P],
+                                       ctypes.c_int),
+    "moe_prefill_combine_f64": ([_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                 _P, _P, _P], ctypes.c_int),
+    "moe_prefill_set_combine": ([_P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_check": ([_P, _P], ctypes.c_int),
     "moe_prefill_destroy": ([_P], None),
     "moe_prefill_last_error": ([], ctypes.c_char_p),
@@ -108,6 +115,29 @@ def moe_prefill_run_noalloc(plan, x, T, chunk, out, topk_id=None, topk_w=None, e
 
 def moe_prefill_combine(y, w, token_row, s, n, k, H, out, stream=None):
     _check(lib().moe_prefill_combine(y, w, token_row, s, n, k, H, out, stream))
+
+
+def moe_prefill_combine_partial_f64(y, w, token_row, topk_id, n, k, H, n_experts, n_parts, part, partial,
+                                    stream=None):
+    _check(lib().moe_prefill_combine_partial_f64(y, w, token_row, topk_id, n, k, H, n_experts, n_parts, part,
+                                                 partial, stream))
+
+
+def moe_prefill_combine_finish_f64(partials, s, n, H, out, out_f32=None, stream=None):
+    """partials: list of device pointers (one per part, part 0 first)."""
+    arr = (ctypes.c_void_p * len(partials))(*partials)
+    _check(lib().moe_prefill_combine_finish_f64(arr, len(partials), s, n, H, out, out_f32, stream))
+
+
+def moe_prefill_combine_f64(y, w, token_row, topk_id, s, n, k, H, n_experts, out, out_f32=None, stream=None):
+    _check(lib().moe_prefill_combine_f64(y, w, token_row, topk_id, s, n, k, H, n_experts, out, out_f32, stream))
+
+
+COMBINE_F32, COMBINE_F64_TREE = 0, 1
+
+
+def moe_prefill_set_combine(plan, mode: int):
+    _check(lib().moe_prefill_set_combine(plan, mode))
 
 
 def moe_prefill_check(workspace, stream=None) -> int:
@@ -209,6 +239,10 @@ class MoePrefill:
                         out.data_ptr(), _ptr(topk_id), _ptr(topk_w), _ptr(expert_offsets), _ptr(row_token),
                         _stream_handle(stream), copy_stream.cuda_stream if copy_stream is not None else None)
         return out
+
+    def set_combine(self, mode: int):
+        """COMBINE_F32 (canonical float32, ascending expert id; default) or COMBINE_F64_TREE."""
+        moe_prefill_set_combine(self.plan, mode)
 
     def check(self, stream=None) -> int:
         return moe_prefill_check(self.workspace.data_ptr(), _stream_handle(stream))

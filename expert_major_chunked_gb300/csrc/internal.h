@@ -146,6 +146,35 @@ cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
 cudaError_t launch_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
                            int k, int H, uint16_t* out, cudaStream_t stream);
 
+// ------------------------------------------------------------------ float64 tree combine (expert-parallel parts)
+struct CombineTreeParams {
+  const float* y;            // [R][H]
+  const float* w;            // [n][k]
+  const int32_t* token_row;  // [n][k]
+  const int32_t* topk_id;    // [n][k]
+  const float* s;            // [n][H] or null (finish only)
+  double* partial;           // [n][H] (part only)
+  uint16_t* out;             // bf16 [n][H] (finish only)
+  float* out_f32;            // [n][H] or null (finish only)
+  int64_t n;
+  int32_t k, H;
+  int32_t lo, block_log2;    // the part's experts: [lo, lo + 2^block_log2)
+};
+constexpr int kMaxFinishParts = 16;
+struct CombineFinishParams {
+  const double* part[kMaxFinishParts];  // n_parts arrays of count values
+  const float* s;
+  uint16_t* out;
+  float* out_f32;
+  int64_t count;  // n * H (even)
+  int32_t n_parts;
+};
+size_t combine_tree_smem_bytes(int k);
+// finish = false: write the part's float64 values to a.partial; true: the unsplit combine (one part covering all
+// experts), + s, float32, bf16 in the same kernel.
+cudaError_t launch_combine_tree(const CombineTreeParams& a, bool finish, cudaStream_t stream);
+cudaError_t launch_combine_finish(const CombineFinishParams& a, int num_sms, cudaStream_t stream);
+
 // ------------------------------------------------------------------ host helpers shared with noalloc.cu
 void set_last_error(const char* msg);
 

@@ -35,6 +35,12 @@ moe_status fail(moe_status st, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int ceil_log2(int v) {
+  int l = 0;
+  while ((1 << l) < v) ++l;
+  return l;
+}
+
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ TMA descriptor encoding
@@ -206,6 +212,7 @@ struct moe_plan {
   cudaEvent_t ev_fork = nullptr, ev_span = nullptr, ev_join = nullptr, ev_ready[2] = {}, ev_down = nullptr,
               ev_comb = nullptr;
   uint64_t timeout_ns = 2000000000ull;
+  int32_t combine_mode = MOE_COMBINE_F32;
   int64_t launches = 0;
   bool profiling = false;
   struct Timed {
@@ -719,14 +726,31 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       const int par = static_cast<int>(cidx & 1);
       moe_status r2 = cuda_status(cudaStreamWaitEvent(side, p->ev_down, 0), "down wait");
       if (r2 != MOE_OK) return r2;
-      // 8. canonical combine
+      // 8. canonical combine (float32, ascending expert id) or the float64 tree over the expert ids
       {
         LaunchScope ls(p, MOE_KERNEL_COMBINE, side);
-        r2 = cuda_status(launch_combine(y, span_w + (c0 - s0) * s.k,
-                                        reinterpret_cast<const int32_t*>(ws + L.token_row[par]),
-                                        s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
-                                        static_cast<uint16_t*>(out) + c0 * s.H, side),
-                         "combine launch");
+        if (p->combine_mode == MOE_COMBINE_F64_TREE) {
+          CombineTreeParams a;
+          memset(&a, 0, sizeof a);
+          a.y = y;
+          a.w = span_w + (c0 - s0) * s.k;
+          a.token_row = reinterpret_cast<const int32_t*>(ws + L.token_row[par]);
+          a.topk_id = span_ids + (c0 - s0) * s.k;
+          a.s = s.Is > 0 ? sbuf : nullptr;
+          a.out = static_cast<uint16_t*>(out) + c0 * s.H;
+          a.n = n;
+          a.k = s.k;
+          a.H = s.H;
+          a.lo = 0;
+          a.block_log2 = ceil_log2(s.E);
+          r2 = cuda_status(launch_combine_tree(a, true, side), "combine launch");
+        } else {
+          r2 = cuda_status(launch_combine(y, span_w + (c0 - s0) * s.k,
+                                          reinterpret_cast<const int32_t*>(ws + L.token_row[par]),
+                                          s.Is > 0 ? sbuf : nullptr, n, s.k, s.H,
+                                          static_cast<uint16_t*>(out) + c0 * s.H, side),
+                           "combine launch");
+        }
       }
       if (r2 != MOE_OK) return r2;
       return cuda_status(cudaEventRecord(p->ev_comb, side), "combine event");
@@ -765,6 +789,105 @@ moe_status moe_prefill_combine(const float* y, const float* w, const int32_t* to
   return cuda_status(launch_combine(y, w, token_row, s, n, k, H, static_cast<uint16_t*>(out),
                                     reinterpret_cast<cudaStream_t>(stream)),
                      "combine launch");
+}
+
+static moe_status check_tree_args(const float* y, const float* w, const int32_t* token_row, const int32_t* topk_id,
+                                  int64_t n, int32_t k, int32_t H, int32_t n_experts) {
+  if (n < 0 || k < 1 || k > 32 || H <= 0 || H % 4 != 0)
+    return fail(MOE_ERR_INVALID_ARG, "need n >= 0, 1 <= k <= 32, H a positive multiple of 4");
+  if (n_experts < 1 || n_experts > 1024) return fail(MOE_ERR_INVALID_ARG, "need 1 <= n_experts <= 1024");
+  if (n >= (1ll << 31)) return fail(MOE_ERR_UNSUPPORTED, "n must be below 2^31");
+  if (n > 0 && (!y || !w || !token_row || !topk_id))
+    return fail(MOE_ERR_INVALID_ARG, "y, w, token_row and topk_id must not be NULL");
+  if (n > 0 && !aligned16(y)) return fail(MOE_ERR_INVALID_ARG, "y must be 16-byte aligned");
+  return MOE_OK;
+}
+
+moe_status moe_prefill_combine_partial_f64(const float* y, const float* w, const int32_t* token_row,
+                                           const int32_t* topk_id, int64_t n, int32_t k, int32_t H,
+                                           int32_t n_experts, int32_t n_parts, int32_t part, double* partial,
+                                           moe_stream_t stream) {
+  moe_status st = check_tree_args(y, w, token_row, topk_id, n, k, H, n_experts);
+  if (st != MOE_OK) return st;
+  const int lg = ceil_log2(n_experts);
+  if (n_parts < 1 || (n_parts & (n_parts - 1)) != 0 || n_parts > (1 << lg) || part < 0 || part >= n_parts)
+    return fail(MOE_ERR_INVALID_ARG, "n_parts must be a power of two <= %d and 0 <= part < n_parts", 1 << lg);
+  if (n == 0) return MOE_OK;
+  if (!partial || !aligned16(partial)) return fail(MOE_ERR_INVALID_ARG, "partial must be a 16-byte aligned pointer");
+  CombineTreeParams a;
+  memset(&a, 0, sizeof a);
+  a.y = y;
+  a.w = w;
+  a.token_row = token_row;
+  a.topk_id = topk_id;
+  a.partial = partial;
+  a.n = n;
+  a.k = k;
+  a.H = H;
+  a.block_log2 = lg - ceil_log2(n_parts);
+  a.lo = part << a.block_log2;
+  return cuda_status(launch_combine_tree(a, false, reinterpret_cast<cudaStream_t>(stream)), "combine part launch");
+}
+
+moe_status moe_prefill_combine_finish_f64(const double* const* partials, int32_t n_parts, const float* s, int64_t n,
+                                          int32_t H, void* out, float* out_f32, moe_stream_t stream) {
+  if (n < 0 || H <= 0 || H % 4 != 0) return fail(MOE_ERR_INVALID_ARG, "need n >= 0 and H a positive multiple of 4");
+  if (n_parts < 1 || n_parts > kMaxFinishParts || (n_parts & (n_parts - 1)) != 0)
+    return fail(MOE_ERR_INVALID_ARG, "n_parts must be a power of two <= %d", kMaxFinishParts);
+  if (n == 0) return MOE_OK;
+  if (!partials || !out) return fail(MOE_ERR_INVALID_ARG, "partials and out must not be NULL");
+  CombineFinishParams a;
+  memset(&a, 0, sizeof a);
+  for (int i = 0; i < n_parts; ++i) {
+    if (!partials[i] || !aligned16(partials[i]))
+      return fail(MOE_ERR_INVALID_ARG, "partials[%d] must be a 16-byte aligned device pointer", i);
+    a.part[i] = partials[i];
+  }
+  if (!aligned16(out) || (s && !aligned16(s)) || (out_f32 && !aligned16(out_f32)))
+    return fail(MOE_ERR_INVALID_ARG, "s, out and out_f32 must be 16-byte aligned");
+  a.s = s;
+  a.out = static_cast<uint16_t*>(out);
+  a.out_f32 = out_f32;
+  a.count = n * H;
+  a.n_parts = n_parts;
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  return cuda_status(launch_combine_finish(a, sms, reinterpret_cast<cudaStream_t>(stream)), "combine finish launch");
+}
+
+moe_status moe_prefill_combine_f64(const float* y, const float* w, const int32_t* token_row, const int32_t* topk_id,
+                                   const float* s, int64_t n, int32_t k, int32_t H, int32_t n_experts, void* out,
+                                   float* out_f32, moe_stream_t stream) {
+  moe_status st = check_tree_args(y, w, token_row, topk_id, n, k, H, n_experts);
+  if (st != MOE_OK) return st;
+  if (n == 0) return MOE_OK;
+  if (!out) return fail(MOE_ERR_INVALID_ARG, "out must not be NULL");
+  if (!aligned16(out) || (s && !aligned16(s)) || (out_f32 && !aligned16(out_f32)))
+    return fail(MOE_ERR_INVALID_ARG, "s, out and out_f32 must be 16-byte aligned");
+  CombineTreeParams a;
+  memset(&a, 0, sizeof a);
+  a.y = y;
+  a.w = w;
+  a.token_row = token_row;
+  a.topk_id = topk_id;
+  a.s = s;
+  a.out = static_cast<uint16_t*>(out);
+  a.out_f32 = out_f32;
+  a.n = n;
+  a.k = k;
+  a.H = H;
+  a.lo = 0;
+  a.block_log2 = ceil_log2(n_experts);
+  return cuda_status(launch_combine_tree(a, true, reinterpret_cast<cudaStream_t>(stream)), "combine launch");
+}
+
+moe_status moe_prefill_set_combine(moe_plan_t p, int32_t mode) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (mode != MOE_COMBINE_F32 && mode != MOE_COMBINE_F64_TREE)
+    return fail(MOE_ERR_INVALID_ARG, "unknown combine mode %d", mode);
+  p->combine_mode = mode;
+  return MOE_OK;
 }
 
 moe_status moe_prefill_check(void* workspace, moe_stream_t stream) {

@@ -131,6 +131,58 @@ moe_status moe_prefill_combine(const float* y, const float* w, const int32_t* to
                                int32_t k, int32_t H, void* out, moe_stream_t stream);
 
 /*
+ * Float64 combine for an expert-parallel split ("EXL3 Flash Next: deep prefill (3/8)", "What this changes": the
+ * tensor-parallel prefill partials are float64; "Checklist": they are summed in float64 and rounded once, to float32,
+ * at the finish, so a split over two GPUs reproduces one GPU bit for bit). The pages leave the order inside a partial
+ * open; this library fixes it as a complete binary tree over the expert ids 0 .. Ep-1, Ep = the least power of two
+ * >= n_experts: leaf e = w*y of the token's slot routed to expert e (the product of two floats, exact in float64),
+ * +0.0 for an expert the token did not choose; each inner node = left + right in float64 (round to nearest).
+ * A part of a split is one of n_parts aligned blocks of Ep/n_parts ids, i.e. a subtree; the finish sums the parts
+ * pairwise in the same tree, adds the shared expert's output (float64), rounds once to float32 and then to bf16
+ * (ties to even). Splitting therefore changes no operation: partial + finish over any n_parts equals
+ * moe_prefill_combine_f64 bit for bit.
+ *
+ * moe_prefill_combine_partial_f64 — one part's float64 value.
+ *   y, w, token_row   as for moe_prefill_combine; token_row is read only for slots whose expert is in the part
+ *                     (an expert-parallel rank needs y rows for its own experts only).
+ *   topk_id   device int32 [n][k]: each slot's expert id in [0, n_experts), distinct within a token, any slot order
+ *             (an id outside the part is skipped; a repeated id counts once, in its first slot).
+ *   n_experts 1..1024.  n_parts: a power of two <= Ep.  part: 0 <= part < n_parts, experts
+ *             [part*Ep/n_parts, (part+1)*Ep/n_parts).
+ *   partial   device double [n][H], 16-byte aligned.
+ * n >= 0, 1 <= k <= 32, H a positive multiple of 4, y 16-byte aligned. Row indices are not range-checked on the
+ * device.
+ */
+moe_status moe_prefill_combine_partial_f64(const float* y, const float* w, const int32_t* token_row,
+                                           const int32_t* topk_id, int64_t n, int32_t k, int32_t H,
+                                           int32_t n_experts, int32_t n_parts, int32_t part, double* partial,
+                                           moe_stream_t stream);
+
+/*
+ * moe_prefill_combine_finish_f64 — sum the parts, add the shared expert, round.
+ *   partials  HOST array of n_parts DEVICE pointers, part 0 first, each double [n][H] (16-byte aligned).
+ *   n_parts   a power of two, 1..16.
+ *   s         device float [n][H] or NULL.
+ *   out       device bf16 [n][H];  out_f32: device float [n][H] or NULL (the float32 value before the bf16
+ *             rounding). All 16-byte aligned; H a positive multiple of 4.
+ */
+moe_status moe_prefill_combine_finish_f64(const double* const* partials, int32_t n_parts, const float* s, int64_t n,
+                                          int32_t H, void* out, float* out_f32, moe_stream_t stream);
+
+/*
+ * moe_prefill_combine_f64 — the unsplit float64 combine in one kernel (one part covering every expert, then the
+ * finish); the kernel the layer runs under MOE_COMBINE_F64_TREE. Arguments as above.
+ */
+moe_status moe_prefill_combine_f64(const float* y, const float* w, const int32_t* token_row, const int32_t* topk_id,
+                                   const float* s, int64_t n, int32_t k, int32_t H, int32_t n_experts, void* out,
+                                   float* out_f32, moe_stream_t stream);
+
+/* Combine of the layer: the float32 canonical reduction (default) or the float64 tree above. */
+enum { MOE_COMBINE_F32 = 0, MOE_COMBINE_F64_TREE = 1 };
+/* moe_prefill_set_combine — select the combine of later runs of this plan. */
+moe_status moe_prefill_set_combine(moe_plan_t plan, int32_t mode);
+
+/*
  * moe_prefill_check — wait for `stream`, then read and clear the device error word in the workspace header.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_CUDA (a failed synchronisation).
  */

@@ -119,6 +119,34 @@ def test_run_combine_and_misc_reject_bad_arguments(L):
     assert L.moe_prefill_debug_gemm(fake, fake, fake, 1, 16, 60, 0, fake, None, 0, None) == -1  # k % 64
 
 
+def test_float64_combine_rejects_bad_arguments(L):
+    fake = ctypes.c_void_p(0x1000)
+    part = L.moe_prefill_combine_partial_f64
+    assert part(fake, fake, fake, fake, 4, 0, 64, 64, 1, 0, fake, None) == -1      # k = 0
+    assert part(fake, fake, fake, fake, 4, 2, 62, 64, 1, 0, fake, None) == -1      # H % 4
+    assert part(fake, fake, fake, fake, 4, 2, 64, 0, 1, 0, fake, None) == -1       # no experts
+    assert part(fake, fake, fake, fake, 4, 2, 64, 2048, 1, 0, fake, None) == -1    # > 1024 experts
+    assert part(fake, fake, fake, fake, 4, 2, 64, 64, 3, 0, fake, None) == -1      # 3 parts
+    assert part(fake, fake, fake, fake, 4, 2, 64, 48, 128, 0, fake, None) == -1    # more parts than Ep = 64
+    assert part(fake, fake, fake, fake, 4, 2, 64, 64, 4, 4, fake, None) == -1      # part out of range
+    assert part(fake, fake, fake, fake, 4, 2, 64, 64, 4, 1, None, None) == -1      # no output
+    assert part(fake, fake, fake, fake, 4, 2, 64, 64, 4, 1, ctypes.c_void_p(0x1008), None) == -1  # misaligned
+    assert part(None, None, None, None, 0, 2, 64, 64, 4, 1, None, None) == 0       # n == 0: no-op
+    finish = L.moe_prefill_combine_finish_f64
+    ptrs = (ctypes.c_void_p * 32)(*([0x1000] * 32))
+    assert finish(ptrs, 32, None, 4, 64, fake, None, None) == -1                   # more than 16 parts
+    assert finish(ptrs, 3, None, 4, 64, fake, None, None) == -1                    # not a power of two
+    assert finish(ptrs, 2, None, 4, 64, None, None, None) == -1                    # no output
+    bad = (ctypes.c_void_p * 2)(0x1000, 0)
+    assert finish(bad, 2, None, 4, 64, fake, None, None) == -1                     # a NULL part
+    assert finish(None, 2, None, 0, 64, None, None, None) == 0                     # n == 0: no-op
+    whole = L.moe_prefill_combine_f64
+    assert whole(fake, fake, fake, fake, None, 4, 33, 64, 64, fake, None, None) == -1  # k > 32
+    assert whole(fake, fake, fake, fake, None, 4, 2, 64, 64, None, None, None) == -1   # no output
+    assert L.moe_prefill_set_combine(None, 1) == -1
+    assert b"plan" in L.moe_prefill_last_error()
+
+
 def test_last_error_is_per_thread(L):
     L.moe_prefill_combine(None, None, None, None, 4, 0, 64, None, None)
     main_msg = L.moe_prefill_last_error()
