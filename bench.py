@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--single-pass", action="store_true", help="also time chunk = T (one pass over all tokens)")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count (profiling runs)")
+    ap.add_argument("--combine", choices=["f32", "f64"], default="f32",
+                    help="layer combine: canonical float32 (default) or the float64 tree over expert ids")
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode-size (1 and 8 token) latency lines")
     return ap.parse_args()
 
 
@@ -269,6 +272,12 @@ def gate_up_bytes_and_flops(wl, offs_per_chunk, chunk_sizes):
     return tot_b / m, tot_f / m
 
 
+def tree_fp64_ops(ids_row, n_experts: int) -> int:
+    """float64 additions per output column of the tree combine for one token: one per merge of two nodes (the leaf
+    products w*y are formed exactly on the integer pipe)."""
+    return max(0, len(set(int(v) for v in ids_row)) - 1)
+
+
 def down_bytes_and_flops(wl, offs_per_chunk, chunk_sizes):
     H, I, Is, k = wl.hidden, wl.inter, wl.shared_inter, wl.top_k
     tot_b = tot_f = 0.0
@@ -305,6 +314,8 @@ def run_ours(args, dist: Dist):
         dev = {k: v.cuda() for k, v in inp.items() if k != "x"}
     layer = binding.MoePrefill(dev, top_k=wl.top_k, max_chunk=max(chunk, T if args.single_pass else chunk),
                                offload_slots=wl.offload_slots)
+    if args.combine == "f64":
+        layer.set_combine(binding.COMBINE_F64_TREE)
     stream = torch.cuda.current_stream()
     x = inp["x"].cuda()
     out = torch.empty_like(x)
@@ -383,6 +394,25 @@ def run_ours(args, dist: Dist):
     grouped["combine_gbs"] = (R * wl.hidden * 4 + T * wl.hidden * (4 + 2)) / (times["combine"][0] / k_steps / 1e3) / 1e9
     grouped["topk_gbs"] = (T * wl.n_experts * 4 + T * wl.hidden * 2 + T * wl.top_k * 8) / \
         (times["topk"][0] / k_steps / 1e3) / 1e9
+    comb_s = times["combine"][0] / max(times["combine"][1], 1) / 1e3
+    comb_bytes = (T * wl.top_k * wl.hidden * 4 + T * wl.hidden * (4 + 2)) / n_chunks
+    combine = {"mode": "f64-tree" if args.combine == "f64" else "f32-canonical", "avg_launch_ms": comb_s * 1e3,
+               "algorithmic_bytes_per_launch": comb_bytes, "gbs": comb_bytes / comb_s / 1e9,
+               "hbm_frac": comb_bytes / comb_s / 1e9 / peaks["hbm_gbs"],
+               "note": "timed inside the step, on the side stream, overlapping the expert GEMMs"}
+    if args.combine == "f64":
+        ids_all = torch.empty((T, wl.top_k), dtype=torch.int32, device="cuda")
+        layer.run(x, chunk, out=out, topk_id=ids_all)
+        ids_np = ids_all.cpu().numpy()
+        ops = sum(tree_fp64_ops(r, wl.n_experts) for r in ids_np) + (T if wl.shared_inter else 0)
+        ops_per_launch = ops * wl.hidden / n_chunks
+        sm_mhz = (clocks_info or {}).get("sm_mhz") or 2070.0
+        fp64_peak = torch.cuda.get_device_properties(0).multi_processor_count * 2 * sm_mhz * 1e6 / 1e9
+        combine.update({"bound": "alu", "fp64_ops_per_launch": ops_per_launch,
+                        "fp64_gops": ops_per_launch / comb_s / 1e9, "fp64_peak_gops": fp64_peak,
+                        "fp64_frac": ops_per_launch / comb_s / 1e9 / fp64_peak,
+                        "peak_source": "2 float64 operations per SM per clock x SMs x median SM clock of the run"})
+    grouped["combine"] = combine
 
     # ---------------------------------------------------------------- end to end: host buffers through the ABI
     x_host = inp["x"].pin_memory()
@@ -437,6 +467,34 @@ def run_ours(args, dist: Dist):
                   "gate_up_hbm_frac": b1 / g_s / 1e9 / peaks["hbm_gbs"]}
         layer.raise_on_device_error()
 
+    # ---------------------------------------------------------------- decode sizes (1 and 8 tokens, same kernels)
+    decode = None
+    if not args.no_decode and not wl.offload_slots:
+        decode = {}
+        for n_dec in (1, 8):
+            xd = x[:n_dec].contiguous()
+            od = torch.empty_like(xd)
+            offs_d = torch.empty((1, wl.n_experts + 1), dtype=torch.int32, device="cuda")
+            layer.run(xd, n_dec, out=od, expert_offsets=offs_d)
+            for _ in range(5):
+                layer.run(xd, n_dec, out=od)
+            torch.cuda.synchronize()
+            reps = 200
+            ev0.record(stream)
+            for _ in range(reps):
+                layer.run(xd, n_dec, out=od)
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            dsec = ev0.elapsed_time(ev1) / 1e3 / reps
+            o = offs_d.cpu().numpy()[0]
+            touched = int(((o[1:] - o[:-1]) > 0).sum())
+            wbytes = touched * 3 * wl.inter * wl.hidden * 2 + wl.n_experts * wl.hidden * 2 + \
+                3 * wl.shared_inter * wl.hidden * 2
+            decode[f"tokens_{n_dec}"] = {"ms_per_call": dsec * 1e3, "tokens_per_s": n_dec / dsec,
+                                         "weight_bytes": wbytes, "gbs": wbytes / dsec / 1e9,
+                                         "hbm_frac": wbytes / dsec / 1e9 / peaks["hbm_gbs"]}
+        layer.raise_on_device_error()
+
     route_stats = layer.stats()
     offload = None
     if wl.offload_slots:
@@ -474,8 +532,11 @@ def run_ours(args, dist: Dist):
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
                 "clocks": clocks_info, "grouped_gemm": grouped,
                 "routing_last_run": route_stats}
+        line["config"]["combine"] = "f64-tree" if args.combine == "f64" else "f32-canonical"
         if single is not None:
             line["single_pass"] = single
+        if decode is not None:
+            line["decode"] = decode
         if offload is not None:
             line["offload"] = offload
         print(json.dumps(line), flush=True)

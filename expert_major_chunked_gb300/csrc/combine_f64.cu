@@ -10,13 +10,13 @@
 // Only the token's own slots are touched: the sparse tree over its sorted ids is evaluated as a post-order program,
 // built once per token by one thread and run by every thread on its columns. Where a node has an empty sibling the
 // dense tree adds +0.0, which changes a value only by turning -0.0 into +0.0; the program applies that as a bit test
-// instead of an addition. A leaf product folds into the first addition that consumes it (fma), which rounds exactly
-// like the addition of the exact product.
+// instead of an addition.
 //
-// The float64 pipe is the bound (GB300 issues two float64 operations per SM per clock, against 128 float32), and
-// float <-> double conversions run on it too: the exact widening of a normal float and the rounding of a double
-// whose float result is normal are done here with integer operations instead (IEEE 754 binary32/binary64 layouts;
-// other values take the conversion instruction).
+// The float64 pipe is the bound (on GB300 it is a small fraction of the float32 rate), and float <-> double
+// conversions and float64 multiplies run on it too. So only the additions use it: a leaf product w*y of two normal
+// floats is formed exactly on the integer pipe (24-bit x 24-bit significands give at most 48 bits, which a double
+// holds), and the exact widening of a normal float and the rounding of a double whose float result is normal are
+// done with integer operations (IEEE 754 binary32/binary64 layouts; other values take the float64 instructions).
 #include "internal.h"
 
 #include <cuda_bf16.h>
@@ -26,14 +26,14 @@
 namespace moe {
 namespace {
 
-constexpr int kTreeThreads = 256;
-constexpr int kTreeSlots = 11;  // stack depth: at most log2(1024) nodes wait for a right sibling
+constexpr int kTreeThreads = 128;
+constexpr int kTreeSlots = 10;  // stored nodes: at most log2(1024) - 1 wait for a right sibling
 constexpr uint8_t kNoLeaf = 0xFF;
 constexpr uint8_t kOpPlusZero = 1;  // the node has an empty sibling below it: turn -0.0 into +0.0
 constexpr uint8_t kOpPush = 2;      // store the current value to stack slot p (no arithmetic)
 
-// MERGE: cur = left + right, left = raw leaf `la` (its product folded into an fma) or stack slot p, right = raw
-// leaf `lb` (product w*y) or the current value (the previous merge's result). PUSH: stack[p] = cur.
+// MERGE: cur = left + right, left = raw leaf `la` (its exact product w*y) or stack slot p, right = raw leaf `lb`
+// or the current value (the previous merge's result). PUSH: stack[p] = cur.
 struct TreeOp {
   uint8_t p, la, lb, flags;
 };
@@ -43,7 +43,7 @@ struct TreeProgram {
   int nops;
   int root_pz;    // the root has an empty sibling below the part's top
   int32_t row[32];
-  double w[32];
+  float w[32];
   TreeOp op[64];
 };
 
@@ -79,6 +79,23 @@ __device__ __forceinline__ float narrow_rn(double v) {
   return __double2float_rn(v);
 }
 
+// Exact w*y as a double. For normal floats the product of the two 24-bit significands (at most 48 bits) is formed
+// with one 32x32->64 integer multiply and packed with the summed exponents; it is never subnormal or infinite in
+// double. Zeros, subnormals, inf and NaN take the float64 multiply, also exact.
+__device__ __forceinline__ double exact_product(float a, float b) {
+  const uint32_t ua = __float_as_uint(a), ub = __float_as_uint(b);
+  const uint32_t ea = (ua >> 23) & 0xFFu, eb = (ub >> 23) & 0xFFu;
+  if (ea - 1u < 254u && eb - 1u < 254u) {
+    const uint64_t p = static_cast<uint64_t>((ua & 0x7FFFFFu) | 0x800000u) * ((ub & 0x7FFFFFu) | 0x800000u);
+    const uint32_t top = static_cast<uint32_t>(p >> 47);                // leading one at bit 46 + top
+    const uint64_t frac = (p << (6u - top)) & 0x000FFFFFFFFFFFFFull;    // the bits below it, as 52 fraction bits
+    const uint64_t expo = static_cast<uint64_t>(ea + eb + 769u + top);  // (46 + top) + (ea - 150) + (eb - 150) + 1023
+    const uint64_t sign = static_cast<uint64_t>((ua ^ ub) & 0x80000000u) << 32;
+    return __longlong_as_double(static_cast<long long>(sign | (expo << 52) | frac));
+  }
+  return __dmul_rn(static_cast<double>(a), static_cast<double>(b));
+}
+
 __device__ __forceinline__ int bit_length(uint32_t v) { return v == 0 ? 0 : 32 - __clz(v); }
 
 // One thread, operands already in shared memory: sort the slots inside [lo, lo + 2^block_log2) by expert id and
@@ -106,7 +123,7 @@ __device__ void build_program(TreeProgram& P, const int32_t* ids, const float* w
     }
     e_sorted[j] = e;
     P.row[j] = rows[s];
-    P.w[j] = static_cast<double>(w[s]);
+    P.w[j] = w[s];
     ++m;
   }
   P.m = m;
@@ -186,8 +203,8 @@ __global__ void __launch_bounds__(kTreeThreads) combine_tree_kernel(CombineTreeP
     double2 cur = make_double2(0.0, 0.0);
     if (m == 1) {
       const float2 yv = yl[tid];
-      cur.x = __dmul_rn(P.w[0], widen(yv.x));
-      cur.y = __dmul_rn(P.w[0], widen(yv.y));
+      cur.x = exact_product(P.w[0], yv.x);
+      cur.y = exact_product(P.w[0], yv.y);
     }
     for (int j = 0; j < nops; ++j) {
       const TreeOp o = P.op[j];
@@ -198,22 +215,23 @@ __global__ void __launch_bounds__(kTreeThreads) combine_tree_kernel(CombineTreeP
       double2 b;
       if (o.lb != kNoLeaf) {
         const float2 yv = yl[o.lb * kTreeThreads + tid];
-        const double wb = P.w[o.lb];
-        b.x = __dmul_rn(wb, widen(yv.x));
-        b.y = __dmul_rn(wb, widen(yv.y));
+        const float wb = P.w[o.lb];
+        b.x = exact_product(wb, yv.x);
+        b.y = exact_product(wb, yv.y);
       } else {
         b = cur;
       }
+      double2 av;
       if (o.la != kNoLeaf) {
         const float2 yv = yl[o.la * kTreeThreads + tid];
-        const double wa = P.w[o.la];
-        cur.x = __fma_rn(wa, widen(yv.x), b.x);
-        cur.y = __fma_rn(wa, widen(yv.y), b.y);
+        const float wa = P.w[o.la];
+        av.x = exact_product(wa, yv.x);
+        av.y = exact_product(wa, yv.y);
       } else {
-        const double2 av = stk[o.p * kTreeThreads + tid];
-        cur.x = __dadd_rn(av.x, b.x);
-        cur.y = __dadd_rn(av.y, b.y);
+        av = stk[o.p * kTreeThreads + tid];
       }
+      cur.x = __dadd_rn(av.x, b.x);
+      cur.y = __dadd_rn(av.y, b.y);
       if (o.flags & kOpPlusZero) {
         cur.x = plus_zero(cur.x);
         cur.y = plus_zero(cur.y);
