@@ -189,16 +189,27 @@ __global__ void __launch_bounds__(kTreeThreads) combine_tree_kernel(CombineTreeP
   if (tid == 0) build_program(P, s_ids, s_w, s_rows, a.k, a.lo, a.block_log2);
   __syncthreads();
   const int m = P.m, nops = P.nops;
-  for (int c = 2 * tid; c < a.H; c += 2 * kTreeThreads) {
-    for (int i0 = 0; i0 < m; i0 += 8) {  // the leaves' y values, loads issued in groups of 8
-      float2 v[8];
+  // The first kPrefetch leaves of the next column pair are loaded into registers while the current pair is summed
+  // (one memory round trip per pair, hidden behind the additions); leaves beyond kPrefetch load on the spot.
+  constexpr int kPrefetch = 16;
+  const int step = 2 * kTreeThreads;
+  float2 nxt[kPrefetch];
+  if (2 * tid < a.H) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (i0 + j < m)
-          v[j] = __ldg(reinterpret_cast<const float2*>(a.y + static_cast<int64_t>(P.row[i0 + j]) * a.H + c));
+    for (int j = 0; j < kPrefetch; ++j)
+      if (j < m) nxt[j] = __ldg(reinterpret_cast<const float2*>(a.y + static_cast<int64_t>(P.row[j]) * a.H + 2 * tid));
+  }
+  for (int c = 2 * tid; c < a.H; c += step) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (i0 + j < m) yl[(i0 + j) * kTreeThreads + tid] = v[j];
+    for (int j = 0; j < kPrefetch; ++j)
+      if (j < m) yl[j * kTreeThreads + tid] = nxt[j];
+    for (int j = kPrefetch; j < m; ++j)
+      yl[j * kTreeThreads + tid] = __ldg(reinterpret_cast<const float2*>(a.y + static_cast<int64_t>(P.row[j]) * a.H + c));
+    if (c + step < a.H) {
+#pragma unroll
+      for (int j = 0; j < kPrefetch; ++j)
+        if (j < m)
+          nxt[j] = __ldg(reinterpret_cast<const float2*>(a.y + static_cast<int64_t>(P.row[j]) * a.H + c + step));
     }
     double2 cur = make_double2(0.0, 0.0);
     if (m == 1) {
