@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--combine", choices=["f32", "f64"], default="f32",
                     help="layer combine: canonical float32 (default) or the float64 tree over expert ids")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-size (1 and 8 token) latency lines")
+    ap.add_argument("--offload-copy", choices=["routed", "all"], default="routed",
+                    help="offloaded experts: stage only the routed experts (kernel) or every expert (copy engines)")
     return ap.parse_args()
 
 
@@ -316,6 +318,9 @@ def run_ours(args, dist: Dist):
                                offload_slots=wl.offload_slots)
     if args.combine == "f64":
         layer.set_combine(binding.COMBINE_F64_TREE)
+    if wl.offload_slots:
+        layer.set_offload_copy(binding.OFFLOAD_COPY_ROUTED if args.offload_copy == "routed"
+                               else binding.OFFLOAD_COPY_ALL)
     stream = torch.cuda.current_stream()
     x = inp["x"].cuda()
     out = torch.empty_like(x)
@@ -498,9 +503,14 @@ def run_ours(args, dist: Dist):
     route_stats = layer.stats()
     offload = None
     if wl.offload_slots:
-        # every chunk stages every expert: bytes over the host link per step, against a plain pinned copy
+        # bytes over the host link per step, against a plain pinned copy: the routed experts of every chunk
+        # (routed staging, counted on the device), else every expert of every chunk (copy engines)
         bank = inp["w_gu"].numel() * 2 + inp["w_down"].numel() * 2
-        h2d_bytes = bank * n_chunks
+        per_expert = bank // wl.n_experts
+        if args.offload_copy == "routed":
+            h2d_bytes = route_stats["experts_copied"] * per_expert
+        else:
+            h2d_bytes = bank * n_chunks
         probe = torch.empty(1 << 30, dtype=torch.uint8).pin_memory()
         dprobe = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
         for _ in range(2):
@@ -513,9 +523,13 @@ def run_ours(args, dist: Dist):
         torch.cuda.synchronize()
         link_gbs = 5 * (1 << 30) / (ev0.elapsed_time(ev1) / 1e3) / 1e9
         achieved_link = h2d_bytes / (ms_per_step / 1e3) / 1e9
-        offload = {"slots": wl.offload_slots, "h2d_bytes_per_step": h2d_bytes, "h2d_gbs": achieved_link,
+        offload = {"slots": wl.offload_slots, "copy": args.offload_copy, "h2d_bytes_per_step": h2d_bytes,
+                   "experts_copied": route_stats["experts_copied"], "experts_skipped": route_stats["experts_skipped"],
+                   "h2d_gbs": achieved_link,
                    "pinned_copy_gbs": link_gbs, "link_frac": achieved_link / link_gbs}
-        roofline = {"bound": "h2d", "kernel": "expert staging copies (copy engines)", "achieved": achieved_link,
+        kname = ("routed-expert staging kernel (reads the pinned banks)" if args.offload_copy == "routed"
+                 else "expert staging copies (copy engines)")
+        roofline = {"bound": "h2d", "kernel": kname, "achieved": achieved_link,
                     "peak": link_gbs, "unit": "GB/s", "frac": achieved_link / link_gbs, "traffic": None,
                     "peak_source": "measured in this run: pinned host->device cudaMemcpyAsync of 1 GiB"}
         del probe, dprobe
@@ -533,6 +547,8 @@ def run_ours(args, dist: Dist):
                 "clocks": clocks_info, "grouped_gemm": grouped,
                 "routing_last_run": route_stats}
         line["config"]["combine"] = "f64-tree" if args.combine == "f64" else "f32-canonical"
+        if wl.offload_slots:
+            line["config"]["offload_copy"] = args.offload_copy
         if single is not None:
             line["single_pass"] = single
         if decode is not None:

@@ -48,6 +48,7 @@ _SIGS = {
     "moe_prefill_combine_f64": ([_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                  _P, _P, _P], ctypes.c_int),
     "moe_prefill_set_combine": ([_P, ctypes.c_int32], ctypes.c_int),
+    "moe_prefill_set_offload_copy": ([_P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_check": ([_P, _P], ctypes.c_int),
     "moe_prefill_destroy": ([_P], None),
     "moe_prefill_last_error": ([], ctypes.c_char_p),
@@ -134,6 +135,11 @@ def moe_prefill_combine_f64(y, w, token_row, topk_id, s, n, k, H, n_experts, out
 
 
 COMBINE_F32, COMBINE_F64_TREE = 0, 1
+OFFLOAD_COPY_ALL, OFFLOAD_COPY_ROUTED = 0, 1
+
+
+def moe_prefill_set_offload_copy(plan, mode: int):
+    _check(lib().moe_prefill_set_offload_copy(plan, mode))
 
 
 def moe_prefill_set_combine(plan, mode: int):
@@ -168,7 +174,8 @@ def moe_prefill_set_wait_timeout(plan, timeout_ns: int):
     _check(lib().moe_prefill_set_wait_timeout(plan, timeout_ns))
 
 
-STATS_NAMES = ["chunks", "flagged", "by_float", "by_double", "by_sequential", "by_many"]
+STATS_NAMES = ["chunks", "flagged", "by_float", "by_double", "by_sequential", "by_many", "experts_copied",
+               "experts_skipped"]
 
 
 def moe_prefill_run_stats(workspace, stream=None) -> dict:
@@ -239,6 +246,10 @@ class MoePrefill:
                         out.data_ptr(), _ptr(topk_id), _ptr(topk_w), _ptr(expert_offsets), _ptr(row_token),
                         _stream_handle(stream), copy_stream.cuda_stream if copy_stream is not None else None)
         return out
+
+    def set_offload_copy(self, mode: int):
+        """OFFLOAD_COPY_ROUTED (stage only routed experts; default where available) or OFFLOAD_COPY_ALL."""
+        moe_prefill_set_offload_copy(self.plan, mode)
 
     def set_combine(self, mode: int):
         """COMBINE_F32 (canonical float32, ascending expert id; default) or COMBINE_F64_TREE."""

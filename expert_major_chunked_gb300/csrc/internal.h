@@ -34,7 +34,9 @@ struct WsHeader {
   int32_t pad0;
   float wnorm_max;             // max_e ||w_router[e]||_2 (upper bound)
   int32_t band_levels[4];      // flagged tokens decided by: float sums, double sums, sequential sums, many-candidate path
-  int32_t pad[55];
+  int32_t experts_copied;      // offloaded experts staged into the ring (this run)
+  int32_t experts_skipped;     // offloaded experts not staged: no row of their chunk was routed to them (this run)
+  int32_t pad[53];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -174,6 +176,19 @@ size_t combine_tree_smem_bytes(int k);
 // experts), + s, float32, bf16 in the same kernel.
 cudaError_t launch_combine_tree(const CombineTreeParams& a, bool finish, cudaStream_t stream);
 cudaError_t launch_combine_finish(const CombineFinishParams& a, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------ ring of offloaded experts
+struct RingCopyParams {
+  const uint4* bank_gu;      // device-accessible address of the pinned host bank [E][2I][H] bf16
+  const uint4* bank_down;    // [E][H][I]
+  uint4* ring_gu;            // [S][2I][H]
+  uint4* ring_down;          // [S][H][I]
+  const int32_t* tile_base;  // the chunk's gate/up tile base per expert [E+1]: expert e is routed to iff it has tiles
+  WsHeader* hdr;
+  int64_t gu16, dn16;        // one expert's gate/up and down bytes / 16
+  int32_t e0, count, slots;  // experts [e0, e0 + count) into slots e % slots
+};
+cudaError_t launch_ring_copy(const RingCopyParams& p, cudaStream_t stream);
 
 // ------------------------------------------------------------------ host helpers shared with noalloc.cu
 void set_last_error(const char* msg);

@@ -204,6 +204,10 @@ struct moe_plan {
   CUtensorMap tm_xp[2], tm_h, tm_hs, tm_ring_gu, tm_ring_down;
   // offloaded experts: w_gu / w_down are pinned host banks; the copy stream fills the ring (see moe_prefill_run)
   bool offload = false;
+  // device-accessible addresses of the pinned banks (null when the device cannot read them directly)
+  const void* bank_gu_dev = nullptr;
+  const void* bank_down_dev = nullptr;
+  int32_t offload_copy = MOE_OFFLOAD_COPY_ALL;
   cudaStream_t own_copy = nullptr;
   cudaEvent_t ev_copy[2] = {}, ev_rel[2] = {};
   // Each chunk's member lists (count, scan, permute) run on a side stream so that they overlap the previous chunk's
@@ -336,6 +340,8 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   p->offload = dims->offload_slots > 0;
   if (p->offload) {
     // the expert banks stay in host memory: they must be page-locked so the copy engines can read them
+    const void* dev_addr[2] = {nullptr, nullptr};
+    int qi = 0;
     for (const void* q : {w_gu, w_down}) {
       cudaPointerAttributes a;
       if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost) {
@@ -343,6 +349,13 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
         delete p;
         return fail(MOE_ERR_INVALID_ARG, "offload_slots > 0 needs w_gu and w_down in pinned host memory");
       }
+      dev_addr[qi++] = a.devicePointer;
+    }
+    // kernels can stage only the routed experts when the device reads the banks directly (16-byte aligned)
+    if (dev_addr[0] && dev_addr[1] && aligned16(dev_addr[0]) && aligned16(dev_addr[1])) {
+      p->bank_gu_dev = dev_addr[0];
+      p->bank_down_dev = dev_addr[1];
+      p->offload_copy = MOE_OFFLOAD_COPY_ROUTED;
     }
   }
   st = encode_bf16_2d(&p->tm_wr_narrow, w_router, s.E, s.H, s.bn_router_narrow);
@@ -585,11 +598,32 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     // Offloaded experts: the ring's halves hold windows of W consecutive experts; window [e0, e0 + W) goes to slots
     // e0 % S ... (one copy for its gate/up weights, one for its down weights) once the copy stream has seen the
     // release of the window that last used those slots.
-    auto copy_window = [&](int e0) -> moe_status {
+    auto copy_window = [&](int64_t cidx, int e0) -> moe_status {
       const int hb = (e0 / s.window) & 1;
       const size_t slot0 = static_cast<size_t>(e0 % s.slots);
       const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H * 2, dn_bytes = static_cast<size_t>(s.H) * s.I * 2;
       moe_status r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[hb], 0), "slot release wait");
+      if (r2 == MOE_OK && p->offload_copy == MOE_OFFLOAD_COPY_ROUTED) {
+        // only the experts this chunk routes rows to, decided on the device once its member lists exist
+        const int par = static_cast<int>(cidx & 1);
+        r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_ready[par], 0), "member lists wait");
+        RingCopyParams rp;
+        rp.bank_gu = static_cast<const uint4*>(p->bank_gu_dev);
+        rp.bank_down = static_cast<const uint4*>(p->bank_down_dev);
+        rp.ring_gu = reinterpret_cast<uint4*>(ws + L.ring_gu);
+        rp.ring_down = reinterpret_cast<uint4*>(ws + L.ring_down);
+        rp.tile_base = reinterpret_cast<const int32_t*>(ws + L.tile_base[par]);
+        rp.hdr = hdr;
+        rp.gu16 = static_cast<int64_t>(gu_bytes / 16);
+        rp.dn16 = static_cast<int64_t>(dn_bytes / 16);
+        rp.e0 = e0;
+        rp.count = s.window;
+        rp.slots = s.slots;
+        if (r2 == MOE_OK) r2 = cuda_status(launch_ring_copy(rp, cp), "expert staging launch");
+        if (r2 == MOE_OK) ++p->launches;
+        if (r2 == MOE_OK) r2 = cuda_status(cudaEventRecord(p->ev_copy[hb], cp), "copy event");
+        return r2;
+      }
       if (r2 == MOE_OK)
         r2 = cuda_status(cudaMemcpyAsync(ws + L.ring_gu + slot0 * gu_bytes,
                                          static_cast<const char*>(p->w_gu) + static_cast<size_t>(e0) * gu_bytes,
@@ -764,7 +798,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         rc = gemms(chunk_idx, 0, s.E);
       } else {
         for (int e0 = 0; rc == MOE_OK && e0 < s.E; e0 += s.window) {
-          rc = copy_window(e0);
+          rc = copy_window(chunk_idx, e0);
           if (rc == MOE_OK) rc = gemms(chunk_idx, e0, e0 + s.window);
         }
       }
@@ -882,6 +916,17 @@ moe_status moe_prefill_combine_f64(const float* y, const float* w, const int32_t
   return cuda_status(launch_combine_tree(a, true, reinterpret_cast<cudaStream_t>(stream)), "combine launch");
 }
 
+moe_status moe_prefill_set_offload_copy(moe_plan_t p, int32_t mode) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (!p->offload) return fail(MOE_ERR_INVALID_ARG, "the plan has no offloaded experts");
+  if (mode != MOE_OFFLOAD_COPY_ALL && mode != MOE_OFFLOAD_COPY_ROUTED)
+    return fail(MOE_ERR_INVALID_ARG, "unknown offload copy mode %d", mode);
+  if (mode == MOE_OFFLOAD_COPY_ROUTED && !p->bank_gu_dev)
+    return fail(MOE_ERR_UNSUPPORTED, "this device cannot read the pinned banks directly");
+  p->offload_copy = mode;
+  return MOE_OK;
+}
+
 moe_status moe_prefill_set_combine(moe_plan_t p, int32_t mode) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
   if (mode != MOE_COMBINE_F32 && mode != MOE_COMBINE_F64_TREE)
@@ -910,8 +955,9 @@ moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* 
   CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
   WsHeader hdr;
   CUDA_TRY(cudaMemcpy(&hdr, workspace, sizeof hdr, cudaMemcpyDeviceToHost));
-  const int32_t all[MOE_STATS_COUNT] = {hdr.chunks_done,     hdr.band_tokens,     hdr.band_levels[0],
-                                        hdr.band_levels[1], hdr.band_levels[2], hdr.band_levels[3]};
+  const int32_t all[MOE_STATS_COUNT] = {hdr.chunks_done,       hdr.band_tokens,       hdr.band_levels[0],
+                                        hdr.band_levels[1],   hdr.band_levels[2],   hdr.band_levels[3],
+                                        hdr.experts_copied, hdr.experts_skipped};
   for (int32_t i = 0; i < n_stats; ++i) stats[i] = i < MOE_STATS_COUNT ? all[i] : 0;
   return MOE_OK;
 }

@@ -73,6 +73,14 @@ WORKLOADS: Dict[str, Workload] = {
                                     top_k=10, shared_inter=512, chunks=(1024,), x_std=1.0, w_std=0.02,
                                     router_std=1.0 / math.sqrt(2048), offload_slots=32,
                                     note="12,001-token prompt; experts staged from pinned host memory"),
+    # The same offloaded layer under the Zipf(1.1) popularity prior: skewed routing leaves experts of a chunk
+    # without rows, which the routed staging mode does not copy.
+    "e512_zipf_offload_t12001": Workload("e512_zipf_offload_t12001", tokens=12001, hidden=2048, n_experts=512,
+                                         inter=512, top_k=10, shared_inter=512, chunks=(1024,), x_std=1.0,
+                                         w_std=0.02, router_std=1.0 / math.sqrt(2047), zipf_prior=1.1,
+                                         offload_slots=32,
+                                         note="12,001-token prompt, Zipf(1.1) prior; experts staged from pinned host"
+                                              " memory"),
 }
 
 

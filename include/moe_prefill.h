@@ -177,6 +177,20 @@ moe_status moe_prefill_combine_f64(const float* y, const float* w, const int32_t
                                    const float* s, int64_t n, int32_t k, int32_t H, int32_t n_experts, void* out,
                                    float* out_f32, moe_stream_t stream);
 
+/*
+ * How offloaded experts reach the ring (plans with offload_slots > 0).
+ *   MOE_OFFLOAD_COPY_ROUTED  (default where the device can read the pinned banks directly) a small kernel on the
+ *     copy stream stages, per chunk and window, only the experts that the chunk's member lists route rows to,
+ *     reading the banks through their device-accessible addresses; the decision is made on the device (umbrella
+ *     PR #1113, "Memory and execution split": device-planned paths fill expert lines from mapped host banks;
+ *     "Latest measured follow-up": transfer volume is the cost). Counts in MOE_STATS_EXPERTS_COPIED / _SKIPPED.
+ *   MOE_OFFLOAD_COPY_ALL  the copy engines stage every expert of every window (two cudaMemcpyAsync per window).
+ * Both give the same output bytes. moe_prefill_set_offload_copy fails with MOE_ERR_UNSUPPORTED for ROUTED when
+ * the device cannot read the banks directly, and with MOE_ERR_INVALID_ARG for a plan without offloaded experts.
+ */
+enum { MOE_OFFLOAD_COPY_ALL = 0, MOE_OFFLOAD_COPY_ROUTED = 1 };
+moe_status moe_prefill_set_offload_copy(moe_plan_t plan, int32_t mode);
+
 /* Combine of the layer: the float32 canonical reduction (default) or the float64 tree above. */
 enum { MOE_COMBINE_F32 = 0, MOE_COMBINE_F64_TREE = 1 };
 /* moe_prefill_set_combine — select the combine of later runs of this plan. */
@@ -262,7 +276,9 @@ enum {
   MOE_STATS_BY_DOUBLE = 3,    /* ... decided by double sums */
   MOE_STATS_BY_SEQUENTIAL = 4,/* ... decided by the sequential float64 sums */
   MOE_STATS_BY_MANY = 5,      /* ... with more candidates than the recheck list holds (sequential sums) */
-  MOE_STATS_COUNT = 6
+  MOE_STATS_EXPERTS_COPIED = 6,  /* offloaded experts staged into the ring, summed over chunks (routed mode) */
+  MOE_STATS_EXPERTS_SKIPPED = 7, /* offloaded experts left out: their chunk routed no row to them (routed mode) */
+  MOE_STATS_COUNT = 8
 };
 /* Writes min(n_stats, ...) entries of the list above to stats (entries past MOE_STATS_COUNT are 0). */
 moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* stats, int32_t n_stats);
