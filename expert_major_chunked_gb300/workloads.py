@@ -138,3 +138,35 @@ def draw_x(wl: Workload, tokens: int, seed: int) -> torch.Tensor:
     if wl.zipf_prior > 0:
         x[:, 0] = 1.0
     return x.to(torch.bfloat16)
+
+
+def quantize_mxfp8(w: torch.Tensor):
+    """Block-scaled FP8 (MXFP8) form of expert weights [E][R][K], K a multiple of 32: E4M3 codes [E][R][K] (uint8)
+    and E8M0 scales [E][K/32][R] (uint8, one plane per 32-wide K block).
+
+    This is an input format, not part of the layer: each block of 32 weights along K shares the power of two
+    2^(s-127) (OCP Microscaling v1.0 E8M0) with s - 127 the least exponent that keeps max |w| / 2^(s-127) <= 448,
+    the largest E4M3 value (so no weight is clipped), kept in [10, 246] so that every code times its scale is
+    exactly a normal bf16 value; the weights divided by the scale are rounded to E4M3 (nearest, ties to even).
+    """
+    E, R, K = w.shape
+    assert K % 32 == 0
+    codes = torch.empty((E, R, K), dtype=torch.uint8)
+    scales = torch.empty((E, K // 32, R), dtype=torch.uint8)
+    for e in range(E):
+        blk = w[e].to(torch.float32).reshape(R, K // 32, 32)
+        amax = blk.abs().amax(dim=2)
+        expo = torch.where(amax > 0, torch.ceil(torch.log2(amax.clamp_min(1e-38).double() / 448.0)).float(),
+                           torch.zeros_like(amax))
+        s = (expo + 127).clamp(10, 246)
+        q = (blk / torch.exp2(s - 127).unsqueeze(2)).clamp(-448.0, 448.0)
+        codes[e] = q.to(torch.float8_e4m3fn).view(torch.uint8).reshape(R, K)
+        scales[e] = s.to(torch.uint8).t()
+    return codes, scales
+
+
+def mxfp8_weights(inp: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
+    """The routed expert weights of a drawn workload in MXFP8 form: w_gu_q/w_gu_s, w_down_q/w_down_s."""
+    gu_q, gu_s = quantize_mxfp8(inp["w_gu"])
+    dn_q, dn_s = quantize_mxfp8(inp["w_down"])
+    return {"w_gu_q": gu_q, "w_gu_s": gu_s, "w_down_q": dn_q, "w_down_s": dn_s}

@@ -58,10 +58,11 @@ def lib():
             L.oracle_combine_f32_canonical.argtypes = [P, P, P, P, i64, i32, i32, P]
             L.oracle_combine_tree_partial_f64.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, P]
             L.oracle_combine_tree_finish_f64.argtypes = [P, i32, P, i64, i32, P, P]
+            L.oracle_dequant_mxfp8.argtypes = [P, P, i64, i64, P]
             for name in ("oracle_bf16_round_array", "oracle_router_logits", "oracle_topk", "oracle_swiglu_ffn",
                          "oracle_moe_forward", "oracle_permutation", "oracle_combine_f64",
                          "oracle_combine_f32_canonical", "oracle_combine_tree_partial_f64",
-                         "oracle_combine_tree_finish_f64"):
+                         "oracle_combine_tree_finish_f64", "oracle_dequant_mxfp8"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -235,3 +236,15 @@ def combine_tree_finish_f64(partials, s=None):
 def combine_tree_f64(y, w, token_row, topk_id, n_experts, s=None):
     """The unsplit float64 tree combine: one part, then the finish."""
     return combine_tree_finish_f64([combine_tree_partial_f64(y, w, token_row, topk_id, n_experts)], s)
+
+
+def dequant_mxfp8(codes, scales):
+    """E4M3 codes [E][R][K] (uint8) with E8M0 scales [E][K/32][R] (uint8) -> exact bf16 bits [E][R][K]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    E, R, K = codes.shape
+    assert scales.shape == (E, K // 32, R), scales.shape
+    out = np.empty((E, R, K), dtype=np.uint16)
+    for e in range(E):
+        _check(lib().oracle_dequant_mxfp8(_ptr(codes[e]), _ptr(scales[e]), R, K, _ptr(out[e])), "dequant_mxfp8")
+    return out

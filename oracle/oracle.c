@@ -398,3 +398,29 @@ int oracle_combine_tree_finish_f64(const double* partials, int32_t n_parts, cons
   }
   return rc;
 }
+
+/* E4M3 code -> exact value, from the format's definition (sign, 4-bit exponent with bias 7, 3-bit fraction). */
+static int e4m3_value(uint8_t code, double* v) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return -1; /* NaN */
+  const double mag = (e == 0) ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  *v = sign ? -mag : mag;
+  return 0;
+}
+
+int oracle_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K, uint16_t* out_bf16) {
+  if (!codes || !scales || !out_bf16 || rows < 0 || K < 0 || K % 32 != 0) return -1;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      const uint8_t s = scales[(k / 32) * rows + r];
+      if (s == 255) return -1;
+      double v;
+      if (e4m3_value(codes[r * K + k], &v) != 0) return -1;
+      v = ldexp(v, (int)s - 127);
+      const uint16_t b = oracle_bf16_from_double(v);
+      if (oracle_bf16_to_double(b) != v) return -1; /* not exactly representable in bf16 */
+      if (v == 0.0 && signbit(v) != ((b >> 15) & 1)) return -1;
+      out_bf16[r * K + k] = b;
+    }
+  return 0;
+}

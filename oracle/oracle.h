@@ -106,6 +106,18 @@ int oracle_combine_tree_partial_f64(const float* y, const float* w, const int32_
 int oracle_combine_tree_finish_f64(const double* partials, int32_t n_parts, const float* s_shared, int64_t n,
                                    int32_t hidden, float* out_f32, uint16_t* out_bf16);
 
+/*
+ * Block-scaled FP8 expert weights (MXFP8): each weight is an E4M3 code (1 sign bit, 4 exponent bits with bias 7,
+ * 3 fraction bits; exponent field 0 holds the subnormals m/8 * 2^-6; codes 0x7F / 0xFF are NaN, there is no
+ * infinity) times the power of two 2^(s - 127) given by an E8M0 scale byte s (255 is NaN) shared by a block of 32
+ * consecutive weights along K (OCP Microscaling Formats v1.0). The pages quantise prompt-tile weights (the
+ * deep-prefill draft's review, "To land": NVFP4 prompt tiles that reproduce the decode bytes); this is the 8-bit
+ * block-scaled member of that family.
+ * codes [R][K], scales [K/32][R] (one plane per 32-wide K block), K a multiple of 32. out_bf16 [R][K]: the exact
+ * value of each weight as bf16 bits. Returns -1 for a NaN code or scale, or a value that bf16 cannot hold exactly.
+ */
+int oracle_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K, uint16_t* out_bf16);
+
 #ifdef __cplusplus
 }
 #endif

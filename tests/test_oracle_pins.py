@@ -467,3 +467,78 @@ def test_tree_combine_rejects_bad_arguments(oracle_lib):
         oracle_lib.combine_tree_partial_f64(y, w, tr, np.array([[0, 4], [1, 2]], np.int32), 4)   # id >= E
     with pytest.raises(ValueError):
         oracle_lib.combine_tree_partial_f64(y, w, tr, np.array([[0, 1], [1, 2]], np.int32), 4, 3, 0)  # 3 parts
+
+
+# ---------------------------------------------------------------- MXFP8 weights (E4M3 codes, E8M0 block scales)
+
+def _fixture_lines(name):
+    import os
+    from conftest import GOLDEN
+    rows = []
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            rows.append(line.split()[1:])
+    return rows
+
+
+def test_mxfp8_hand_worked_codes(oracle_lib):
+    for code, scale, value in _fixture_lines("e4m3_codes.txt"):
+        codes = np.zeros((1, 1, 32), np.uint8)
+        codes[0, 0, 5] = int(code)
+        scales = np.full((1, 1, 1), int(scale), np.uint8)
+        got = float(oracle_lib.bf16_to_double(oracle_lib.dequant_mxfp8(codes, scales)[0, 0, 5:6])[0])
+        want = float(value)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want), (code, scale, got, want)
+
+
+def test_mxfp8_matches_library_decoding(oracle_lib):
+    """Every non-NaN code against torch's float8_e4m3fn decoding, times 2^(s-127) for scales across the range."""
+    rng = np.random.default_rng(31)
+    codes_all = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    R, K = 8, 256
+    codes = rng.choice(codes_all, size=(2, R, K)).astype(np.uint8)
+    codes[0, 0, :len(codes_all)] = codes_all
+    scales = rng.integers(10, 247, size=(2, K // 32, R)).astype(np.uint8)
+    got = oracle_lib.bf16_to_double(oracle_lib.dequant_mxfp8(codes, scales))
+    lib_vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    s_full = np.repeat(scales.transpose(0, 2, 1), 32, axis=2).astype(np.int64)  # [E][R][K]
+    want = np.ldexp(lib_vals, s_full - 127)
+    np.testing.assert_array_equal(got, want)
+    np.testing.assert_array_equal(np.signbit(got), np.signbit(want))
+
+
+def test_mxfp8_rejects_nan_and_unrepresentable(oracle_lib):
+    base = np.zeros((1, 2, 32), np.uint8)
+    ok = np.full((1, 1, 2), 127, np.uint8)
+    oracle_lib.dequant_mxfp8(base, ok)
+    for code in (0x7F, 0xFF):
+        bad = base.copy()
+        bad[0, 1, 3] = code
+        with pytest.raises(ValueError):
+            oracle_lib.dequant_mxfp8(bad, ok)
+    with pytest.raises(ValueError):
+        oracle_lib.dequant_mxfp8(base, np.full((1, 1, 2), 255, np.uint8))
+    tiny = base.copy()
+    tiny[0, 0, 0] = 0x01
+    with pytest.raises(ValueError):  # 2^-9 * 2^-127 is below every bf16 value
+        oracle_lib.dequant_mxfp8(tiny, np.full((1, 1, 2), 0, np.uint8))
+
+
+def test_mxfp8_quantizer_round_trip(oracle_lib):
+    """The synthetic MXFP8 inputs decode (oracle) to within half an E4M3 step of the drawn weights, and every
+    block's largest weight lands in (224, 448] after scaling (the least scale that clips nothing)."""
+    from expert_major_chunked_gb300 import workloads
+    g = torch.Generator().manual_seed(5)
+    w = (torch.randn((3, 16, 128), generator=g) * 0.02).to(torch.bfloat16)
+    codes, scales = workloads.quantize_mxfp8(w)
+    got = oracle_lib.bf16_to_double(oracle_lib.dequant_mxfp8(codes.numpy(), scales.numpy()))
+    ref = w.double().numpy()
+    blk_scale = np.repeat(np.ldexp(1.0, scales.numpy().astype(np.int64) - 127).transpose(0, 2, 1), 32, axis=2)
+    # E4M3 spacing at magnitude |q| = |w| / scale is 2^(floor(log2|q|) - 3) (normal) or 2^-9 (subnormal)
+    q = np.abs(ref) / blk_scale
+    step = np.where(q >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(q, 2.0 ** -6))) - 3), 2.0 ** -9)
+    assert np.all(np.abs(got - ref) <= 0.5 * step * blk_scale + 1e-30)
+    amax = np.abs(ref).reshape(3, 16, 4, 32).max(axis=3)
+    qmax = amax / np.ldexp(1.0, scales.numpy().astype(np.int64).transpose(0, 2, 1) - 127)
+    assert np.all((qmax > 224) & (qmax <= 448))
