@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--combine", choices=["f32", "f64"], default="f32",
                     help="layer combine: canonical float32 (default) or the float64 tree over expert ids")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-size (1 and 8 token) latency lines")
+    ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
+                    help="routed expert weights: bf16, or MXFP8 (E4M3 codes + E8M0 scale per 32 along K)")
     ap.add_argument("--offload-copy", choices=["routed", "all"], default="routed",
                     help="offloaded experts: stage only the routed experts (kernel) or every expert (copy engines)")
     return ap.parse_args()
@@ -198,11 +200,17 @@ def run_reference(args, dist: Dist):
         dist.close()
         return
     import numpy as np
+    import torch
     import oracle
     from expert_major_chunked_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
     chunk = args.chunk or wl.chunks[0]
     inp = workloads.generate(wl)
+    if args.weights == "mxfp8":  # the oracle runs on the decoded MXFP8 weights
+        q = workloads.mxfp8_weights(inp)
+        for w, c, sc in (("w_gu", "w_gu_q", "w_gu_s"), ("w_down", "w_down_q", "w_down_s")):
+            inp[w] = torch.from_numpy(oracle.dequant_mxfp8(q[c].numpy(), q[sc].numpy()).view(np.int16)).view(
+                torch.bfloat16)
     cores = oracle.num_threads()
     # calibrate, then size each step so that warm-up + timed steps fit in about two minutes
     t0 = time.perf_counter()
@@ -256,16 +264,17 @@ def cpu_baseline(inp, wl, budget_s: float = 10.0) -> dict:
             "sample": f"first {n} of {wl.tokens} tokens, full layer in float64 ({secs:.1f} s)"}
 
 
-def gate_up_bytes_and_flops(wl, offs_per_chunk, chunk_sizes):
+def gate_up_bytes_and_flops(wl, offs_per_chunk, chunk_sizes, wb=2.0):
     """Algorithmic DRAM bytes and useful FLOPs of one gate/up launch (per chunk, averaged over the chunks):
-    weights of the touched experts + shared expert, the gathered input rows read once, h written once."""
+    weights of the touched experts (wb bytes per routed weight: 2 for bf16, 1 + 1/32 for MXFP8 codes and scales)
+    + shared expert, the gathered input rows read once, h written once."""
     H, I, Is, k = wl.hidden, wl.inter, wl.shared_inter, wl.top_k
     tot_b = tot_f = 0.0
     for offs, n in zip(offs_per_chunk, chunk_sizes):
         counts = offs[1:] - offs[:-1]
         touched = int((counts > 0).sum())
         R = n * k
-        b = touched * 2 * I * H * 2 + (2 * Is * H * 2 if Is else 0) + (R + (n if Is else 0)) * H * 2 \
+        b = touched * 2 * I * H * wb + (2 * Is * H * 2 if Is else 0) + (R + (n if Is else 0)) * H * 2 \
             + (R * I + n * Is) * 2
         f = 2.0 * R * H * 2 * I + 2.0 * n * H * 2 * Is
         tot_b += b
@@ -280,14 +289,14 @@ def tree_fp64_ops(ids_row, n_experts: int) -> int:
     return max(0, len(set(int(v) for v in ids_row)) - 1)
 
 
-def down_bytes_and_flops(wl, offs_per_chunk, chunk_sizes):
+def down_bytes_and_flops(wl, offs_per_chunk, chunk_sizes, wb=2.0):
     H, I, Is, k = wl.hidden, wl.inter, wl.shared_inter, wl.top_k
     tot_b = tot_f = 0.0
     for offs, n in zip(offs_per_chunk, chunk_sizes):
         counts = offs[1:] - offs[:-1]
         touched = int((counts > 0).sum())
         R = n * k
-        b = touched * H * I * 2 + (H * Is * 2 if Is else 0) + (R * I + n * Is) * 2 + (R + (n if Is else 0)) * H * 4
+        b = touched * H * I * wb + (H * Is * 2 if Is else 0) + (R * I + n * Is) * 2 + (R + (n if Is else 0)) * H * 4
         f = 2.0 * R * I * H + 2.0 * n * Is * H
         tot_b += b
         tot_f += f
@@ -308,10 +317,23 @@ def run_ours(args, dist: Dist):
     chunk = args.chunk or wl.chunks[0]
     T = wl.tokens
     inp = workloads.generate(wl)
-    if wl.offload_slots:
+    wb = 2.0
+    if args.weights == "mxfp8":
+        q = workloads.mxfp8_weights(inp)
+        wb = 1.0 + 1.0 / 32.0
+    if wl.offload_slots and args.weights == "mxfp8":
+        # E4M3 code banks in pinned host memory, scales, router and shared expert in device memory
+        dev = {k: v.cuda() for k, v in inp.items() if k not in ("x", "w_gu", "w_down")}
+        dev.update({"w_gu_q": q["w_gu_q"].pin_memory(), "w_down_q": q["w_down_q"].pin_memory(),
+                    "w_gu_s": q["w_gu_s"].cuda(), "w_down_s": q["w_down_s"].cuda()})
+        args.single_pass = False
+    elif wl.offload_slots:
         # expert banks stay in pinned host memory; router and shared expert in device memory
         dev = {k: (v.pin_memory() if k in ("w_gu", "w_down") else v.cuda()) for k, v in inp.items() if k != "x"}
         args.single_pass = False
+    elif args.weights == "mxfp8":
+        dev = {k: v.cuda() for k, v in inp.items() if k not in ("x", "w_gu", "w_down")}
+        dev.update({k: v.cuda() for k, v in q.items()})
     else:
         dev = {k: v.cuda() for k, v in inp.items() if k != "x"}
     layer = binding.MoePrefill(dev, top_k=wl.top_k, max_chunk=max(chunk, T if args.single_pass else chunk),
@@ -377,12 +399,12 @@ def run_ours(args, dist: Dist):
     # per chunk (offloaded experts run one launch per window of the ring: add up a chunk's launches)
     gu_avg_s = gu_ms / (n_chunks * k_steps if wl.offload_slots else gu_n) / 1e3
     dn_avg_s = dn_ms / (n_chunks * k_steps if wl.offload_slots else dn_n) / 1e3
-    gu_bytes, gu_flops = gate_up_bytes_and_flops(wl, offs_host, chunk_sizes)
-    dn_bytes, dn_flops = down_bytes_and_flops(wl, offs_host, chunk_sizes)
+    gu_bytes, gu_flops = gate_up_bytes_and_flops(wl, offs_host, chunk_sizes, wb)
+    dn_bytes, dn_flops = down_bytes_and_flops(wl, offs_host, chunk_sizes, wb)
     achieved = gu_bytes / gu_avg_s / 1e9
     roofline = {"bound": "hbm", "kernel": "grouped gate/up GEMM + SwiGLU", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": ncu_traffic(wl.name, chunk), "algorithmic_bytes_per_launch": gu_bytes,
+                "traffic": ncu_traffic(wl.name + ("_mxfp8" if args.weights == "mxfp8" else ""), chunk), "algorithmic_bytes_per_launch": gu_bytes,
                 "avg_launch_ms": gu_avg_s * 1e3, "peak_source": peaks["source"] + " (hbm_gbs)"}
     tc_peak = peaks["bf16_tflops_sustained"]
     grouped = {
@@ -461,8 +483,8 @@ def run_ours(args, dist: Dist):
         offs1 = torch.empty((1, wl.n_experts + 1), dtype=torch.int32, device="cuda")
         step(x, out, ch=T, offs_buf=offs1)
         o1 = offs1.cpu().numpy()
-        b1, f1 = gate_up_bytes_and_flops(wl, o1, [T])
-        b2, f2 = down_bytes_and_flops(wl, o1, [T])
+        b1, f1 = gate_up_bytes_and_flops(wl, o1, [T], wb)
+        b2, f2 = down_bytes_and_flops(wl, o1, [T], wb)
         g_s = t2["gate_up"][0] / t2["gate_up"][1] / 1e3
         d_s = t2["down"][0] / t2["down"][1] / 1e3
         single = {"tokens_per_s": T * sp_steps / sp_secs, "ms_per_step": sp_secs / sp_steps * 1e3,
@@ -493,7 +515,7 @@ def run_ours(args, dist: Dist):
             dsec = ev0.elapsed_time(ev1) / 1e3 / reps
             o = offs_d.cpu().numpy()[0]
             touched = int(((o[1:] - o[:-1]) > 0).sum())
-            wbytes = touched * 3 * wl.inter * wl.hidden * 2 + wl.n_experts * wl.hidden * 2 + \
+            wbytes = touched * 3 * wl.inter * wl.hidden * wb + wl.n_experts * wl.hidden * 2 + \
                 3 * wl.shared_inter * wl.hidden * 2
             decode[f"tokens_{n_dec}"] = {"ms_per_call": dsec * 1e3, "tokens_per_s": n_dec / dsec,
                                          "weight_bytes": wbytes, "gbs": wbytes / dsec / 1e9,
@@ -505,7 +527,7 @@ def run_ours(args, dist: Dist):
     if wl.offload_slots:
         # bytes over the host link per step, against a plain pinned copy: the routed experts of every chunk
         # (routed staging, counted on the device), else every expert of every chunk (copy engines)
-        bank = inp["w_gu"].numel() * 2 + inp["w_down"].numel() * 2
+        bank = (inp["w_gu"].numel() + inp["w_down"].numel()) * (1 if args.weights == "mxfp8" else 2)
         per_expert = bank // wl.n_experts
         if args.offload_copy == "routed":
             h2d_bytes = route_stats["experts_copied"] * per_expert
@@ -536,7 +558,14 @@ def run_ours(args, dist: Dist):
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, wl)
+        cpu_inp = inp
+        if args.weights == "mxfp8":  # the oracle runs on the decoded weights
+            import numpy as np
+            import oracle
+            dec = lambda c, sc: torch.from_numpy(oracle.dequant_mxfp8(c.numpy(), sc.numpy()).view(np.int16)).view(
+                torch.bfloat16)
+            cpu_inp = dict(inp, w_gu=dec(q["w_gu_q"], q["w_gu_s"]), w_down=dec(q["w_down_q"], q["w_down_s"]))
+        cpu = cpu_baseline(cpu_inp, wl)
 
     if dist.rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
@@ -547,6 +576,8 @@ def run_ours(args, dist: Dist):
                 "clocks": clocks_info, "grouped_gemm": grouped,
                 "routing_last_run": route_stats}
         line["config"]["combine"] = "f64-tree" if args.combine == "f64" else "f32-canonical"
+        line["config"]["weights"] = ("mxfp8 (E4M3 codes + E8M0 scale per 32 along K; bf16 tensor-core math)"
+                                     if args.weights == "mxfp8" else "bf16")
         if wl.offload_slots:
             line["config"]["offload_copy"] = args.offload_copy
         if single is not None:

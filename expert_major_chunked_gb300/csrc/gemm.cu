@@ -11,10 +11,17 @@
 // Warp roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns the TMEM allocation and lane 0 issues the
 // UMMAs; warps 2..5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..+31) and store the outputs.
 // Two TMEM accumulators of 256 columns let the epilogue of one tile overlap the main loop of the next.
+//
+// Block-scaled FP8 weights (MXFP8: E4M3 codes, one E8M0 power-of-two scale per 32 weights along K) take the variant
+// with eight more warps (448 threads). TMA lands a stage's E4M3 B tile in the upper half of the stage's B buffer
+// and its scales next to the epilogue staging; warps 6..9 (even stages) and 10..13 (odd stages) decode it to bf16
+// in place, in the same 128B-swizzled layout TMA writes, and release the stage to the UMMA issuer. A code times its scale is exactly a bf16 value, so
+// the tensor core sees exactly the decoded weights and the accumulation order is that of the bf16 path.
 #include "internal.h"
 #include "ptx.cuh"
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace moe {
 namespace {
@@ -80,8 +87,55 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+// Two E4M3 codes times the scale f (a power of two) as two bf16 values; every step is exact (E4M3 -> f16 -> f32,
+// times a power of two, -> bf16 of a value bf16 holds).
+__device__ __forceinline__ uint32_t decode_pair(uint32_t codes16, float f) {
+  const uint32_t h2 = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
+  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return pack_bf16(__fmul_rn(v.x, f), __fmul_rn(v.y, f));
+}
+
+// Decodes one stage's MXFP8 B tile in place: `rows` rows of 64 E4M3 codes, row-major in the upper half of the
+// stage's B buffer (as TMA landed them), scales sc[2][rows] (K blocks 0..31 and 32..63 of the stage). Writes bf16
+// rows of 128 B in the 128B-swizzled K-major layout (8-row atoms of 1024 B, 16-byte chunk c of row r at chunk
+// c ^ (r % 8)). Bf16 rows 128..255 overwrite the codes, so the group's 128 threads read their codes first and
+// meet at the group's named barrier before any write. `skip` (a failed wait) leaves the data alone but keeps the
+// barrier.
+__device__ __forceinline__ void decode_stage(uint8_t* bstage, const uint8_t* sc, int rows, int ct, bool skip,
+                                             uint32_t bar_id) {
+  const uint8_t* codes = bstage + kStageBBytes / 2;
+  const int items = rows * 4;  // 16-code chunks, chunk i = row i / 4, K elements 16 * (i % 4) ..
+  uint4 v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = ct + 128 * j;
+    if (!skip && i < items) v[j] = *reinterpret_cast<const uint4*>(codes + i * 16);
+  }
+  ptx::named_barrier(bar_id, 128);
+  if (skip) return;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = ct + 128 * j;
+    if (i < items) {
+      const int r = i >> 2, c = i & 3;
+      const float f = __uint_as_float(static_cast<uint32_t>(sc[(c >> 1) * rows + r]) << 23);  // 2^(s - 127)
+      const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      uint32_t o[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        o[2 * q] = decode_pair(w[q], f);
+        o[2 * q + 1] = decode_pair(w[q] >> 16, f);
+      }
+      uint8_t* rowp = bstage + (r >> 3) * 1024 + (r & 7) * 128;
+      *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
+template <int EPI, bool WQ>
+__global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -90,9 +144,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   const uint32_t sB = base + kStages * kStageABytes;
   const uint32_t bars = sB + kStages * kStageBBytes;
   uint8_t* bars_ptr = base_ptr + kStages * (kStageABytes + kStageBBytes);
-  // barrier slots: full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain
+  // barrier slots: full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain; MXFP8: decoded[kStages]
   const uint32_t full0 = bars, empty0 = bars + 8u * kStages, tfull0 = bars + 16u * kStages;
   const uint32_t tempty0 = tfull0 + 16u, drain_bar = tempty0 + 16u;
+  const uint32_t dec0 = bars + 128u;
+  const uint32_t sc0 = bars + 256u + kEpiStageBytes;  // MXFP8 scales, kStageScaleBytes per stage
+  uint8_t* sc0_ptr = bars_ptr + 256 + kEpiStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 16 * kStages + 40);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 16 * kStages + 44);
 
@@ -109,6 +166,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       ptx::mbar_init(tempty0 + 8u * a, 4 * 32);
     }
     ptx::mbar_init(drain_bar, 1);
+    if (WQ)
+      for (int s = 0; s < kStages; ++s) ptx::mbar_init(dec0 + 8u * s, 4);  // one arrival per decoder warp
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -156,7 +215,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         const void* tB = &p.tmB[ti.cls];
         const int nA = (ti.rows + kABoxRows - 1) / kABoxRows;
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
-        const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * 128u;
+        const bool q = WQ && C.b_scale != nullptr;  // E4M3 B tile (64 B rows) plus 2 scale bytes per row
+        const uint32_t b_row_bytes = q ? 64u + 2u : 128u;
+        const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * b_row_bytes;
         int b_row0, b_row1 = 0;
         const int slot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
         if (EPI == kEpiSwiGLU) {
@@ -178,7 +239,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const int kc = kb * kBlockK;
           for (int j = 0; j < nA; ++j)
             ptx::tma_load_2d(a_dst + j * (kABoxRows * 128), tA, kc, ti.a_row0 + j * kABoxRows, fb);
-          if (C.b_stream && ti.stream) {
+          if (q) {
+            // codes into the upper half of the B buffer (the converters decode them in place), then the scales
+            // of the stage's two 32-wide K blocks: plane kb32 of the group, the box's rows
+            const uint32_t c_dst = b_dst + kStageBBytes / 2;
+            const uint32_t s_dst = sc0 + stage * kStageScaleBytes;
+            const int64_t planes = 2 * C.kblocks;
+            if (C.b_stream && ti.stream) {
+              ptx::tma_load_2d_hint(c_dst, tB, kc, b_row0, fb, pol_stream);
+              if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb, pol_stream);
+            } else {
+              ptx::tma_load_2d(c_dst, tB, kc, b_row0, fb);
+              if (EPI == kEpiSwiGLU) ptx::tma_load_2d(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb);
+            }
+            for (int h = 0; h < 2; ++h) {
+              const uint8_t* plane = C.b_scale + (static_cast<int64_t>(ti.group) * planes + 2 * kb + h) *
+                                                     static_cast<int64_t>(C.b_group_rows);
+              const int r0 = b_row0 - slot * C.b_group_rows;
+              ptx::bulk_load(s_dst + h * C.n_tile, plane + r0, C.b_box_rows, fb);
+              if (EPI == kEpiSwiGLU)
+                ptx::bulk_load(s_dst + h * C.n_tile + C.b_box_rows, plane + r0 + C.b_up_offset, C.b_box_rows, fb);
+            }
+          } else if (C.b_stream && ti.stream) {
             ptx::tma_load_2d_hint(b_dst, tB, kc, b_row0, fb, pol_stream);
             if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb, pol_stream);
           } else {
@@ -224,7 +306,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxN);
         const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, static_cast<uint32_t>(C.n_tile));
         for (int kb = 0; kb < C.kblocks; ++kb) {
-          if (!ptx::wait_bounded(full0 + 8u * stage, phase, tmo, abort_flag)) {
+          if (!ptx::wait_bounded((WQ ? dec0 : full0) + 8u * stage, phase, tmo, abort_flag)) {
             raise_error(p, abort_flag, kSiteMmaFull);
             failed = true;
             break;
@@ -255,7 +337,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;
     uint32_t* stage = reinterpret_cast<uint32_t*>(bars_ptr + 256) + (warp - 2) * (32 * 33);
@@ -336,6 +418,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       ptx::tc_fence_before();
       ptx::mbar_arrive(tempty0 + 8u * acc);
     }
+  } else if (WQ) {
+    // ------------------------------------------------------------ MXFP8 decoders (warps 6..13)
+    // Group g (128 threads) takes the stages s with s % 2 == g. Every thread of a group walks the same stages and
+    // meets its group's named barrier at each E4M3 stage, also after a failed wait (then it decodes nothing), so
+    // no thread can be left waiting at the barrier.
+    const int dt = static_cast<int>(threadIdx.x) - kGemmThreads;
+    const int group = dt / 128, ct = dt % 128;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool failed = false;
+    for (int t = tfirst; t < ntiles; t += gridDim.x) {
+      const TileInfo ti = decode_tile(p, t);
+      const GemmClass& C = p.cls[ti.cls];
+      const bool q = C.b_scale != nullptr;
+      for (int kb = 0; kb < C.kblocks; ++kb) {
+        if ((stage % kDecodeGroups) == group) {
+          // one lane per warp polls the stage's barrier; the warp then shares the outcome
+          bool ok = true;
+          if (lane == 0 && !failed) ok = ptx::wait_bounded(full0 + 8u * stage, phase, tmo, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!failed && !ok) {
+            if (lane == 0) raise_error(p, abort_flag, kSiteDecodeFull);
+            failed = true;
+          }
+          if (q)
+            decode_stage(base_ptr + kStages * kStageABytes + stage * kStageBBytes,
+                         sc0_ptr + stage * kStageScaleBytes, C.n_tile, ct, failed, 1u + static_cast<uint32_t>(group));
+          // each lane's writes to the async proxy, then one arrival per warp
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(dec0 + 8u * stage);
+        }
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   }
 
   // ------------------------------------------------------------ teardown
@@ -350,19 +470,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 }  // namespace
 
 cudaError_t prepare_gemm_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kGemmSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kGemmSmemBytes);
+  const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32, false>, attr, kGemmSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU, false>, attr, kGemmSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32, true>, attr, kGemmSmemBytesQ);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU, true>, attr, kGemmSmemBytesQ);
+  return e;
 }
 
-cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream, bool mxfp8) {
   if (grid <= 0) return cudaSuccess;
-  if (epilogue == kEpiSwiGLU)
-    grouped_gemm_kernel<kEpiSwiGLU><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
-  else
-    grouped_gemm_kernel<kEpiF32><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  if (mxfp8) {
+    if (epilogue == kEpiSwiGLU)
+      grouped_gemm_kernel<kEpiSwiGLU, true><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+    else
+      grouped_gemm_kernel<kEpiF32, true><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+  } else if (epilogue == kEpiSwiGLU) {
+    grouped_gemm_kernel<kEpiSwiGLU, false><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  } else {
+    grouped_gemm_kernel<kEpiF32, false><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

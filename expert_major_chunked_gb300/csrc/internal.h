@@ -21,6 +21,7 @@ enum DeviceErrorSite : int32_t {
   kSiteStallFlag = 5,
   kSiteDrain = 6,
   kSiteRouting = 7,
+  kSiteDecodeFull = 8,  // an MXFP8 decoder warp waiting for its stage
 };
 __host__ __device__ inline int32_t dev_error_code(int32_t kind, int32_t site, int32_t block) {
   return kind | (site << 8) | ((block > 0xFFFF ? 0xFFFF : block) << 16);
@@ -51,6 +52,14 @@ constexpr int kStageABytes = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBBytes = kMaxN * kBlockK * 2;     // 32 KB
 constexpr int kEpiStageBytes = 4 * 32 * 33 * 4;            // epilogue staging: a 32 x 33-word block per warp
 constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + 256 + kEpiStageBytes;
+// Block-scaled FP8 weights (MXFP8): 8 more warps, in two groups of 4 taking alternate stages, convert each
+// stage's E4M3 B tile (landed by TMA in the upper half of the stage's B buffer) to bf16 in place; the E8M0 scales
+// of a stage (2 K blocks x up to 256 rows) sit after the epilogue staging.
+constexpr int kDecodeGroups = 2;
+constexpr int kGemmThreadsQ = kGemmThreads + kDecodeGroups * 128;
+static_assert(kStages % kDecodeGroups == 0, "decoder groups take stages by parity");
+constexpr int kStageScaleBytes = 2 * kMaxN;
+constexpr int kGemmSmemBytesQ = kGemmSmemBytes + kStages * kStageScaleBytes;
 
 enum Epilogue : int { kEpiF32 = 0, kEpiSwiGLU = 1 };
 
@@ -66,6 +75,8 @@ struct GemmClass {
   int32_t b_group_mod;    // > 0: B holds a ring of b_group_mod groups and group e lives in slot e % b_group_mod
   int64_t out_ld;         // output row stride in elements
   void* out;              // F32: float*, SwiGLU: bf16*
+  const uint8_t* b_scale; // MXFP8 B (kernel variant with converter warps): E8M0 scales [G][K/32][b_group_rows];
+                          // nullptr: B is bf16
 };
 
 // Tile record: x = group | (cls << 15) | (n_idx << 16) | (stream << 31); y = first A row; z = valid rows (1..128);
@@ -88,7 +99,9 @@ struct GemmParams {
   uint64_t timeout_ns;        // bound on every mbarrier wait
 };
 
-cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream);
+// mxfp8: the variant whose classes may hold MXFP8 B (a class with b_scale != nullptr; its tmB is a uint8 map).
+cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream,
+                                bool mxfp8 = false);
 cudaError_t prepare_gemm_kernels();   // sets the dynamic shared memory attribute (once per device)
 
 // ------------------------------------------------------------------ routing

@@ -79,6 +79,24 @@ moe_status encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return MOE_OK;
 }
 
+// E4M3 code matrix [rows][cols] (one byte per element, row-major), boxes of box_rows x 64 codes, no swizzle (the
+// MXFP8 decoder warps read the rows densely), zero fill out of range.
+moe_status encode_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu x %llu] code matrix, box %u rows",
+                (int)r, (unsigned long long)rows, (unsigned long long)cols, box_rows);
+  return MOE_OK;
+}
+
 // ------------------------------------------------------------------ device checks
 moe_status check_device(int* device, int* num_sms) {
   CUDA_TRY(cudaGetDevice(device));
@@ -117,6 +135,7 @@ constexpr int kRouteSpan = 16384;
 
 struct Shape {
   int H, E, I, k, Is, C, span_cap, slots, window;
+  int wbytes;  // bytes per routed expert weight: 2 (bf16) or 1 (MXFP8 code)
   int gu_half, gu_half_s, bn_down, bn_router_narrow, bn_router_wide;
   int nt_gu, nt_gu_s, nt_down;
 };
@@ -131,6 +150,7 @@ Shape make_shape(const moe_dims& d) {
   s.C = d.max_chunk;
   s.span_cap = std::max(s.C, kRouteSpan);
   s.slots = d.offload_slots;
+  s.wbytes = 2;
   s.window = d.offload_slots / 2;
   s.gu_half = (s.I % 128 == 0) ? 128 : 64;
   s.gu_half_s = (s.Is % 128 == 0) ? 128 : 64;
@@ -180,8 +200,8 @@ Layout make_layout(const Shape& s) {
     L.tile_base[b] = take(2 * (E + 1) * 4);
   }
   const size_t S = static_cast<size_t>(s.slots);
-  L.ring_gu = take(S * 2 * I * H * 2);
-  L.ring_down = take(S * H * I * 2);
+  L.ring_gu = take(S * 2 * I * H * s.wbytes);
+  L.ring_down = take(S * H * I * s.wbytes);
   L.h = take(R * I * 2);
   L.hs = take(Is > 0 ? C * Is * 2 : 0);
   L.y = take(R * H * 4);
@@ -208,6 +228,9 @@ struct moe_plan {
   const void* bank_gu_dev = nullptr;
   const void* bank_down_dev = nullptr;
   int32_t offload_copy = MOE_OFFLOAD_COPY_ALL;
+  // MXFP8 routed experts: w_gu / w_down hold E4M3 codes, these their E8M0 scales ([E][K/32][rows])
+  const uint8_t* w_gu_scale = nullptr;
+  const uint8_t* w_down_scale = nullptr;
   cudaStream_t own_copy = nullptr;
   cudaEvent_t ev_copy[2] = {}, ev_rel[2] = {};
   // Each chunk's member lists (count, scan, permute) run on a side stream so that they overlap the previous chunk's
@@ -306,13 +329,18 @@ size_t plan_workspace_bytes(moe_plan_t plan) { return plan ? plan->lay.total : 0
 void set_last_error(const char* msg) { g_last_error = msg; }
 }  // namespace moe
 
-extern "C" {
+namespace {
 
-moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
-                            const void* ws_gu, const void* ws_down, size_t* workspace_bytes, moe_plan_t* plan) {
+moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
+                     const void* ws_gu, const void* ws_down, const void* gu_scale, const void* down_scale,
+                     size_t* workspace_bytes, moe_plan_t* plan) {
   if (plan) *plan = nullptr;
   moe_status st = validate_dims(dims);
   if (st != MOE_OK) return st;
+  const bool mxfp8 = gu_scale != nullptr || down_scale != nullptr;
+  if (mxfp8 && (!gu_scale || !down_scale)) return fail(MOE_ERR_INVALID_ARG, "both scale arrays are needed");
+  if (mxfp8 && (!aligned16(gu_scale) || !aligned16(down_scale)))
+    return fail(MOE_ERR_INVALID_ARG, "scale arrays must be 16-byte aligned");
   if (!workspace_bytes || !plan) return fail(MOE_ERR_INVALID_ARG, "workspace_bytes and plan must not be NULL");
   if (!w_router || !w_gu || !w_down) return fail(MOE_ERR_INVALID_ARG, "weight pointers must not be NULL");
   if (dims->shared_inter > 0 && (!ws_gu || !ws_down))
@@ -328,6 +356,7 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   moe_plan* p = new moe_plan();
   p->d = *dims;
   p->sh = make_shape(*dims);
+  if (mxfp8) p->sh.wbytes = 1;
   p->lay = make_layout(p->sh);
   p->device = device;
   p->num_sms = num_sms;
@@ -336,7 +365,20 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   p->w_down = w_down;
   p->ws_gu = ws_gu;
   p->ws_down = ws_down;
+  p->w_gu_scale = static_cast<const uint8_t*>(gu_scale);
+  p->w_down_scale = static_cast<const uint8_t*>(down_scale);
   const Shape& s = p->sh;
+  if (mxfp8) {
+    // the GEMM streams the scales with bulk copies: they stay in device memory, also when the codes are offloaded
+    for (const void* q : {gu_scale, down_scale}) {
+      cudaPointerAttributes a;
+      if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();
+        delete p;
+        return fail(MOE_ERR_INVALID_ARG, "MXFP8 scale arrays must be in device memory");
+      }
+    }
+  }
   p->offload = dims->offload_slots > 0;
   if (p->offload) {
     // the expert banks stay in host memory: they must be page-locked so the copy engines can read them
@@ -360,10 +402,14 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   }
   st = encode_bf16_2d(&p->tm_wr_narrow, w_router, s.E, s.H, s.bn_router_narrow);
   if (st == MOE_OK) st = encode_bf16_2d(&p->tm_wr_wide, w_router, s.E, s.H, s.bn_router_wide);
-  if (st == MOE_OK && !p->offload)
+  if (st == MOE_OK && !p->offload && !mxfp8)
     st = encode_bf16_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H, s.gu_half);
-  if (st == MOE_OK && !p->offload)
+  if (st == MOE_OK && !p->offload && !mxfp8)
     st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
+  if (st == MOE_OK && mxfp8 && !p->offload)
+    st = encode_u8_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H, s.gu_half);
+  if (st == MOE_OK && mxfp8 && !p->offload)
+    st = encode_u8_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
   if (st == MOE_OK) {
@@ -385,6 +431,25 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
   *workspace_bytes = p->lay.total;
   *plan = p;
   return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
+                            const void* ws_gu, const void* ws_down, size_t* workspace_bytes, moe_plan_t* plan) {
+  return plan_impl(dims, w_router, w_gu, w_down, ws_gu, ws_down, nullptr, nullptr, workspace_bytes, plan);
+}
+
+moe_status moe_prefill_plan_mxfp8(const moe_dims* dims, const void* w_router, const uint8_t* w_gu_codes,
+                                  const uint8_t* w_gu_scales, const uint8_t* w_down_codes,
+                                  const uint8_t* w_down_scales, const void* ws_gu, const void* ws_down,
+                                  size_t* workspace_bytes, moe_plan_t* plan) {
+  if (plan) *plan = nullptr;
+  if (!w_gu_scales || !w_down_scales) return fail(MOE_ERR_INVALID_ARG, "scale arrays must not be NULL");
+  return plan_impl(dims, w_router, w_gu_codes, w_down_codes, ws_gu, ws_down, w_gu_scales, w_down_scales,
+                   workspace_bytes, plan);
 }
 
 moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void* workspace,
@@ -436,10 +501,11 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_xp[1], ws + L.xp[1], R, s.H, kABoxRows);
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_h, h, R, s.I, kABoxRows);
     if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(&p->tm_hs, hs, s.C, s.Is, kABoxRows);
+    auto encode_w = s.wbytes == 1 ? encode_u8_2d : encode_bf16_2d;  // ring slots hold codes or bf16 weights
     if (rc == MOE_OK && p->offload)
-      rc = encode_bf16_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
+      rc = encode_w(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
     if (rc == MOE_OK && p->offload)
-      rc = encode_bf16_2d(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I, s.bn_down);
+      rc = encode_w(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I, s.bn_down);
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;
@@ -488,7 +554,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     memset(&g, 0, sizeof g);
     g.tmA[0] = g.tmA[1] = tm_x;
     g.tmB[0] = g.tmB[1] = wide ? p->tm_wr_wide : p->tm_wr_narrow;
-    GemmClass rc0;
+    GemmClass rc0{};
     rc0.kblocks = s.H / kBlockK;
     rc0.n_tile = bn_router;
     rc0.b_box_rows = bn_router;
@@ -601,7 +667,8 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     auto copy_window = [&](int64_t cidx, int e0) -> moe_status {
       const int hb = (e0 / s.window) & 1;
       const size_t slot0 = static_cast<size_t>(e0 % s.slots);
-      const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H * 2, dn_bytes = static_cast<size_t>(s.H) * s.I * 2;
+      const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H * s.wbytes;
+      const size_t dn_bytes = static_cast<size_t>(s.H) * s.I * s.wbytes;
       moe_status r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[hb], 0), "slot release wait");
       if (r2 == MOE_OK && p->offload_copy == MOE_OFFLOAD_COPY_ROUTED) {
         // only the experts this chunk routes rows to, decided on the device once its member lists exist
@@ -654,7 +721,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       memset(&gu, 0, sizeof gu);
       gu.tmA[0] = p->tm_xp[par];
       gu.tmB[0] = windowed ? p->tm_ring_gu : p->tm_wgu;
-      GemmClass c_r;
+      GemmClass c_r{};
       c_r.kblocks = s.H / kBlockK;
       c_r.n_tile = 2 * s.gu_half;
       c_r.b_box_rows = s.gu_half;
@@ -665,11 +732,12 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       c_r.b_group_mod = windowed ? s.slots : 0;
       c_r.out_ld = s.I;
       c_r.out = h;
+      c_r.b_scale = p->w_gu_scale;
       gu.cls[0] = c_r;
       if (s.Is > 0) {
         gu.tmA[1] = tm_x;
         gu.tmB[1] = p->tm_wsgu;
-        GemmClass c_s;
+        GemmClass c_s{};
         c_s.kblocks = s.H / kBlockK;
         c_s.n_tile = 2 * s.gu_half_s;
         c_s.b_box_rows = s.gu_half_s;
@@ -696,7 +764,9 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       gu.timeout_ns = p->timeout_ns;
       {
         LaunchScope ls(p, MOE_KERNEL_GATE_UP, st);
-        r2 = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st), "gate/up launch");
+        r2 = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st,
+                                             p->w_gu_scale != nullptr),
+                         "gate/up launch");
       }
       if (r2 != MOE_OK) return r2;
 
@@ -708,7 +778,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       memset(&dn, 0, sizeof dn);
       dn.tmA[0] = p->tm_h;
       dn.tmB[0] = windowed ? p->tm_ring_down : p->tm_wdown;
-      GemmClass d_r;
+      GemmClass d_r{};
       d_r.kblocks = s.I / kBlockK;
       d_r.n_tile = s.bn_down;
       d_r.b_box_rows = s.bn_down;
@@ -719,11 +789,13 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       d_r.b_group_mod = windowed ? s.slots : 0;
       d_r.out_ld = s.H;
       d_r.out = y;
+      d_r.b_scale = p->w_down_scale;
       dn.cls[0] = d_r;
       if (s.Is > 0) {
         dn.tmA[1] = p->tm_hs;
         dn.tmB[1] = p->tm_wsdown;
         GemmClass d_s = d_r;
+        d_s.b_scale = nullptr;
         d_s.kblocks = s.Is / kBlockK;
         d_s.b_group_rows = 0;
         d_s.b_stream = 0;
@@ -745,7 +817,9 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
       dn.timeout_ns = p->timeout_ns;
       {
         LaunchScope ls(p, MOE_KERNEL_DOWN, st);
-        r2 = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st), "down launch");
+        r2 = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st,
+                                             p->w_down_scale != nullptr),
+                         "down launch");
       }
       if (r2 != MOE_OK) return r2;
       if (windowed) {
@@ -1033,7 +1107,7 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
   if (st != MOE_OK) return st;
   GemmParams g;
   memset(&g, 0, sizeof g);
-  GemmClass cl;
+  GemmClass cl{};
   cl.kblocks = k_dim / kBlockK;
   cl.b_group_rows = 0;
   cl.out_cols = n;

@@ -83,6 +83,32 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t smem_dst, const void* 
       : "memory");
 }
 
+// Plain (non-tensor) bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte aligned),
+// completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Makes this thread's ordinary shared-memory writes visible to the async proxy (TMA, tensor core).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Barrier over `count` threads (a multiple of 32) of the CTA, id 1..15 (0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Two E4M3 codes (low byte -> low half) to two f16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
+  uint32_t out;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(out) : "h"(codes));
+  return out;
+}
+
 // L2 policy for data read once and not needed again soon (streamed expert weights).
 __device__ __forceinline__ uint64_t make_policy_evict_first() {
   uint64_t pol;

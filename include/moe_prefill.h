@@ -94,6 +94,29 @@ moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const vo
                             const void* ws_gu, const void* ws_down, size_t* workspace_bytes, moe_plan_t* plan);
 
 /*
+ * moe_prefill_plan_mxfp8 — moe_prefill_plan for routed experts stored as block-scaled FP8 (MXFP8).
+ * The deep-prefill draft's review ("To land") quantises the weights of prompt tiles (NVFP4) and asks for the same
+ * bytes as decode; this is the 8-bit block-scaled member of that family (OCP Microscaling Formats v1.0, MXFP8
+ * E4M3), for the bytes that bound the layer: the routed experts' weights are read at half the bf16 size.
+ *   w_gu_codes    device uint8 [E][2I][H]: E4M3 codes (1 sign, 4 exponent bits with bias 7, 3 fraction bits;
+ *                 exponent field 0 = subnormals m/8 * 2^-6), same row order as w_gu.
+ *   w_gu_scales   device uint8 [E][H/32][2I]: E8M0 scale s of each 32-wide K block (value 2^(s-127)), one plane
+ *                 of 2I bytes per K block.
+ *   w_down_codes  device uint8 [E][H][I];  w_down_scales: device uint8 [E][I/32][H].
+ *   Other arguments as for moe_prefill_plan (router and shared expert stay bf16). With offload_slots > 0 the two
+ *   code arrays are pinned host memory staged through the ring like bf16 banks (half the bytes over the host
+ *   link); the scale arrays stay in device memory in every case. All pointers 16-byte aligned.
+ * A weight is code * 2^(s-127). The kernels decode each tile to bf16 in shared memory and run the bf16 tensor-core
+ * path on it; the results equal, byte for byte, moe_prefill_plan on the decoded bf16 weights, provided every
+ * decoded weight is exactly a bf16 value: no NaN code (0x7F, 0xFF), scales in [10, 246] (then every code times
+ * its scale is a normal bf16 number). These are not checked on the device.
+ */
+moe_status moe_prefill_plan_mxfp8(const moe_dims* dims, const void* w_router, const uint8_t* w_gu_codes,
+                                  const uint8_t* w_gu_scales, const uint8_t* w_down_codes,
+                                  const uint8_t* w_down_scales, const void* ws_gu, const void* ws_down,
+                                  size_t* workspace_bytes, moe_plan_t* plan);
+
+/*
  * moe_prefill_run — the layer over T tokens, in chunks of `chunk` tokens (the last chunk may be shorter).
  *   x               device bf16 [T][H].
  *   T               tokens (T == 0: no-op, MOE_OK).
