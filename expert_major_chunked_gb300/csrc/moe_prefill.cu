@@ -542,66 +542,69 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     int32_t* span_ids = topk_id ? topk_id + s0 * s.k : reinterpret_cast<int32_t*>(ws + L.topk_id);
     float* span_w = topk_w ? topk_w + s0 * s.k : reinterpret_cast<float*>(ws + L.topk_w);
 
-    // the previous span's combines and member lists read this span's buffers (logits, top-k): wait for them
+    // Routing of the tokens [g0, g0 + ng) of this span on stream `rs`: router GEMM (logits, fp32), then top-k with
+    // weights and the float64 recheck of tokens whose fp32 selection is not certain. Results land at the tokens'
+    // offsets in the span buffers.
+    auto route = [&](int64_t g0, int ng, cudaStream_t rs) -> moe_status {
+      const int64_t off = g0 - s0;
+      const bool wide = ng >= 4096;
+      const int bn_router = wide ? s.bn_router_wide : s.bn_router_narrow;
+      const int nt_router = (s.E + bn_router - 1) / bn_router;
+      GemmParams g;
+      memset(&g, 0, sizeof g);
+      g.tmA[0] = g.tmA[1] = tm_x;
+      g.tmB[0] = g.tmB[1] = wide ? p->tm_wr_wide : p->tm_wr_narrow;
+      GemmClass rc0{};
+      rc0.kblocks = s.H / kBlockK;
+      rc0.n_tile = bn_router;
+      rc0.b_box_rows = bn_router;
+      rc0.out_cols = s.E;
+      rc0.out_ld = s.E;
+      rc0.out = logits + off * s.E;
+      g.cls[0] = g.cls[1] = rc0;
+      g.tiles = nullptr;
+      g.num_tiles = nullptr;
+      g.dense_m = ng;
+      g.dense_n_tiles = nt_router;
+      g.dense_a_row0 = static_cast<int32_t>(g0);
+      g.err = &hdr->err;
+      g.stall_flag = nullptr;
+      g.timeout_ns = p->timeout_ns;
+      moe_status r2;
+      {
+        const int tiles = ((ng + kBlockM - 1) / kBlockM) * nt_router;
+        LaunchScope ls(p, MOE_KERNEL_ROUTER, rs);
+        r2 = cuda_status(launch_grouped_gemm(g, kEpiF32, std::min(p->num_sms, tiles), rs), "router GEMM launch");
+      }
+      if (r2 != MOE_OK) return r2;
+      RouteParams r;
+      r.logits = logits + off * s.E;
+      r.x = static_cast<const uint16_t*>(x) + g0 * s.H;
+      r.w_router = static_cast<const uint16_t*>(p->w_router);
+      r.wnorm = wnorm;
+      r.hdr = hdr;
+      r.n = ng;
+      r.E = s.E;
+      r.H = s.H;
+      r.k = s.k;
+      r.tau_coef = tau_coef;
+      r.topk_id = span_ids + off * s.k;
+      r.topk_w = span_w + off * s.k;
+      r.band_flag = band + off;
+      r.band_info = reinterpret_cast<BandInfo*>(ws + L.band_info);
+      r.band_grid = p->num_sms;
+      LaunchScope ls(p, MOE_KERNEL_TOPK, rs, 2);  // top-k, then the float64 recheck of flagged tokens
+      return cuda_status(launch_topk(r, rs), "top-k launch");
+    };
+
+    // The span's first chunk is routed on `compute` before anything else; the rest of the span is routed on the
+    // side stream after the first chunk's member lists, so it runs beside the first chunk's GEMMs, and the member
+    // lists of later chunks follow it on that stream. Routing is per token: splitting it changes no result.
+    // The previous span's combines and member lists read this span's buffers (logits, top-k): wait for them.
     rc = cuda_status(cudaStreamWaitEvent(st, p->ev_comb, 0), "span start wait");
     if (rc != MOE_OK) return join(rc);
-
-    // 1. router GEMM: logits [ns][E] fp32
-    const bool wide = ns >= 4096;
-    const int bn_router = wide ? s.bn_router_wide : s.bn_router_narrow;
-    const int nt_router = (s.E + bn_router - 1) / bn_router;
-    GemmParams g;
-    memset(&g, 0, sizeof g);
-    g.tmA[0] = g.tmA[1] = tm_x;
-    g.tmB[0] = g.tmB[1] = wide ? p->tm_wr_wide : p->tm_wr_narrow;
-    GemmClass rc0{};
-    rc0.kblocks = s.H / kBlockK;
-    rc0.n_tile = bn_router;
-    rc0.b_box_rows = bn_router;
-    rc0.b_group_rows = 0;
-    rc0.b_up_offset = 0;
-    rc0.out_cols = s.E;
-    rc0.b_stream = 0;
-    rc0.b_group_mod = 0;
-    rc0.out_ld = s.E;
-    rc0.out = logits;
-    g.cls[0] = g.cls[1] = rc0;
-    g.tiles = nullptr;
-    g.num_tiles = nullptr;
-    g.dense_m = ns;
-    g.dense_n_tiles = nt_router;
-    g.dense_a_row0 = static_cast<int32_t>(s0);
-    g.err = &hdr->err;
-    g.stall_flag = nullptr;
-    g.timeout_ns = p->timeout_ns;
-    {
-      const int tiles = ((ns + kBlockM - 1) / kBlockM) * nt_router;
-      LaunchScope ls(p, MOE_KERNEL_ROUTER, st);
-      rc = cuda_status(launch_grouped_gemm(g, kEpiF32, std::min(p->num_sms, tiles), st), "router GEMM launch");
-    }
-    if (rc != MOE_OK) return join(rc);
-
-    // 2. top-k + weights (and the float64 recheck of tokens whose fp32 selection is not certain)
-    RouteParams r;
-    r.logits = logits;
-    r.x = static_cast<const uint16_t*>(x) + s0 * s.H;
-    r.w_router = static_cast<const uint16_t*>(p->w_router);
-    r.wnorm = wnorm;
-    r.hdr = hdr;
-    r.n = ns;
-    r.E = s.E;
-    r.H = s.H;
-    r.k = s.k;
-    r.tau_coef = tau_coef;
-    r.topk_id = span_ids;
-    r.topk_w = span_w;
-    r.band_flag = band;
-    r.band_info = reinterpret_cast<BandInfo*>(ws + L.band_info);
-    r.band_grid = p->num_sms;
-    {
-      LaunchScope ls(p, MOE_KERNEL_TOPK, st, 2);  // top-k, then the float64 recheck of flagged tokens
-      rc = cuda_status(launch_topk(r, st), "top-k launch");
-    }
+    const int head = static_cast<int>(std::min<int64_t>(chunk, ns));
+    rc = route(s0, head, st);
     if (rc == MOE_OK) rc = cuda_status(cudaEventRecord(p->ev_span, st), "span event");
     if (rc != MOE_OK) return join(rc);
 
@@ -866,6 +869,7 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
 
     rc = cuda_status(cudaStreamWaitEvent(side, p->ev_span, 0), "span wait");
     if (rc == MOE_OK) rc = lists(s0, chunk_idx);
+    if (rc == MOE_OK && ns > head) rc = route(s0 + head, ns - head, side);
     if (rc != MOE_OK) return join(rc);
     for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
       if (!p->offload) {
