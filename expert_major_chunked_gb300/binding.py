@@ -42,6 +42,8 @@ _SIGS = {
                                 ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_P)], ctypes.c_int),
     "moe_prefill_run": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
+    "moe_prefill_run_host": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P, _P,
+                              _P, _P, _P], ctypes.c_int),
     "moe_prefill_combine": ([_P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
     "moe_prefill_combine_partial_f64": ([_P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P], ctypes.c_int),
@@ -282,6 +284,22 @@ class MoePrefill:
     def set_combine(self, mode: int):
         """COMBINE_F32 (canonical float32, ascending expert id; default) or COMBINE_F64_TREE."""
         moe_prefill_set_combine(self.plan, mode)
+
+    def run_host(self, x_host, chunk: int, x_dev, out_dev, out_host, topk_id=None, topk_w=None,
+                 expert_offsets=None, row_token=None, stream=None, copy_stream=None):
+        """The layer on pinned host activations: X rows in, out rows back, overlapped with the compute.
+        x_dev / out_dev are device staging tensors shaped like x_host."""
+        import torch
+        for t, where in ((x_host, "host"), (out_host, "host"), (x_dev, "dev"), (out_dev, "dev")):
+            if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.is_cuda != (where == "dev"):
+                raise ValueError("run_host needs contiguous bf16 pinned host x/out and device staging tensors")
+        T = x_host.shape[0]
+        _check(lib().moe_prefill_run_host(self.plan, x_host.data_ptr(), T, chunk, self.workspace.data_ptr(),
+                                          self.workspace_bytes, x_dev.data_ptr(), out_dev.data_ptr(),
+                                          out_host.data_ptr(), _ptr(topk_id), _ptr(topk_w), _ptr(expert_offsets),
+                                          _ptr(row_token), _stream_handle(stream),
+                                          copy_stream.cuda_stream if copy_stream is not None else None))
+        return out_host
 
     def check(self, stream=None) -> int:
         return moe_prefill_check(self.workspace.data_ptr(), _stream_handle(stream))

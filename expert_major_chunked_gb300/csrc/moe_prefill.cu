@@ -238,6 +238,9 @@ struct moe_plan {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_span = nullptr, ev_join = nullptr, ev_ready[2] = {}, ev_down = nullptr,
               ev_comb = nullptr;
+  // runs from host buffers (moe_prefill_run_host): activations move on their own stream, chunk by chunk
+  cudaStream_t host_io = nullptr;
+  cudaEvent_t ev_x_head = nullptr, ev_x_rest = nullptr;
   uint64_t timeout_ns = 2000000000ull;
   int32_t combine_mode = MOE_COMBINE_F32;
   int64_t launches = 0;
@@ -417,9 +420,10 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&p->side, cudaStreamNonBlocking, hi);
     if (e == cudaSuccess && p->offload) e = cudaStreamCreateWithFlags(&p->own_copy, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->host_io, cudaStreamNonBlocking);
     cudaEvent_t* evs[] = {&p->ev_fork,    &p->ev_span,    &p->ev_join,    &p->ev_ready[0], &p->ev_ready[1],
                           &p->ev_down,    &p->ev_comb,    &p->ev_copy[0], &p->ev_copy[1], &p->ev_rel[0],
-                          &p->ev_rel[1]};
+                          &p->ev_rel[1],  &p->ev_x_head,  &p->ev_x_rest};
     for (cudaEvent_t* ev : evs)
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) st = fail(MOE_ERR_CUDA, "stream/event creation: %s", cudaGetErrorString(e));
@@ -452,9 +456,20 @@ moe_status moe_prefill_plan_mxfp8(const moe_dims* dims, const void* w_router, co
                    workspace_bytes, plan);
 }
 
-moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void* workspace,
-                           size_t workspace_bytes, void* out, int32_t* topk_id, float* topk_w,
-                           int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute_, moe_stream_t copy) {
+}  // extern "C"
+
+namespace {
+
+// Host buffers of moe_prefill_run_host: X rows are copied into the device staging rows before the routing and the
+// member lists that read them, out rows back once their chunk's combine has written them.
+struct HostIO {
+  const void* x_host;
+  void* out_host;
+};
+
+moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void* workspace, size_t workspace_bytes,
+                    void* out, int32_t* topk_id, float* topk_w, int32_t* expert_offsets, int32_t* row_token,
+                    moe_stream_t compute_, moe_stream_t copy, const HostIO* hio) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
   if (T < 0) return fail(MOE_ERR_INVALID_ARG, "T must be >= 0");
   if (chunk < 1 || chunk > p->d.max_chunk)
@@ -518,12 +533,45 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   rc = cuda_status(cudaEventRecord(p->ev_fork, st), "fork event");
   if (rc == MOE_OK) rc = cuda_status(cudaStreamWaitEvent(side, p->ev_fork, 0), "fork wait");
   if (rc == MOE_OK && p->offload) rc = cuda_status(cudaStreamWaitEvent(cp, p->ev_fork, 0), "fork wait");
+  if (rc == MOE_OK && hio) rc = cuda_status(cudaStreamWaitEvent(p->host_io, p->ev_fork, 0), "fork wait");
   if (rc != MOE_OK) return rc;
   auto join = [&](moe_status r) {
     if (cudaEventRecord(p->ev_join, side) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
     if (p->offload && cudaEventRecord(p->ev_join, cp) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
+    if (hio && cudaEventRecord(p->ev_join, p->host_io) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
     return r;
   };
+  // A span is routed in two segments: its first chunk (on `compute`, before anything else) and the rest (on the
+  // side stream, beside the first chunk's GEMMs). With host buffers the span's X rows go to the device in the same
+  // two copies, each with its event, so each segment starts once its own rows have landed.
+  const int64_t span = static_cast<int64_t>(chunk) * std::max(1, s.span_cap / chunk);
+  auto segments = [&](int64_t a0, int64_t* n1, int64_t* n2) {
+    const int64_t n_span = std::min<int64_t>(span, T - a0);
+    *n1 = std::min<int64_t>(chunk, n_span);
+    *n2 = n_span - *n1;
+  };
+  const size_t row_bytes = static_cast<size_t>(s.H) * 2;
+  auto copy_x_span = [&](int64_t a0) -> moe_status {
+    int64_t n1, n2;
+    segments(a0, &n1, &n2);
+    const char* src = static_cast<const char*>(hio->x_host) + a0 * row_bytes;
+    char* dst = static_cast<char*>(const_cast<void*>(x)) + a0 * row_bytes;
+    moe_status r2 = MOE_OK;
+    const int64_t lens[2] = {n1, n2};
+    cudaEvent_t evs[2] = {p->ev_x_head, p->ev_x_rest};
+    for (int i = 0; i < 2 && r2 == MOE_OK; ++i) {
+      if (lens[i] > 0)
+        r2 = cuda_status(cudaMemcpyAsync(dst, src, lens[i] * row_bytes, cudaMemcpyHostToDevice, p->host_io), "X copy");
+      if (r2 == MOE_OK) r2 = cuda_status(cudaEventRecord(evs[i], p->host_io), "X event");
+      dst += lens[i] * row_bytes;
+      src += lens[i] * row_bytes;
+    }
+    return r2;
+  };
+  if (hio) {
+    rc = copy_x_span(0);
+    if (rc != MOE_OK) return join(rc);
+  }
 
   {
     LaunchScope ls(p, MOE_KERNEL_NORMS, st);
@@ -534,7 +582,6 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
 
   // |fp32 tensor-core logit - exact| <= one ulp per 16-wide K step of a partial sum bounded by ||x|| ||w||
   const float tau_coef = static_cast<float>(s.H / 16 + 1) * 0x1p-23f;
-  const int64_t span = static_cast<int64_t>(chunk) * std::max(1, s.span_cap / chunk);
   int64_t chunk_idx = 0;
   for (int64_t s0 = 0; s0 < T; s0 += span) {
     // ---------------------------------------------------------------- routing of the span's tokens
@@ -598,12 +645,15 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
     };
 
     // The span's first chunk is routed on `compute` before anything else; the rest of the span is routed on the
-    // side stream after the first chunk's member lists, so it runs beside the first chunk's GEMMs, and the member
-    // lists of later chunks follow it on that stream. Routing is per token: splitting it changes no result.
+    // side stream after the first chunk's member lists, beside the first chunk's GEMMs, and the member lists of
+    // later chunks follow it on that stream. Routing is per token: splitting it changes no result.
     // The previous span's combines and member lists read this span's buffers (logits, top-k): wait for them.
     rc = cuda_status(cudaStreamWaitEvent(st, p->ev_comb, 0), "span start wait");
+    if (rc == MOE_OK && hio) rc = cuda_status(cudaStreamWaitEvent(st, p->ev_x_head, 0), "X wait");
     if (rc != MOE_OK) return join(rc);
-    const int head = static_cast<int>(std::min<int64_t>(chunk, ns));
+    int64_t n1, n2;
+    segments(s0, &n1, &n2);
+    const int head = static_cast<int>(n1);
     rc = route(s0, head, st);
     if (rc == MOE_OK) rc = cuda_status(cudaEventRecord(p->ev_span, st), "span event");
     if (rc != MOE_OK) return join(rc);
@@ -864,12 +914,25 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
         }
       }
       if (r2 != MOE_OK) return r2;
-      return cuda_status(cudaEventRecord(p->ev_comb, side), "combine event");
+      r2 = cuda_status(cudaEventRecord(p->ev_comb, side), "combine event");
+      if (r2 == MOE_OK && hio) {
+        // the chunk's out rows back to the host once its combine has written them
+        r2 = cuda_status(cudaStreamWaitEvent(p->host_io, p->ev_comb, 0), "out wait");
+        if (r2 == MOE_OK)
+          r2 = cuda_status(cudaMemcpyAsync(static_cast<char*>(hio->out_host) + c0 * row_bytes,
+                                           static_cast<const char*>(out) + c0 * row_bytes, n * row_bytes,
+                                           cudaMemcpyDeviceToHost, p->host_io),
+                           "out copy");
+      }
+      return r2;
     };
 
     rc = cuda_status(cudaStreamWaitEvent(side, p->ev_span, 0), "span wait");
     if (rc == MOE_OK) rc = lists(s0, chunk_idx);
-    if (rc == MOE_OK && ns > head) rc = route(s0 + head, ns - head, side);
+    if (rc == MOE_OK && hio) rc = cuda_status(cudaStreamWaitEvent(side, p->ev_x_rest, 0), "X wait");
+    if (rc == MOE_OK && n2 > 0) rc = route(s0 + n1, static_cast<int>(n2), side);
+    // both waits of this span are enqueued: the next span's X rows may now reuse the events
+    if (rc == MOE_OK && hio && s0 + span < T) rc = copy_x_span(s0 + span);
     if (rc != MOE_OK) return join(rc);
     for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
       if (!p->offload) {
@@ -887,6 +950,40 @@ moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk
   }
   // The side stream's last combine joins `compute` here: the run ends after all of its work.
   return join(MOE_OK);
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_prefill_run(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void* workspace,
+                           size_t workspace_bytes, void* out, int32_t* topk_id, float* topk_w,
+                           int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute, moe_stream_t copy) {
+  return run_impl(p, x, T, chunk, workspace, workspace_bytes, out, topk_id, topk_w, expert_offsets, row_token,
+                  compute, copy, nullptr);
+}
+
+moe_status moe_prefill_run_host(moe_plan_t p, const void* x_host, int64_t T, int32_t chunk, void* workspace,
+                                size_t workspace_bytes, void* x_dev, void* out_dev, void* out_host, int32_t* topk_id,
+                                float* topk_w, int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute,
+                                moe_stream_t copy) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (T > 0) {
+    if (!x_host || !out_host || !x_dev || !out_dev)
+      return fail(MOE_ERR_INVALID_ARG, "x_host, out_host, x_dev and out_dev must not be NULL");
+    for (const void* q : {x_host, static_cast<const void*>(out_host)}) {
+      cudaPointerAttributes a;
+      if (cudaPointerGetAttributes(&a, q) != cudaSuccess || a.type != cudaMemoryTypeHost) {
+        cudaGetLastError();
+        return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be pinned host memory");
+      }
+    }
+    if (!aligned16(x_host) || !aligned16(out_host))
+      return fail(MOE_ERR_INVALID_ARG, "x_host and out_host must be 16-byte aligned");
+  }
+  const HostIO hio{x_host, out_host};
+  return run_impl(p, x_dev, T, chunk, workspace, workspace_bytes, out_dev, topk_id, topk_w, expert_offsets,
+                  row_token, compute, copy, &hio);
 }
 
 moe_status moe_prefill_combine(const float* y, const float* w, const int32_t* token_row, const float* s, int64_t n,
@@ -1042,6 +1139,8 @@ moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* 
 
 void moe_prefill_destroy(moe_plan_t p) {
   if (!p) return;
+  if (p->host_io) cudaStreamDestroy(p->host_io);
+  for (cudaEvent_t e : {p->ev_x_head, p->ev_x_rest}) if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : {p->ev_fork, p->ev_span, p->ev_join, p->ev_ready[0], p->ev_ready[1], p->ev_down, p->ev_comb,
                         p->ev_copy[0], p->ev_copy[1], p->ev_rel[0], p->ev_rel[1]})
     if (e) cudaEventDestroy(e);

@@ -142,6 +142,24 @@ moe_status moe_prefill_run(moe_plan_t plan, const void* x, int64_t T, int32_t ch
                            int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute, moe_stream_t copy);
 
 /*
+ * moe_prefill_run_host — moe_prefill_run for activations in host memory, with the copies overlapped.
+ *   x_host     pinned host bf16 [T][H] (cudaHostAlloc / cudaHostRegister), read.
+ *   out_host   pinned host bf16 [T][H], written.
+ *   x_dev, out_dev   device bf16 [T][H] staging buffers owned by the caller (16-byte aligned).
+ *   Other arguments as for moe_prefill_run.
+ * The X rows of each routing span are copied to x_dev on a stream of the plan in two parts, the span's first
+ * chunk and the rest: the first chunk's routing and expert GEMMs start once its rows have landed while the rest is
+ * in flight (routing of the rest waits for them). Each chunk's out rows are copied back as soon as its combine has
+ * written them, beside the next chunks' GEMMs. The results (out_host, and the optional device outputs) are those of
+ * moe_prefill_run on x_dev; every copy is ordered after the work enqueued on `compute` before the call, and all of
+ * them have finished when `compute` reaches the end of the run.
+ */
+moe_status moe_prefill_run_host(moe_plan_t plan, const void* x_host, int64_t T, int32_t chunk, void* workspace,
+                                size_t workspace_bytes, void* x_dev, void* out_dev, void* out_host, int32_t* topk_id,
+                                float* topk_w, int32_t* expert_offsets, int32_t* row_token, moe_stream_t compute,
+                                moe_stream_t copy);
+
+/*
  * moe_prefill_combine — the canonical combine alone (the same kernel run uses).
  *   y          device float [R][H]: per-row expert outputs.
  *   w          device float [n][k]: weights, slot order = ascending expert id.

@@ -246,3 +246,25 @@ def test_standalone_combine_matches_fp32_canonical_oracle(oracle_lib):
     torch.cuda.synchronize()
     want = oracle_lib.combine_f32_canonical(y.numpy(), w.numpy(), tr.numpy(), None)
     np.testing.assert_array_equal(out_bits(out.cpu()), want)
+
+
+@pytest.mark.parametrize("name,chunk,tokens", [("tiny", 16, None), ("e128_t3001", 1024, None),
+                                               ("e128_t3001", 1024, 17000), ("e512_t16022", 2048, None)])
+def test_run_from_host_buffers_equals_device_run(name, chunk, tokens):
+    """moe_prefill_run_host (X in, out back from pinned host memory, copies overlapped with the chunks) gives the
+    bytes of the device run, also over several routing spans (17,000 tokens); repeated calls reuse the staging
+    buffers."""
+    wl, inp = cpu_inputs(name, tokens=tokens)
+    wl = wl.with_(tokens=inp["x"].shape[0])
+    g = GpuLayer(inp, wl.top_k, max_chunk=chunk)
+    ref = g.run(chunk)["out"]
+    x_host = inp["x"].pin_memory()
+    x_dev = torch.empty_like(g.dev["x"])
+    out_dev = torch.empty_like(g.dev["x"])
+    for _ in range(2):
+        out_host = torch.full(x_host.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+        ids = torch.empty((wl.tokens, wl.top_k), dtype=torch.int32, device="cuda")
+        g.layer.run_host(x_host, chunk, x_dev, out_dev, out_host, topk_id=ids)
+        torch.cuda.current_stream().synchronize()
+        g.layer.raise_on_device_error()
+        np.testing.assert_array_equal(out_bits(out_host), out_bits(ref))
