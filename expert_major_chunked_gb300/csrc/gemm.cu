@@ -8,15 +8,18 @@
 // so every output element is computed with the same accumulation order whatever the tile's row position or the
 // number of members of its expert. That makes each row independent of the chunk size.
 //
-// Warp roles (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns the TMEM allocation and lane 0 issues the
-// UMMAs; warps 2..5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..+31) and store the outputs.
-// Two TMEM accumulators of 256 columns let the epilogue of one tile overlap the main loop of the next.
+// bf16 weights, grouped_gemm_kernel (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns the TMEM allocation
+// and lane 0 issues the UMMAs; warps 2..5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..+31) and
+// store the outputs. Two TMEM accumulators of 256 columns let the epilogue of one tile overlap the main loop of the
+// next.
 //
-// Block-scaled FP8 weights (MXFP8: E4M3 codes, one E8M0 power-of-two scale per 32 weights along K) take the variant
-// with eight more warps (448 threads). TMA lands a stage's E4M3 B tile in the upper half of the stage's B buffer
-// and its scales next to the epilogue staging; warps 6..9 (even stages) and 10..13 (odd stages) decode it to bf16
-// in place, in the same 128B-swizzled layout TMA writes, and release the stage to the UMMA issuer. A code times its scale is exactly a bf16 value, so
-// the tensor core sees exactly the decoded weights and the accumulation order is that of the bf16 path.
+// Block-scaled FP8 weights (MXFP8: E4M3 codes, one E8M0 power-of-two scale per 32 weights along K),
+// grouped_gemm_q_kernel (480 threads): the weight codes stream through their own ring of 5 stages, which carries
+// twice the weights per byte of shared memory that a bf16 stage does, and the activation rows through a ring of 3.
+// Two groups of four warps take alternate steps: each decodes a stage's codes to bf16 into its own buffer, in the
+// 128B-swizzled layout the UMMA descriptor reads (the layout TMA writes for bf16), and hands it to the UMMA issuer.
+// A code times its scale is exactly a bf16 value, so the tensor core sees exactly the decoded weights and the
+// accumulation order is that of the bf16 path. Warp 14 issues the activation loads.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -61,13 +64,12 @@ __device__ __forceinline__ int total_tiles(const GemmParams& p) {
   return ((p.dense_m + kBlockM - 1) / kBlockM) * p.dense_n_tiles;
 }
 
-// First tile of this launch and the end of its range: the whole list, or [*range_lo, *range_hi) of it.
+// First tile of this launch and the end of its range: the whole list, or the part [*range_lo, *range_hi) of it
+// (either bound may be absent).
 __device__ __forceinline__ int2 tile_range(const GemmParams& p) {
   int lo = 0, hi = total_tiles(p);
-  if (p.range_lo != nullptr) {
-    lo = max(0, *reinterpret_cast<const volatile int32_t*>(p.range_lo));
-    hi = min(hi, *reinterpret_cast<const volatile int32_t*>(p.range_hi));
-  }
+  if (p.range_lo != nullptr) lo = max(0, *reinterpret_cast<const volatile int32_t*>(p.range_lo));
+  if (p.range_hi != nullptr) hi = min(hi, *reinterpret_cast<const volatile int32_t*>(p.range_hi));
   return make_int2(lo, hi);
 }
 
@@ -87,6 +89,103 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// First B row of a tile's (first) box: the group's (or ring slot's) row base plus the N tile's offset.
+template <int EPI>
+__device__ __forceinline__ int tile_b_row(const GemmClass& C, int slot, int n_idx) {
+  return slot * C.b_group_rows + n_idx * (EPI == kEpiSwiGLU ? C.b_box_rows : C.n_tile);
+}
+
+// Reads one tile's accumulator (columns [0, n_tile) at tbase) back from TMEM and stores the tile's outputs. Each of
+// the four epilogue warps owns a 32-row slab. A 32-column block of the accumulator arrives one row per lane; it is
+// staged in shared memory (odd row stride: no bank conflicts) and written back row-contiguously, so every store
+// instruction covers whole 128-byte lines instead of 32 different rows.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const GemmClass& C, const TileInfo& ti, uint32_t tbase,
+                                              uint32_t* stage, int lane, int q) {
+  const int slab_rows = ti.rows - q * 32;
+  const int64_t slab_row0 = static_cast<int64_t>(ti.out_row0) + q * 32;
+  if (EPI == kEpiSwiGLU) {
+    const int half = C.b_box_rows;
+    const int64_t ldw = C.out_ld / 2;  // row stride in 32-bit words (two bf16 each)
+    uint32_t* outw = reinterpret_cast<uint32_t*>(C.out) + (static_cast<int64_t>(ti.n_idx) * half) / 2;
+    for (int c = 0; c < half; c += 32) {
+      uint32_t g[32], u[32];
+      ptx::tmem_ld32(tbase + c, g);
+      ptx::tmem_ld32(tbase + half + c, u);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        stage[lane * 17 + i] = pack_bf16(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                         swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+      __syncwarp();
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int r = m * 8 + (lane >> 2), w0 = (lane & 3) * 4;
+        if (r < slab_rows) {
+          const uint32_t* sr = stage + r * 17 + w0;
+          *reinterpret_cast<uint4*>(outw + (slab_row0 + r) * ldw + c / 2 + w0) = make_uint4(sr[0], sr[1], sr[2], sr[3]);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    const int col0 = ti.n_idx * C.n_tile;
+    float* outb = static_cast<float*>(C.out) + col0;
+    const bool vec = (C.out_ld % 4) == 0;
+    for (int c = 0; c < C.n_tile; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld32(tbase + c, v);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
+      __syncwarp();
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int r = m * 4 + (lane >> 3), cc = (lane & 7) * 4;
+        if (r < slab_rows) {
+          const uint32_t* sr = stage + r * 33 + cc;
+          float* dst = outb + (slab_row0 + r) * C.out_ld + c + cc;
+          const int gc = col0 + c + cc;
+          if (vec && gc + 4 <= C.out_cols) {
+            *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(sr[0]), __uint_as_float(sr[1]),
+                                                          __uint_as_float(sr[2]), __uint_as_float(sr[3]));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              if (gc + jj < C.out_cols) dst[jj] = __uint_as_float(sr[jj]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// The epilogue role (warps 2..5) of both kernels: waits for each tile's accumulator, stores it, frees it.
+template <int EPI>
+__device__ __forceinline__ void epilogue_role(const GemmParams& p, int tfirst, int ntiles, uint32_t tmem_base,
+                                              uint32_t tfull0, uint32_t tempty0, uint32_t* stage, int warp, int lane,
+                                              volatile int* abort_flag) {
+  const int q = warp & 3;
+  int local = 0;
+  for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
+    const TileInfo ti = decode_tile(p, t);
+    const int acc = local & 1;
+    const uint32_t use = static_cast<uint32_t>(local >> 1);
+    bool ok = ptx::wait_bounded(tfull0 + 8u * acc, use & 1u, p.timeout_ns, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+      if (lane == 0) raise_error(p, abort_flag, kSiteEpilogueFull);
+      break;
+    }
+    ptx::tc_fence_after();
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kMaxN);
+    epilogue_tile<EPI>(p.cls[ti.cls], ti, tbase, stage, lane, q);
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(tempty0 + 8u * acc);
+  }
+}
+
 // Two E4M3 codes times the scale f (a power of two) as two bf16 values; every step is exact (E4M3 -> f16 -> f32,
 // times a power of two, -> bf16 of a value bf16 holds).
 __device__ __forceinline__ uint32_t decode_pair(uint32_t codes16, float f) {
@@ -95,24 +194,19 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t codes16, float f) {
   return pack_bf16(__fmul_rn(v.x, f), __fmul_rn(v.y, f));
 }
 
-// Decodes one stage's MXFP8 B tile in place: `rows` rows of 64 E4M3 codes, row-major in the upper half of the
-// stage's B buffer (as TMA landed them), scales sc[2][rows] (K blocks 0..31 and 32..63 of the stage). Writes bf16
-// rows of 128 B in the 128B-swizzled K-major layout (8-row atoms of 1024 B, 16-byte chunk c of row r at chunk
-// c ^ (r % 8)). Bf16 rows 128..255 overwrite the codes, so the group's 128 threads read their codes first and
-// meet at the group's named barrier before any write. `skip` (a failed wait) leaves the data alone but keeps the
-// barrier.
-__device__ __forceinline__ void decode_stage(uint8_t* bstage, const uint8_t* sc, int rows, int ct, bool skip,
-                                             uint32_t bar_id) {
-  const uint8_t* codes = bstage + kStageBBytes / 2;
+// Decodes one stage of MXFP8 weights: `rows` rows of 64 E4M3 codes (row-major, as TMA landed them) with scales
+// sc[2][rows] (K blocks 0..31 and 32..63 of the stage), by the 128 threads of a decoder group (ct = 0..127), into
+// bf16 rows of 128 B in the 128B-swizzled K-major layout (8-row atoms of 1024 B, 16-byte chunk c of row r at chunk
+// c ^ (r % 8)).
+__device__ __forceinline__ void decode_stage(const uint8_t* codes, const uint8_t* sc, uint8_t* dst, int rows,
+                                             int ct) {
   const int items = rows * 4;  // 16-code chunks, chunk i = row i / 4, K elements 16 * (i % 4) ..
   uint4 v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int i = ct + 128 * j;
-    if (!skip && i < items) v[j] = *reinterpret_cast<const uint4*>(codes + i * 16);
+    if (i < items) v[j] = *reinterpret_cast<const uint4*>(codes + i * 16);
   }
-  ptx::named_barrier(bar_id, 128);
-  if (skip) return;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int i = ct + 128 * j;
@@ -126,16 +220,16 @@ __device__ __forceinline__ void decode_stage(uint8_t* bstage, const uint8_t* sc,
         o[2 * q] = decode_pair(w[q], f);
         o[2 * q + 1] = decode_pair(w[q] >> 16, f);
       }
-      uint8_t* rowp = bstage + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
       *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
 }
 
-template <int EPI, bool WQ>
-__global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+// ============================================================================================ bf16 weights
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -144,12 +238,9 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
   const uint32_t sB = base + kStages * kStageABytes;
   const uint32_t bars = sB + kStages * kStageBBytes;
   uint8_t* bars_ptr = base_ptr + kStages * (kStageABytes + kStageBBytes);
-  // barrier slots: full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain; MXFP8: decoded[kStages]
+  // barrier slots: full[kStages], empty[kStages], tmem_full[2], tmem_empty[2], drain
   const uint32_t full0 = bars, empty0 = bars + 8u * kStages, tfull0 = bars + 16u * kStages;
   const uint32_t tempty0 = tfull0 + 16u, drain_bar = tempty0 + 16u;
-  const uint32_t dec0 = bars + 128u;
-  const uint32_t sc0 = bars + 256u + kEpiStageBytes;  // MXFP8 scales, kStageScaleBytes per stage
-  uint8_t* sc0_ptr = bars_ptr + 256 + kEpiStageBytes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + 16 * kStages + 40);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + 16 * kStages + 44);
 
@@ -166,8 +257,6 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
       ptx::mbar_init(tempty0 + 8u * a, 4 * 32);
     }
     ptx::mbar_init(drain_bar, 1);
-    if (WQ)
-      for (int s = 0; s < kStages; ++s) ptx::mbar_init(dec0 + 8u * s, 4);  // one arrival per decoder warp
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -215,17 +304,10 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
         const void* tB = &p.tmB[ti.cls];
         const int nA = (ti.rows + kABoxRows - 1) / kABoxRows;
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
-        const bool q = WQ && C.b_scale != nullptr;  // E4M3 B tile (64 B rows) plus 2 scale bytes per row
-        const uint32_t b_row_bytes = q ? 64u + 2u : 128u;
-        const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * b_row_bytes;
-        int b_row0, b_row1 = 0;
+        const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * 128u;
         const int slot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
-        if (EPI == kEpiSwiGLU) {
-          b_row0 = slot * C.b_group_rows + ti.n_idx * C.b_box_rows;
-          b_row1 = b_row0 + C.b_up_offset;
-        } else {
-          b_row0 = slot * C.b_group_rows + ti.n_idx * C.n_tile;
-        }
+        const int b_row0 = tile_b_row<EPI>(C, slot, ti.n_idx);
+        const int b_row1 = b_row0 + C.b_up_offset;
         for (int kb = 0; kb < C.kblocks; ++kb) {
           if (!ptx::wait_bounded(empty0 + 8u * stage, phase ^ 1u, tmo, abort_flag)) {
             raise_error(p, abort_flag, kSiteProducerEmpty);
@@ -239,28 +321,7 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
           const int kc = kb * kBlockK;
           for (int j = 0; j < nA; ++j)
             ptx::tma_load_2d(a_dst + j * (kABoxRows * 128), tA, kc, ti.a_row0 + j * kABoxRows, fb);
-          if (q) {
-            // codes into the upper half of the B buffer (the converters decode them in place), then the scales
-            // of the stage's two 32-wide K blocks: plane kb32 of the group, the box's rows
-            const uint32_t c_dst = b_dst + kStageBBytes / 2;
-            const uint32_t s_dst = sc0 + stage * kStageScaleBytes;
-            const int64_t planes = 2 * C.kblocks;
-            if (C.b_stream && ti.stream) {
-              ptx::tma_load_2d_hint(c_dst, tB, kc, b_row0, fb, pol_stream);
-              if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb, pol_stream);
-            } else {
-              ptx::tma_load_2d(c_dst, tB, kc, b_row0, fb);
-              if (EPI == kEpiSwiGLU) ptx::tma_load_2d(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb);
-            }
-            for (int h = 0; h < 2; ++h) {
-              const uint8_t* plane = C.b_scale + (static_cast<int64_t>(ti.group) * planes + 2 * kb + h) *
-                                                     static_cast<int64_t>(C.b_group_rows);
-              const int r0 = b_row0 - slot * C.b_group_rows;
-              ptx::bulk_load(s_dst + h * C.n_tile, plane + r0, C.b_box_rows, fb);
-              if (EPI == kEpiSwiGLU)
-                ptx::bulk_load(s_dst + h * C.n_tile + C.b_box_rows, plane + r0 + C.b_up_offset, C.b_box_rows, fb);
-            }
-          } else if (C.b_stream && ti.stream) {
+          if (C.b_stream && ti.stream) {
             ptx::tma_load_2d_hint(b_dst, tB, kc, b_row0, fb, pol_stream);
             if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb, pol_stream);
           } else {
@@ -306,7 +367,7 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxN);
         const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, static_cast<uint32_t>(C.n_tile));
         for (int kb = 0; kb < C.kblocks; ++kb) {
-          if (!ptx::wait_bounded((WQ ? dec0 : full0) + 8u * stage, phase, tmo, abort_flag)) {
+          if (!ptx::wait_bounded(full0 + 8u * stage, phase, tmo, abort_flag)) {
             raise_error(p, abort_flag, kSiteMmaFull);
             failed = true;
             break;
@@ -337,124 +398,281 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
       }
     }
     __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    uint32_t* stage = reinterpret_cast<uint32_t*>(bars_ptr + 256) + (warp - 2) * (32 * 33);
+    epilogue_role<EPI>(p, tfirst, ntiles, tmem_base, tfull0, tempty0, stage, warp, lane, abort_flag);
+  }
+
+  // ------------------------------------------------------------ teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, 2 * kMaxN);
+  }
+}
+
+// ============================================================================================ MXFP8 weights
+// Rings: A (activation rows, kQStagesA x 16 KB), C (E4M3 codes, kQStagesC x 16 KB, with 2 x rows scale bytes
+// each), D (decoded bf16 B tiles, one 32 KB buffer per decoder group). Step i of the CTA's (tile, K block) sequence
+// uses A slot i % kQStagesA, C slot i % kQStagesC and D buffer i % 2, decoded by group i % 2. Only tiles whose
+// class has scales run here (the routed experts); the bf16 shared expert takes grouped_gemm_kernel.
+template <int EPI>
+__global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t sA = base;
+  const uint32_t sD = sA + kQStagesA * kStageABytes;
+  const uint32_t sC = sD + kQStagesD * kStageBBytes;
+  const uint32_t sS = sC + kQStagesC * kQStageCodeBytes;
+  const uint32_t bars = sS + kQStagesC * kQStageScaleBytes;
+  uint8_t* sD_ptr = base_ptr + (sD - base);
+  const uint8_t* sC_ptr = base_ptr + (sC - base);
+  const uint8_t* sS_ptr = base_ptr + (sS - base);
+  uint8_t* bars_ptr = base_ptr + (bars - base);
+  const uint32_t a_full0 = bars, a_empty0 = a_full0 + 8u * kQStagesA;
+  const uint32_t c_full0 = a_empty0 + 8u * kQStagesA, c_empty0 = c_full0 + 8u * kQStagesC;
+  const uint32_t d_full0 = c_empty0 + 8u * kQStagesC, d_empty0 = d_full0 + 8u * kQStagesD;
+  const uint32_t tfull0 = d_empty0 + 8u * kQStagesD, tempty0 = tfull0 + 16u, drain_bar = tempty0 + 16u;
+  static_assert(8 * (2 * kQStagesA + 2 * kQStagesC + 2 * kQStagesD + 5) + 8 <= 256, "barrier region");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars_ptr + (drain_bar + 8u - bars));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars_ptr + (drain_bar + 12u - bars));
+
+  const int warp = static_cast<int>(threadIdx.x) / 32;
+  const int lane = static_cast<int>(threadIdx.x) % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStagesA; ++s) {
+      ptx::mbar_init(a_full0 + 8u * s, 1);
+      ptx::mbar_init(a_empty0 + 8u * s, 1);
+    }
+    for (int s = 0; s < kQStagesC; ++s) {
+      ptx::mbar_init(c_full0 + 8u * s, 1);
+      ptx::mbar_init(c_empty0 + 8u * s, 4);  // one arrival per warp of the decoder group
+    }
+    for (int s = 0; s < kQStagesD; ++s) {
+      ptx::mbar_init(d_full0 + 8u * s, 4);
+      ptx::mbar_init(d_empty0 + 8u * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull0 + 8u * a, 1);
+      ptx::mbar_init(tempty0 + 8u * a, 4 * 32);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&p.tmA[0]);
+    ptx::tma_prefetch_desc(&p.tmB[0]);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 2 * kMaxN);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  const int2 trange = tile_range(p);
+  const int tfirst = trange.x + static_cast<int>(blockIdx.x);
+  const int ntiles = trange.y;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA: E4M3 codes and their scales
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0, issued = 0;
+      bool failed = false;
+      const uint64_t pol_stream = ptx::make_policy_evict_first();
+      for (int t = tfirst; !failed && t < ntiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t);
+        const GemmClass& C = p.cls[ti.cls];
+        const void* tB = &p.tmB[ti.cls];
+        const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
+        const uint32_t bytes = b_loads * C.b_box_rows * (64u + 2u);
+        const int gslot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
+        const int b_row0 = tile_b_row<EPI>(C, gslot, ti.n_idx);
+        const int b_row1 = b_row0 + C.b_up_offset;
+        const int r0 = b_row0 - gslot * C.b_group_rows;  // first row inside the group
+        const int64_t planes = 2 * C.kblocks;             // 32-wide K blocks per row
+        const bool hint = C.b_stream && ti.stream;
+        for (int kb = 0; kb < C.kblocks; ++kb) {
+          if (!ptx::wait_bounded(c_empty0 + 8u * slot, phase ^ 1u, tmo, abort_flag)) {
+            raise_error(p, abort_flag, kSiteProducerEmpty);
+            failed = true;
+            break;
+          }
+          const uint32_t fb = c_full0 + 8u * slot;
+          ptx::mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t c_dst = sC + slot * kQStageCodeBytes;
+          const uint32_t s_dst = sS + slot * kQStageScaleBytes;
+          const int kc = kb * kBlockK;
+          if (hint) {
+            ptx::tma_load_2d_hint(c_dst, tB, kc, b_row0, fb, pol_stream);
+            if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb, pol_stream);
+          } else {
+            ptx::tma_load_2d(c_dst, tB, kc, b_row0, fb);
+            if (EPI == kEpiSwiGLU) ptx::tma_load_2d(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb);
+          }
+          for (int h = 0; h < 2; ++h) {
+            const uint8_t* plane = C.b_scale + (static_cast<int64_t>(ti.group) * planes + 2 * kb + h) *
+                                                   static_cast<int64_t>(C.b_group_rows);
+            ptx::bulk_load(s_dst + h * C.n_tile, plane + r0, C.b_box_rows, fb);
+            if (EPI == kEpiSwiGLU)
+              ptx::bulk_load(s_dst + h * C.n_tile + C.b_box_rows, plane + r0 + C.b_up_offset, C.b_box_rows, fb);
+          }
+          ++issued;
+          if (++slot == kQStagesC) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (failed) {
+        int no_abort = 0;
+        for (int s = 0; s < kQStagesC; ++s) {
+          const uint32_t cnt = issued / kQStagesC + (static_cast<uint32_t>(s) < issued % kQStagesC ? 1u : 0u);
+          if (cnt == 0) continue;
+          if (!ptx::wait_bounded(c_full0 + 8u * s, (cnt - 1u) & 1u, tmo, &no_abort))
+            atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, kSiteDrain, static_cast<int>(blockIdx.x)));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kGemmThreadsQ / 32 - 1) {
+    // ------------------------------------------------------------ TMA: activation rows
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0, issued = 0;
+      bool failed = false;
+      for (int t = tfirst; !failed && t < ntiles; t += gridDim.x) {
+        const TileInfo ti = decode_tile(p, t);
+        const GemmClass& C = p.cls[ti.cls];
+        const void* tA = &p.tmA[ti.cls];
+        const int nA = (ti.rows + kABoxRows - 1) / kABoxRows;
+        const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128);
+        for (int kb = 0; kb < C.kblocks; ++kb) {
+          if (!ptx::wait_bounded(a_empty0 + 8u * slot, phase ^ 1u, tmo, abort_flag)) {
+            raise_error(p, abort_flag, kSiteProducerEmpty);
+            failed = true;
+            break;
+          }
+          const uint32_t fb = a_full0 + 8u * slot;
+          ptx::mbar_arrive_expect_tx(fb, bytes);
+          const uint32_t a_dst = sA + slot * kStageABytes;
+          for (int j = 0; j < nA; ++j)
+            ptx::tma_load_2d(a_dst + j * (kABoxRows * 128), tA, kb * kBlockK, ti.a_row0 + j * kABoxRows, fb);
+          ++issued;
+          if (++slot == kQStagesA) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (failed) {
+        int no_abort = 0;
+        for (int s = 0; s < kQStagesA; ++s) {
+          const uint32_t cnt = issued / kQStagesA + (static_cast<uint32_t>(s) < issued % kQStagesA ? 1u : 0u);
+          if (cnt == 0) continue;
+          if (!ptx::wait_bounded(a_full0 + 8u * s, (cnt - 1u) & 1u, tmo, &no_abort))
+            atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, kSiteDrain, static_cast<int>(blockIdx.x)));
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      int local = 0;
+      uint32_t i = 0;
+      bool failed = false, issued_any = false;
+      for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
+        const TileInfo ti = decode_tile(p, t);
+        const GemmClass& C = p.cls[ti.cls];
+        const int acc = local & 1;
+        const uint32_t use = static_cast<uint32_t>(local >> 1);
+        if (!ptx::wait_bounded(tempty0 + 8u * acc, (use & 1u) ^ 1u, tmo, abort_flag)) {
+          raise_error(p, abort_flag, kSiteMmaTmemEmpty);
+          failed = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxN);
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBlockM, static_cast<uint32_t>(C.n_tile));
+        for (int kb = 0; kb < C.kblocks; ++kb, ++i) {
+          const uint32_t as = i % kQStagesA, aph = (i / kQStagesA) & 1u;
+          const uint32_t ds = i % kQStagesD, dph = (i / kQStagesD) & 1u;
+          if (!ptx::wait_bounded(a_full0 + 8u * as, aph, tmo, abort_flag) ||
+              !ptx::wait_bounded(d_full0 + 8u * ds, dph, tmo, abort_flag)) {
+            raise_error(p, abort_flag, kSiteMmaFull);
+            failed = true;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t a_desc = ptx::sw128_kmajor_desc(sA + as * kStageABytes);
+          const uint64_t b_desc = ptx::sw128_kmajor_desc(sD + ds * kStageBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBlockK / 16; ++kk)
+            ptx::umma_bf16(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          ptx::umma_commit(a_empty0 + 8u * as);  // both buffers are free once these UMMAs have read them
+          ptx::umma_commit(d_empty0 + 8u * ds);
+          issued_any = true;
+        }
+        if (failed) break;
+        ptx::umma_commit(tfull0 + 8u * acc);
+      }
+      if (failed && issued_any) {
+        int no_abort = 0;
+        ptx::umma_commit(drain_bar);
+        if (!ptx::wait_bounded(drain_bar, 0u, tmo, &no_abort))
+          atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, kSiteDrain, static_cast<int>(blockIdx.x)));
+      }
+    }
+    __syncwarp();
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;
     uint32_t* stage = reinterpret_cast<uint32_t*>(bars_ptr + 256) + (warp - 2) * (32 * 33);
-    int local = 0;
-    for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
-      const TileInfo ti = decode_tile(p, t);
-      const GemmClass& C = p.cls[ti.cls];
-      const int acc = local & 1;
-      const uint32_t use = static_cast<uint32_t>(local >> 1);
-      bool ok = ptx::wait_bounded(tfull0 + 8u * acc, use & 1u, tmo, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) raise_error(p, abort_flag, kSiteEpilogueFull);
-        break;
-      }
-      ptx::tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kMaxN);
-      // Each warp owns a 32-row slab of the tile. A 32-column block of the accumulator arrives one row per lane;
-      // it is staged in shared memory (odd row stride: no bank conflicts) and written back row-contiguously, so
-      // every store instruction covers whole 128-byte lines instead of 32 different rows.
-      const int slab_rows = ti.rows - q * 32;
-      const int64_t slab_row0 = static_cast<int64_t>(ti.out_row0) + q * 32;
-      if (EPI == kEpiSwiGLU) {
-        const int half = C.b_box_rows;
-        const int64_t ldw = C.out_ld / 2;  // row stride in 32-bit words (two bf16 each)
-        uint32_t* outw = reinterpret_cast<uint32_t*>(C.out) + (static_cast<int64_t>(ti.n_idx) * half) / 2;
-        for (int c = 0; c < half; c += 32) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld32(tbase + c, g);
-          ptx::tmem_ld32(tbase + half + c, u);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            stage[lane * 17 + i] = pack_bf16(swiglu(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                                             swiglu(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-          __syncwarp();
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int r = m * 8 + (lane >> 2), w0 = (lane & 3) * 4;
-            if (r < slab_rows) {
-              const uint32_t* sr = stage + r * 17 + w0;
-              *reinterpret_cast<uint4*>(outw + (slab_row0 + r) * ldw + c / 2 + w0) = make_uint4(sr[0], sr[1], sr[2], sr[3]);
-            }
-          }
-          __syncwarp();
-        }
-      } else {
-        const int col0 = ti.n_idx * C.n_tile;
-        float* outb = static_cast<float*>(C.out) + col0;
-        const bool vec = (C.out_ld % 4) == 0;
-        for (int c = 0; c < C.n_tile; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tbase + c, v);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
-          __syncwarp();
-#pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            const int r = m * 4 + (lane >> 3), cc = (lane & 7) * 4;
-            if (r < slab_rows) {
-              const uint32_t* sr = stage + r * 33 + cc;
-              float* dst = outb + (slab_row0 + r) * C.out_ld + c + cc;
-              const int gc = col0 + c + cc;
-              if (vec && gc + 4 <= C.out_cols) {
-                *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(sr[0]), __uint_as_float(sr[1]),
-                                                              __uint_as_float(sr[2]), __uint_as_float(sr[3]));
-              } else {
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-                  if (gc + jj < C.out_cols) dst[jj] = __uint_as_float(sr[jj]);
-              }
-            }
-          }
-          __syncwarp();
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(tempty0 + 8u * acc);
-    }
-  } else if (WQ) {
-    // ------------------------------------------------------------ MXFP8 decoders (warps 6..13)
-    // Group g (128 threads) takes the stages s with s % 2 == g. Every thread of a group walks the same stages and
-    // meets its group's named barrier at each E4M3 stage, also after a failed wait (then it decodes nothing), so
-    // no thread can be left waiting at the barrier.
-    const int dt = static_cast<int>(threadIdx.x) - kGemmThreads;
+    epilogue_role<EPI>(p, tfirst, ntiles, tmem_base, tfull0, tempty0, stage, warp, lane, abort_flag);
+  } else {
+    // ------------------------------------------------------------ decoders (warps 6..13: groups 0 and 1)
+    const int dt = static_cast<int>(threadIdx.x) - 6 * 32;
     const int group = dt / 128, ct = dt % 128;
-    int stage = 0;
-    uint32_t phase = 0;
+    uint32_t i = 0;
     bool failed = false;
     for (int t = tfirst; t < ntiles; t += gridDim.x) {
       const TileInfo ti = decode_tile(p, t);
       const GemmClass& C = p.cls[ti.cls];
-      const bool q = C.b_scale != nullptr;
-      for (int kb = 0; kb < C.kblocks; ++kb) {
-        if ((stage % kDecodeGroups) == group) {
-          // one lane per warp polls the stage's barrier; the warp then shares the outcome
-          bool ok = true;
-          if (lane == 0 && !failed) ok = ptx::wait_bounded(full0 + 8u * stage, phase, tmo, abort_flag);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!failed && !ok) {
-            if (lane == 0) raise_error(p, abort_flag, kSiteDecodeFull);
-            failed = true;
-          }
-          if (q)
-            decode_stage(base_ptr + kStages * kStageABytes + stage * kStageBBytes,
-                         sc0_ptr + stage * kStageScaleBytes, C.n_tile, ct, failed, 1u + static_cast<uint32_t>(group));
-          // each lane's writes to the async proxy, then one arrival per warp
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(dec0 + 8u * stage);
+      for (int kb = 0; kb < C.kblocks; ++kb, ++i) {
+        if (static_cast<int>(i % kQStagesD) != group) continue;
+        const uint32_t cs = i % kQStagesC, cph = (i / kQStagesC) & 1u;
+        const uint32_t dph = (i / kQStagesD) & 1u;
+        // one lane per warp waits for the codes and for the group's buffer; the warp shares the outcome
+        int ok = 1;
+        if (lane == 0 && !failed)
+          ok = (ptx::wait_bounded(c_full0 + 8u * cs, cph, tmo, abort_flag) &&
+                ptx::wait_bounded(d_empty0 + 8u * group, dph ^ 1u, tmo, abort_flag)) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok && !failed) {
+          if (lane == 0) raise_error(p, abort_flag, kSiteDecodeFull);
+          failed = true;
         }
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (failed) break;
+        decode_stage(sC_ptr + cs * kQStageCodeBytes, sS_ptr + cs * kQStageScaleBytes,
+                     sD_ptr + group * kStageBBytes, C.n_tile, ct);
+        // the decoded tile to the async proxy; the codes have been consumed
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(c_empty0 + 8u * cs);
+          ptx::mbar_arrive(d_full0 + 8u * group);
         }
       }
+      if (failed) break;
     }
   }
 
@@ -471,10 +689,10 @@ __global__ void __launch_bounds__(WQ ? kGemmThreadsQ : kGemmThreads, 1)
 
 cudaError_t prepare_gemm_kernels() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32, false>, attr, kGemmSmemBytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU, false>, attr, kGemmSmemBytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32, true>, attr, kGemmSmemBytesQ);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU, true>, attr, kGemmSmemBytesQ);
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32>, attr, kGemmSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU>, attr, kGemmSmemBytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiF32>, attr, kGemmSmemBytesQ);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiSwiGLU>, attr, kGemmSmemBytesQ);
   return e;
 }
 
@@ -482,13 +700,13 @@ cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cud
   if (grid <= 0) return cudaSuccess;
   if (mxfp8) {
     if (epilogue == kEpiSwiGLU)
-      grouped_gemm_kernel<kEpiSwiGLU, true><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+      grouped_gemm_q_kernel<kEpiSwiGLU><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
     else
-      grouped_gemm_kernel<kEpiF32, true><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+      grouped_gemm_q_kernel<kEpiF32><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
   } else if (epilogue == kEpiSwiGLU) {
-    grouped_gemm_kernel<kEpiSwiGLU, false><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+    grouped_gemm_kernel<kEpiSwiGLU><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
   } else {
-    grouped_gemm_kernel<kEpiF32, false><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
+    grouped_gemm_kernel<kEpiF32><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
   }
   return cudaGetLastError();
 }

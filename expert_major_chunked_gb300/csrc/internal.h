@@ -52,14 +52,17 @@ constexpr int kStageABytes = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBBytes = kMaxN * kBlockK * 2;     // 32 KB
 constexpr int kEpiStageBytes = 4 * 32 * 33 * 4;            // epilogue staging: a 32 x 33-word block per warp
 constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + 256 + kEpiStageBytes;
-// Block-scaled FP8 weights (MXFP8): 8 more warps, in two groups of 4 taking alternate stages, convert each
-// stage's E4M3 B tile (landed by TMA in the upper half of the stage's B buffer) to bf16 in place; the E8M0 scales
-// of a stage (2 K blocks x up to 256 rows) sit after the epilogue staging.
-constexpr int kDecodeGroups = 2;
-constexpr int kGemmThreadsQ = kGemmThreads + kDecodeGroups * 128;
-static_assert(kStages % kDecodeGroups == 0, "decoder groups take stages by parity");
-constexpr int kStageScaleBytes = 2 * kMaxN;
-constexpr int kGemmSmemBytesQ = kGemmSmemBytes + kStages * kStageScaleBytes;
+// Block-scaled FP8 weights (MXFP8), grouped_gemm_q_kernel: rings of activation rows (A), E4M3 codes with their
+// E8M0 scales (C) and decoded bf16 B tiles (D, one per decoder group). Warps: 0 codes TMA, 1 UMMA, 2..5 epilogue,
+// 6..13 two decoder groups of 4, 14 activation TMA.
+constexpr int kQStagesA = 3;
+constexpr int kQStagesC = 5;
+constexpr int kQStagesD = 2;
+constexpr int kQStageCodeBytes = kMaxN * kBlockK;  // 16 KB: up to 256 rows x 64 codes
+constexpr int kQStageScaleBytes = 2 * kMaxN;       // two 32-wide K blocks x up to 256 rows
+constexpr int kGemmThreadsQ = 15 * 32;
+constexpr int kGemmSmemBytesQ = 1024 /*align slack*/ + kQStagesA * kStageABytes + kQStagesD * kStageBBytes +
+                                kQStagesC * (kQStageCodeBytes + kQStageScaleBytes) + 256 + kEpiStageBytes;
 
 enum Epilogue : int { kEpiF32 = 0, kEpiSwiGLU = 1 };
 

@@ -760,6 +760,33 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
 
     // The grouped GEMMs of experts [e0, e1) of a chunk (all experts when the weights are resident); the range
     // of the last experts also covers the shared expert's tiles, which follow the routed ones in the lists.
+    // One grouped GEMM over the tiles of experts [e0, e1) (and the shared expert's, which follow the routed ones,
+    // when the range reaches the last expert). MXFP8 plans run the routed tiles in the decoding kernel and the
+    // bf16 shared expert in the plain one, as a second launch on the same stream.
+    auto grouped = [&](GemmParams prm, int epi, int cap, const int32_t* tb, const int32_t* n_tiles, int e0, int e1,
+                       bool windowed, int kind, const char* what) -> moe_status {
+      const bool q = p->w_gu_scale != nullptr;
+      if (!q) {
+        if (windowed) {
+          prm.range_lo = tb + e0;
+          prm.range_hi = (e1 >= s.E) ? n_tiles : tb + e1;
+        }
+        LaunchScope ls(p, kind, st);
+        return cuda_status(launch_grouped_gemm(prm, epi, std::min(p->num_sms, cap), st), what);
+      }
+      const bool shared = s.Is > 0 && e1 >= s.E;
+      LaunchScope ls(p, kind, st, shared ? 2 : 1);
+      prm.range_lo = windowed ? tb + e0 : nullptr;
+      prm.range_hi = tb + std::min(e1, s.E);
+      moe_status r2 = cuda_status(launch_grouped_gemm(prm, epi, std::min(p->num_sms, cap), st, true), what);
+      if (r2 == MOE_OK && shared) {
+        prm.range_lo = tb + s.E;
+        prm.range_hi = n_tiles;
+        r2 = cuda_status(launch_grouped_gemm(prm, epi, p->num_sms, st, false), what);
+      }
+      return r2;
+    };
+
     auto gemms = [&](int64_t cidx, int e0, int e1) -> moe_status {
       const int par = static_cast<int>(cidx & 1);
       const int32_t* num_tiles = reinterpret_cast<const int32_t*>(ws + L.num_tiles[par]);
@@ -809,18 +836,9 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       }
       gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu[par]);
       gu.num_tiles = num_tiles;
-      if (windowed) {
-        gu.range_lo = tbase + e0;
-        gu.range_hi = (e1 >= s.E) ? num_tiles : tbase + e1;
-      }
       gu.err = &hdr->err;
       gu.timeout_ns = p->timeout_ns;
-      {
-        LaunchScope ls(p, MOE_KERNEL_GATE_UP, st);
-        r2 = cuda_status(launch_grouped_gemm(gu, kEpiSwiGLU, std::min(p->num_sms, L.cap_gu), st,
-                                             p->w_gu_scale != nullptr),
-                         "gate/up launch");
-      }
+      r2 = grouped(gu, kEpiSwiGLU, L.cap_gu, tbase, num_tiles, e0, e1, windowed, MOE_KERNEL_GATE_UP, "gate/up launch");
       if (r2 != MOE_OK) return r2;
 
       // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s), once the previous chunk's combine
@@ -862,18 +880,10 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       }
       dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down[par]);
       dn.num_tiles = num_tiles + 1;
-      if (windowed) {
-        dn.range_lo = tbase + (s.E + 1) + e0;
-        dn.range_hi = (e1 >= s.E) ? num_tiles + 1 : tbase + (s.E + 1) + e1;
-      }
       dn.err = &hdr->err;
       dn.timeout_ns = p->timeout_ns;
-      {
-        LaunchScope ls(p, MOE_KERNEL_DOWN, st);
-        r2 = cuda_status(launch_grouped_gemm(dn, kEpiF32, std::min(p->num_sms, L.cap_down), st,
-                                             p->w_down_scale != nullptr),
-                         "down launch");
-      }
+      r2 = grouped(dn, kEpiF32, L.cap_down, tbase + (s.E + 1), num_tiles + 1, e0, e1, windowed, MOE_KERNEL_DOWN,
+                   "down launch");
       if (r2 != MOE_OK) return r2;
       if (windowed) {
         r2 = cuda_status(cudaEventRecord(p->ev_rel[hb], st), "slot release event");
