@@ -170,3 +170,53 @@ def mxfp8_weights(inp: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
     gu_q, gu_s = quantize_mxfp8(inp["w_gu"])
     dn_q, dn_s = quantize_mxfp8(inp["w_down"])
     return {"w_gu_q": gu_q, "w_gu_s": gu_s, "w_down_q": dn_q, "w_down_s": dn_s}
+
+
+_E2M1_GRID = torch.tensor([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=torch.float32)
+
+
+def quantize_nvfp4(w: torch.Tensor):
+    """Block-scaled FP4 (NVFP4) form of expert weights [E][R][K], K a multiple of 16: E2M1 codes [E][R][K/2] (uint8,
+    element 2j in the low nibble of byte j) and E4M3 scales [E][K/16][R] (uint8, one plane per 16-wide K block).
+
+    An input format, not part of the layer: each block of 16 weights along K gets the least E4M3 scale that is at
+    least max |w| / 6 (6 = the largest E2M1 value, so nothing is clipped), and every weight divided by its scale is
+    rounded to the nearest E2M1 value, ties to the even code. No tensor-wide scale.
+    """
+    E, R, K = w.shape
+    assert K % 16 == 0
+    codes = torch.empty((E, R, K // 2), dtype=torch.uint8)
+    scales = torch.empty((E, K // 16, R), dtype=torch.uint8)
+    grid = _E2M1_GRID
+    for e in range(E):
+        blk = w[e].to(torch.float32).reshape(R, K // 16, 16)
+        need = blk.abs().amax(dim=2) / 6.0
+        s8 = need.to(torch.float8_e4m3fn)
+        s = s8.to(torch.float32)
+        bump = s < need  # round the scale up to the next E4M3 value
+        s8 = torch.where(bump, (s8.view(torch.uint8) + 1).view(torch.float8_e4m3fn), s8)
+        s = s8.to(torch.float32)
+        s = torch.where(s > 0, s, torch.ones_like(s))  # an all-zero block: any scale
+        s8 = s.to(torch.float8_e4m3fn)
+        q = (blk / s.unsqueeze(2)).clamp(-6.0, 6.0)
+        mag = q.abs()
+        d = (mag.unsqueeze(-1) - grid).abs()  # distance to each grid value
+        best = d.argmin(dim=-1)
+        # ties between two grid neighbours go to the even code (fraction bit 0): argmin keeps the lower index,
+        # which is the even one for the ties 0.25, 1.25, 2.5, 5; for 0.75, 1.75, 3.5 the even code is the upper
+        tie_up = torch.zeros_like(mag, dtype=torch.bool)
+        for t in (0.75, 1.75, 3.5):
+            tie_up |= mag == t
+        best = torch.where(tie_up, best + 1, best)
+        nib = best.to(torch.uint8) | ((q < 0).to(torch.uint8) << 3)
+        nib = nib.reshape(R, K)
+        codes[e] = nib[:, 0::2] | (nib[:, 1::2] << 4)
+        scales[e] = s8.view(torch.uint8).t()
+    return codes, scales
+
+
+def nvfp4_weights(inp: Dict[str, torch.Tensor]) -> Dict[str, torch.Tensor]:
+    """The routed expert weights of a drawn workload in NVFP4 form: w_gu_q/w_gu_s, w_down_q/w_down_s."""
+    gu_q, gu_s = quantize_nvfp4(inp["w_gu"])
+    dn_q, dn_s = quantize_nvfp4(inp["w_down"])
+    return {"w_gu_q": gu_q, "w_gu_s": gu_s, "w_down_q": dn_q, "w_down_s": dn_s}

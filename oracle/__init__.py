@@ -59,10 +59,12 @@ def lib():
             L.oracle_combine_tree_partial_f64.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, P]
             L.oracle_combine_tree_finish_f64.argtypes = [P, i32, P, i64, i32, P, P]
             L.oracle_dequant_mxfp8.argtypes = [P, P, i64, i64, P]
+            L.oracle_dequant_nvfp4.argtypes = [P, P, i64, i64, P]
             for name in ("oracle_bf16_round_array", "oracle_router_logits", "oracle_topk", "oracle_swiglu_ffn",
                          "oracle_moe_forward", "oracle_permutation", "oracle_combine_f64",
                          "oracle_combine_f32_canonical", "oracle_combine_tree_partial_f64",
-                         "oracle_combine_tree_finish_f64", "oracle_dequant_mxfp8"):
+                         "oracle_combine_tree_finish_f64", "oracle_dequant_mxfp8",
+                         "oracle_dequant_nvfp4"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -247,4 +249,17 @@ def dequant_mxfp8(codes, scales):
     out = np.empty((E, R, K), dtype=np.uint16)
     for e in range(E):
         _check(lib().oracle_dequant_mxfp8(_ptr(codes[e]), _ptr(scales[e]), R, K, _ptr(out[e])), "dequant_mxfp8")
+    return out
+
+
+def dequant_nvfp4(codes, scales):
+    """E2M1 codes [E][R][K/2] (two per byte, low nibble first) with E4M3 scales [E][K/16][R] -> bf16 bits [E][R][K]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    E, R, K2 = codes.shape
+    K = 2 * K2
+    assert scales.shape == (E, K // 16, R), scales.shape
+    out = np.empty((E, R, K), dtype=np.uint16)
+    for e in range(E):
+        _check(lib().oracle_dequant_nvfp4(_ptr(codes[e]), _ptr(scales[e]), R, K, _ptr(out[e])), "dequant_nvfp4")
     return out

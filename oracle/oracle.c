@@ -424,3 +424,26 @@ int oracle_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales, int64_t ro
     }
   return 0;
 }
+
+/* E2M1 code (low 4 bits) -> exact value: sign, 2-bit exponent with bias 1, 1-bit fraction; exponent 0 gives m/2. */
+static double e2m1_value(uint8_t nib) {
+  const int sign = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+  const double mag = (e == 0) ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+  return sign ? -mag : mag;
+}
+
+int oracle_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K, uint16_t* out_bf16) {
+  if (!codes || !scales || !out_bf16 || rows < 0 || K < 0 || K % 16 != 0) return -1;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t k = 0; k < K; ++k) {
+      double sv;
+      if (e4m3_value(scales[(k / 16) * rows + r], &sv) != 0) return -1;
+      const uint8_t byte = codes[r * (K / 2) + k / 2];
+      const double v = e2m1_value((k % 2 == 0) ? (byte & 15) : (byte >> 4)) * sv;
+      const uint16_t b = oracle_bf16_from_double(v);
+      if (oracle_bf16_to_double(b) != v) return -1;
+      if (v == 0.0 && signbit(v) != ((b >> 15) & 1)) return -1;
+      out_bf16[r * K + k] = b;
+    }
+  return 0;
+}

@@ -118,6 +118,17 @@ int oracle_combine_tree_finish_f64(const double* partials, int32_t n_parts, cons
  */
 int oracle_dequant_mxfp8(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K, uint16_t* out_bf16);
 
+/*
+ * Block-scaled FP4 expert weights (NVFP4, the format the deep-prefill review names for prompt tiles): each weight
+ * is an E2M1 code (1 sign bit, 2 exponent bits with bias 1, 1 fraction bit; exponent field 0 holds 0 and 0.5) times
+ * an E4M3 scale shared by a block of 16 consecutive weights along K. No tensor-wide scale (it is taken as 1).
+ * codes [R][K/2], two codes per byte, element 2j in the low nibble of byte j, element 2j+1 in the high nibble;
+ * scales [K/16][R] (one plane per 16-wide K block), K a multiple of 16. out_bf16 [R][K]: the exact value of each
+ * weight as bf16 bits (a product of a 2-bit and a 4-bit significand always fits bf16 here). Returns -1 for a NaN
+ * scale (0x7F / 0xFF).
+ */
+int oracle_dequant_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K, uint16_t* out_bf16);
+
 #ifdef __cplusplus
 }
 #endif

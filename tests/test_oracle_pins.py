@@ -542,3 +542,62 @@ def test_mxfp8_quantizer_round_trip(oracle_lib):
     amax = np.abs(ref).reshape(3, 16, 4, 32).max(axis=3)
     qmax = amax / np.ldexp(1.0, scales.numpy().astype(np.int64).transpose(0, 2, 1) - 127)
     assert np.all((qmax > 224) & (qmax <= 448))
+
+
+# ---------------------------------------------------------------- NVFP4 weights (E2M1 codes, E4M3 block scales)
+
+def test_nvfp4_hand_worked_codes(oracle_lib):
+    table = {int(c): float(v) for c, v in _fixture_lines("e2m1_codes.txt")}
+    assert len(table) == 16
+    for lo in range(16):
+        hi = 15 - lo
+        codes = np.zeros((1, 1, 8), np.uint8)
+        codes[0, 0, 3] = lo | (hi << 4)  # elements 6 (low nibble) and 7 (high nibble)
+        scales = np.full((1, 1, 1), 0x38, np.uint8)  # E4M3 1.0
+        got = oracle_lib.bf16_to_double(oracle_lib.dequant_nvfp4(codes, scales)[0, 0, 6:8])
+        for g, want in zip(got, (table[lo], table[hi])):
+            assert g == want and math.copysign(1, g) == math.copysign(1, want), (lo, hi, got)
+
+
+def test_nvfp4_matches_library_scale_decoding(oracle_lib):
+    """Every code with E4M3 scales across the format (subnormal to 448, either sign), against the hand table times
+    torch's float8_e4m3fn decoding of the scale; every product is exact in bf16."""
+    table = np.array([float(v) for _, v in _fixture_lines("e2m1_codes.txt")])
+    rng = np.random.default_rng(41)
+    R, K = 6, 512
+    codes = rng.integers(0, 256, size=(2, R, K // 2)).astype(np.uint8)
+    scale_codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    scales = rng.choice(scale_codes, size=(2, K // 16, R)).astype(np.uint8)
+    scales[0, :, 0] = scale_codes[:K // 16]
+    got = oracle_lib.bf16_to_double(oracle_lib.dequant_nvfp4(codes, scales))
+    nib = np.stack([codes & 15, codes >> 4], axis=-1).reshape(2, R, K)
+    s_val = torch.from_numpy(scales).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    want = table[nib] * np.repeat(s_val.transpose(0, 2, 1), 16, axis=2)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_nvfp4_rejects_nan_scale(oracle_lib):
+    codes = np.zeros((1, 2, 8), np.uint8)
+    with pytest.raises(ValueError):
+        oracle_lib.dequant_nvfp4(codes, np.full((1, 1, 2), 0x7F, np.uint8))
+
+
+def test_nvfp4_quantizer_round_trip(oracle_lib):
+    """The synthetic NVFP4 inputs decode (oracle) to the nearest E2M1 multiple of the block scale (ties even), and
+    every block's scale is the least E4M3 value >= max |w| / 6."""
+    from expert_major_chunked_gb300 import workloads
+    g = torch.Generator().manual_seed(6)
+    w = (torch.randn((2, 8, 64), generator=g) * 0.02).to(torch.bfloat16)
+    codes, scales = workloads.quantize_nvfp4(w)
+    got = oracle_lib.bf16_to_double(oracle_lib.dequant_nvfp4(codes.numpy(), scales.numpy()))
+    ref = w.double().numpy()
+    s = torch.from_numpy(scales.numpy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()  # [E][K/16][R]
+    s_full = np.repeat(s.transpose(0, 2, 1), 16, axis=2)
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    q = np.abs(ref) / s_full
+    nearest = np.min(np.abs(q[..., None] - grid), axis=-1)
+    assert np.all(np.abs(np.abs(got) / s_full - q) <= nearest + 1e-12)
+    amax = np.abs(ref).reshape(2, 8, 4, 16).max(axis=3).transpose(0, 2, 1)  # [E][K/16][R]
+    assert np.all(s * 6.0 >= amax)
+    smaller = torch.from_numpy((scales.numpy() - 1).astype(np.uint8)).view(torch.float8_e4m3fn).to(torch.float64)
+    assert np.all((smaller.numpy() * 6.0 < amax) | (scales.numpy() == 0))
