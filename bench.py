@@ -48,8 +48,9 @@ def parse_args():
     ap.add_argument("--combine", choices=["f32", "f64"], default="f32",
                     help="layer combine: canonical float32 (default) or the float64 tree over expert ids")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode-size (1 and 8 token) latency lines")
-    ap.add_argument("--weights", choices=["bf16", "mxfp8"], default="bf16",
-                    help="routed expert weights: bf16, or MXFP8 (E4M3 codes + E8M0 scale per 32 along K)")
+    ap.add_argument("--weights", choices=["bf16", "mxfp8", "nvfp4"], default="bf16",
+                    help="routed expert weights: bf16, MXFP8 (E4M3 codes + E8M0 scale per 32 along K) or NVFP4 "
+                         "(E2M1 codes + E4M3 scale per 16 along K)")
     ap.add_argument("--offload-copy", choices=["routed", "all"], default="routed",
                     help="offloaded experts: stage only the routed experts (kernel) or every expert (copy engines)")
     return ap.parse_args()
@@ -206,11 +207,8 @@ def run_reference(args, dist: Dist):
     wl = workloads.WORKLOADS[args.workload]
     chunk = args.chunk or wl.chunks[0]
     inp = workloads.generate(wl)
-    if args.weights == "mxfp8":  # the oracle runs on the decoded MXFP8 weights
-        q = workloads.mxfp8_weights(inp)
-        for w, c, sc in (("w_gu", "w_gu_q", "w_gu_s"), ("w_down", "w_down_q", "w_down_s")):
-            inp[w] = torch.from_numpy(oracle.dequant_mxfp8(q[c].numpy(), q[sc].numpy()).view(np.int16)).view(
-                torch.bfloat16)
+    if args.weights != "bf16":  # the oracle runs on the decoded block-scaled weights
+        inp = decoded_weights(inp, quantized_weights(inp, args.weights), args.weights)
     cores = oracle.num_threads()
     # calibrate, then size each step so that warm-up + timed steps fit in about two minutes
     t0 = time.perf_counter()
@@ -264,9 +262,30 @@ def cpu_baseline(inp, wl, budget_s: float = 10.0) -> dict:
             "sample": f"first {n} of {wl.tokens} tokens, full layer in float64 ({secs:.1f} s)"}
 
 
+WEIGHT_BYTES = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32.0, "nvfp4": 0.5 + 1.0 / 16.0}  # per routed weight, with scales
+WEIGHT_DESC = {"bf16": "bf16",
+               "mxfp8": "mxfp8 (E4M3 codes + E8M0 scale per 32 along K; bf16 tensor-core math)",
+               "nvfp4": "nvfp4 (E2M1 codes + E4M3 scale per 16 along K; bf16 tensor-core math)"}
+
+
+def quantized_weights(inp, fmt):
+    from expert_major_chunked_gb300 import workloads
+    return workloads.mxfp8_weights(inp) if fmt == "mxfp8" else workloads.nvfp4_weights(inp)
+
+
+def decoded_weights(inp, q, fmt):
+    """The inputs with the routed expert weights replaced by the oracle's decoding of their block-scaled form."""
+    import numpy as np
+    import torch
+    import oracle
+    deq = oracle.dequant_mxfp8 if fmt == "mxfp8" else oracle.dequant_nvfp4
+    dec = lambda c, sc: torch.from_numpy(deq(c.numpy(), sc.numpy()).view(np.int16)).view(torch.bfloat16)
+    return dict(inp, w_gu=dec(q["w_gu_q"], q["w_gu_s"]), w_down=dec(q["w_down_q"], q["w_down_s"]))
+
+
 def gate_up_bytes_and_flops(wl, offs_per_chunk, chunk_sizes, wb=2.0):
     """Algorithmic DRAM bytes and useful FLOPs of one gate/up launch (per chunk, averaged over the chunks):
-    weights of the touched experts (wb bytes per routed weight: 2 for bf16, 1 + 1/32 for MXFP8 codes and scales)
+    weights of the touched experts (wb bytes per routed weight, WEIGHT_BYTES: codes and scales)
     + shared expert, the gathered input rows read once, h written once."""
     H, I, Is, k = wl.hidden, wl.inter, wl.shared_inter, wl.top_k
     tot_b = tot_f = 0.0
@@ -317,12 +336,12 @@ def run_ours(args, dist: Dist):
     chunk = args.chunk or wl.chunks[0]
     T = wl.tokens
     inp = workloads.generate(wl)
-    wb = 2.0
-    if args.weights == "mxfp8":
-        q = workloads.mxfp8_weights(inp)
-        wb = 1.0 + 1.0 / 32.0
-    if wl.offload_slots and args.weights == "mxfp8":
-        # E4M3 code banks in pinned host memory, scales, router and shared expert in device memory
+    wb = WEIGHT_BYTES[args.weights]
+    quant = args.weights != "bf16"
+    if quant:
+        q = quantized_weights(inp, args.weights)
+    if wl.offload_slots and quant:
+        # code banks in pinned host memory, scales, router and shared expert in device memory
         dev = {k: v.cuda() for k, v in inp.items() if k not in ("x", "w_gu", "w_down")}
         dev.update({"w_gu_q": q["w_gu_q"].pin_memory(), "w_down_q": q["w_down_q"].pin_memory(),
                     "w_gu_s": q["w_gu_s"].cuda(), "w_down_s": q["w_down_s"].cuda()})
@@ -331,13 +350,13 @@ def run_ours(args, dist: Dist):
         # expert banks stay in pinned host memory; router and shared expert in device memory
         dev = {k: (v.pin_memory() if k in ("w_gu", "w_down") else v.cuda()) for k, v in inp.items() if k != "x"}
         args.single_pass = False
-    elif args.weights == "mxfp8":
+    elif quant:
         dev = {k: v.cuda() for k, v in inp.items() if k not in ("x", "w_gu", "w_down")}
         dev.update({k: v.cuda() for k, v in q.items()})
     else:
         dev = {k: v.cuda() for k, v in inp.items() if k != "x"}
     layer = binding.MoePrefill(dev, top_k=wl.top_k, max_chunk=max(chunk, T if args.single_pass else chunk),
-                               offload_slots=wl.offload_slots)
+                               offload_slots=wl.offload_slots, weight_format=args.weights if quant else None)
     if args.combine == "f64":
         layer.set_combine(binding.COMBINE_F64_TREE)
     if wl.offload_slots:
@@ -404,7 +423,7 @@ def run_ours(args, dist: Dist):
     achieved = gu_bytes / gu_avg_s / 1e9
     roofline = {"bound": "hbm", "kernel": "grouped gate/up GEMM + SwiGLU", "achieved": achieved,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": ncu_traffic(wl.name + ("_mxfp8" if args.weights == "mxfp8" else ""), chunk), "algorithmic_bytes_per_launch": gu_bytes,
+                "traffic": ncu_traffic(wl.name + ("" if args.weights == "bf16" else "_" + args.weights), chunk), "algorithmic_bytes_per_launch": gu_bytes,
                 "avg_launch_ms": gu_avg_s * 1e3, "peak_source": peaks["source"] + " (hbm_gbs)"}
     tc_peak = peaks["bf16_tflops_sustained"]
     grouped = {
@@ -530,7 +549,8 @@ def run_ours(args, dist: Dist):
     if wl.offload_slots:
         # bytes over the host link per step, against a plain pinned copy: the routed experts of every chunk
         # (routed staging, counted on the device), else every expert of every chunk (copy engines)
-        bank = (inp["w_gu"].numel() + inp["w_down"].numel()) * (1 if args.weights == "mxfp8" else 2)
+        code_bytes = {"bf16": 2.0, "mxfp8": 1.0, "nvfp4": 0.5}[args.weights]  # the banks hold codes only
+        bank = int((inp["w_gu"].numel() + inp["w_down"].numel()) * code_bytes)
         per_expert = bank // wl.n_experts
         if args.offload_copy == "routed":
             h2d_bytes = route_stats["experts_copied"] * per_expert
@@ -562,12 +582,8 @@ def run_ours(args, dist: Dist):
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         cpu_inp = inp
-        if args.weights == "mxfp8":  # the oracle runs on the decoded weights
-            import numpy as np
-            import oracle
-            dec = lambda c, sc: torch.from_numpy(oracle.dequant_mxfp8(c.numpy(), sc.numpy()).view(np.int16)).view(
-                torch.bfloat16)
-            cpu_inp = dict(inp, w_gu=dec(q["w_gu_q"], q["w_gu_s"]), w_down=dec(q["w_down_q"], q["w_down_s"]))
+        if quant:  # the oracle runs on the decoded weights
+            cpu_inp = decoded_weights(inp, q, args.weights)
         cpu = cpu_baseline(cpu_inp, wl)
 
     if dist.rank == 0:
@@ -579,8 +595,7 @@ def run_ours(args, dist: Dist):
                 "clocks": clocks_info, "grouped_gemm": grouped,
                 "routing_last_run": route_stats}
         line["config"]["combine"] = "f64-tree" if args.combine == "f64" else "f32-canonical"
-        line["config"]["weights"] = ("mxfp8 (E4M3 codes + E8M0 scale per 32 along K; bf16 tensor-core math)"
-                                     if args.weights == "mxfp8" else "bf16")
+        line["config"]["weights"] = WEIGHT_DESC[args.weights]
         if wl.offload_slots:
             line["config"]["offload_copy"] = args.offload_copy
         if single is not None:

@@ -40,6 +40,8 @@ _SIGS = {
                           ctypes.POINTER(_P)], ctypes.c_int),
     "moe_prefill_plan_mxfp8": ([ctypes.POINTER(moe_dims), _P, _P, _P, _P, _P, _P, _P,
                                 ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_P)], ctypes.c_int),
+    "moe_prefill_plan_nvfp4": ([ctypes.POINTER(moe_dims), _P, _P, _P, _P, _P, _P, _P,
+                                ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(_P)], ctypes.c_int),
     "moe_prefill_run": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P, _P, _P],
                         ctypes.c_int),
     "moe_prefill_run_host": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P, _P,
@@ -106,12 +108,13 @@ def moe_prefill_plan(dims: moe_dims, w_router: int, w_gu: int, w_down: int, ws_g
 
 
 def moe_prefill_plan_mxfp8(dims: moe_dims, w_router: int, gu_codes: int, gu_scales: int, down_codes: int,
-                           down_scales: int, ws_gu: Optional[int], ws_down: Optional[int]):
-    """Returns (plan handle, workspace bytes) for MXFP8 routed experts."""
+                           down_scales: int, ws_gu: Optional[int], ws_down: Optional[int], fmt: str = "mxfp8"):
+    """Returns (plan handle, workspace bytes) for block-scaled routed experts (fmt "mxfp8" or "nvfp4")."""
     ws = ctypes.c_size_t(0)
     plan = _P(None)
-    _check(lib().moe_prefill_plan_mxfp8(ctypes.byref(dims), w_router, gu_codes, gu_scales, down_codes, down_scales,
-                                        ws_gu, ws_down, ctypes.byref(ws), ctypes.byref(plan)))
+    fn = lib().moe_prefill_plan_nvfp4 if fmt == "nvfp4" else lib().moe_prefill_plan_mxfp8
+    _check(fn(ctypes.byref(dims), w_router, gu_codes, gu_scales, down_codes, down_scales, ws_gu, ws_down,
+              ctypes.byref(ws), ctypes.byref(plan)))
     return plan.value, ws.value
 
 
@@ -219,20 +222,24 @@ class MoePrefill:
 
     weights: dict with w_router [E][H], w_gu [E][2I][H], w_down [E][H][I] and optionally ws_gu [2I_s][H],
     ws_down [H][I_s], all bf16 CUDA tensors; with offload_slots > 0, w_gu and w_down are pinned CPU tensors.
-    MXFP8 routed experts: instead of w_gu / w_down, uint8 CUDA tensors w_gu_q [E][2I][H], w_gu_s [E][H/32][2I],
-    w_down_q [E][H][I], w_down_s [E][I/32][H] (E4M3 codes and E8M0 block scales).
+    Block-scaled routed experts: instead of w_gu / w_down, uint8 tensors w_gu_q / w_gu_s / w_down_q / w_down_s —
+    weight_format "mxfp8": E4M3 codes [E][2I][H], [E][H][I] with E8M0 scales [E][H/32][2I], [E][I/32][H];
+    weight_format "nvfp4": E2M1 codes two per byte [E][2I][H/2], [E][H][I/2] with E4M3 scales [E][H/16][2I],
+    [E][I/16][H]. Codes are CUDA tensors (pinned CPU with offload_slots), scales CUDA tensors.
     """
 
-    def __init__(self, weights: dict, top_k: int, max_chunk: int, offload_slots: int = 0):
+    def __init__(self, weights: dict, top_k: int, max_chunk: int, offload_slots: int = 0,
+                 weight_format: Optional[str] = None):
         import torch
         wr = weights["w_router"]
         wsg, wsd = weights.get("ws_gu"), weights.get("ws_down")
         self.mxfp8 = "w_gu_q" in weights
+        self.weight_format = weight_format or ("mxfp8" if self.mxfp8 else "bf16")
         if self.mxfp8:
             wgu, wd = weights["w_gu_q"], weights["w_down_q"]
             for t in (weights["w_gu_s"], weights["w_down_s"]) + (() if offload_slots else (wgu, wd)):
                 if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
-                    raise ValueError("MXFP8 codes and scales must be contiguous uint8 CUDA tensors")
+                    raise ValueError("block-scaled codes and scales must be contiguous uint8 CUDA tensors")
         else:
             wgu, wd = weights["w_gu"], weights["w_down"]
         for t in (wr, wsg, wsd) + (() if (offload_slots or self.mxfp8) else (wgu, wd)):
@@ -244,14 +251,14 @@ class MoePrefill:
                 if t.dtype != want or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
                     raise ValueError("offloaded expert banks must be contiguous pinned CPU tensors")
         E, H = wr.shape
-        I = wgu.shape[1] // 2
+        I = wgu.shape[1] // 2  # rows of w_gu are 2I in every format
         Is = wsg.shape[0] // 2 if wsg is not None else 0
         self.dims = moe_dims(H, E, I, top_k, Is, 1, max_chunk, offload_slots)
         self.weights = weights  # keep alive: the plan points at them
         if self.mxfp8:
             self.plan, self.workspace_bytes = moe_prefill_plan_mxfp8(
                 self.dims, wr.data_ptr(), wgu.data_ptr(), weights["w_gu_s"].data_ptr(), wd.data_ptr(),
-                weights["w_down_s"].data_ptr(), _ptr(wsg), _ptr(wsd))
+                weights["w_down_s"].data_ptr(), _ptr(wsg), _ptr(wsd), fmt=self.weight_format)
         else:
             self.plan, self.workspace_bytes = moe_prefill_plan(self.dims, wr.data_ptr(), wgu.data_ptr(),
                                                                wd.data_ptr(), _ptr(wsg), _ptr(wsd))

@@ -15,7 +15,8 @@
 //
 // Block-scaled FP8 weights (MXFP8: E4M3 codes, one E8M0 power-of-two scale per 32 weights along K),
 // grouped_gemm_q_kernel (480 threads): the weight codes stream through their own ring of 5 stages, which carries
-// twice the weights per byte of shared memory that a bf16 stage does, and the activation rows through a ring of 3.
+// twice (four times for NVFP4: E2M1 codes, one E4M3 scale per 16) the weights per byte of shared memory that a
+// bf16 stage does, and the activation rows through a ring of 3.
 // Two groups of four warps take alternate steps: each decodes a stage's codes to bf16 into its own buffer, in the
 // 128B-swizzled layout the UMMA descriptor reads (the layout TMA writes for bf16), and hands it to the UMMA issuer.
 // A code times its scale is exactly a bf16 value, so the tensor core sees exactly the decoded weights and the
@@ -227,6 +228,45 @@ __device__ __forceinline__ void decode_stage(const uint8_t* codes, const uint8_t
   }
 }
 
+// Two E2M1 codes (one byte) times the scale f as two bf16 values; exact (E2M1 -> f16 -> f32, times an E4M3 value:
+// at most 2 x 4 significant bits, -> bf16 of a value bf16 holds).
+__device__ __forceinline__ uint32_t decode_pair_fp4(uint32_t byte, float f) {
+  const uint32_t h2 = ptx::e2m1x2_to_f16x2(byte & 0xFFu);
+  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  return pack_bf16(__fmul_rn(v.x, f), __fmul_rn(v.y, f));
+}
+
+// Decodes one stage of NVFP4 weights: `rows` rows of 32 bytes (64 E2M1 codes, element 2j in the low nibble of byte
+// j) with E4M3 scales sc[4][rows] (16-wide K blocks of the stage), into the same bf16 layout as decode_stage.
+__device__ __forceinline__ void decode_stage_fp4(const uint8_t* codes, const uint8_t* sc, uint8_t* dst, int rows,
+                                                 int ct) {
+  const int items = rows * 4;  // 16-code (8-byte) chunks, chunk i = row i / 4, K block i % 4
+  uint2 v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = ct + 128 * j;
+    if (i < items) v[j] = *reinterpret_cast<const uint2*>(codes + i * 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = ct + 128 * j;
+    if (i < items) {
+      const int r = i >> 2, c = i & 3;
+      const uint32_t sh = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(sc[c * rows + r]));
+      const float f = __half2float(*reinterpret_cast<const __half*>(&sh));  // the block's E4M3 scale
+      const uint32_t w[2] = {v[j].x, v[j].y};
+      uint32_t o[8];
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) o[4 * q + b] = decode_pair_fp4(w[q] >> (8 * b), f);
+      uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
+      *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+  }
+}
+
 // ============================================================================================ bf16 weights
 template <int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -418,8 +458,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
 // each), D (decoded bf16 B tiles, one 32 KB buffer per decoder group). Step i of the CTA's (tile, K block) sequence
 // uses A slot i % kQStagesA, C slot i % kQStagesC and D buffer i % 2, decoded by group i % 2. Only tiles whose
 // class has scales run here (the routed experts); the bf16 shared expert takes grouped_gemm_kernel.
-template <int EPI>
+template <int EPI, int FMT>
 __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const __grid_constant__ GemmParams p) {
+  // per row and 64-wide K step: code bytes and scale blocks (MXFP8: 64 codes, 2 blocks of 32; NVFP4: 32 bytes of
+  // two codes each, 4 blocks of 16)
+  constexpr uint32_t kCodeBytes = FMT == kFmtNvfp4 ? 32u : 64u;
+  constexpr int kScaleBlocks = FMT == kFmtNvfp4 ? 4 : 2;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -494,12 +538,12 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
         const GemmClass& C = p.cls[ti.cls];
         const void* tB = &p.tmB[ti.cls];
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
-        const uint32_t bytes = b_loads * C.b_box_rows * (64u + 2u);
+        const uint32_t bytes = b_loads * C.b_box_rows * (kCodeBytes + kScaleBlocks);
         const int gslot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
         const int b_row0 = tile_b_row<EPI>(C, gslot, ti.n_idx);
         const int b_row1 = b_row0 + C.b_up_offset;
         const int r0 = b_row0 - gslot * C.b_group_rows;  // first row inside the group
-        const int64_t planes = 2 * C.kblocks;             // 32-wide K blocks per row
+        const int64_t planes = kScaleBlocks * C.kblocks;  // scale blocks per row
         const bool hint = C.b_stream && ti.stream;
         for (int kb = 0; kb < C.kblocks; ++kb) {
           if (!ptx::wait_bounded(c_empty0 + 8u * slot, phase ^ 1u, tmo, abort_flag)) {
@@ -511,16 +555,17 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
           ptx::mbar_arrive_expect_tx(fb, bytes);
           const uint32_t c_dst = sC + slot * kQStageCodeBytes;
           const uint32_t s_dst = sS + slot * kQStageScaleBytes;
-          const int kc = kb * kBlockK;
+          const int kx = kb * static_cast<int>(kCodeBytes);  // inner coordinate of the code map, in bytes
           if (hint) {
-            ptx::tma_load_2d_hint(c_dst, tB, kc, b_row0, fb, pol_stream);
-            if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb, pol_stream);
+            ptx::tma_load_2d_hint(c_dst, tB, kx, b_row0, fb, pol_stream);
+            if (EPI == kEpiSwiGLU)
+              ptx::tma_load_2d_hint(c_dst + C.b_box_rows * kCodeBytes, tB, kx, b_row1, fb, pol_stream);
           } else {
-            ptx::tma_load_2d(c_dst, tB, kc, b_row0, fb);
-            if (EPI == kEpiSwiGLU) ptx::tma_load_2d(c_dst + C.b_box_rows * 64, tB, kc, b_row1, fb);
+            ptx::tma_load_2d(c_dst, tB, kx, b_row0, fb);
+            if (EPI == kEpiSwiGLU) ptx::tma_load_2d(c_dst + C.b_box_rows * kCodeBytes, tB, kx, b_row1, fb);
           }
-          for (int h = 0; h < 2; ++h) {
-            const uint8_t* plane = C.b_scale + (static_cast<int64_t>(ti.group) * planes + 2 * kb + h) *
+          for (int h = 0; h < kScaleBlocks; ++h) {
+            const uint8_t* plane = C.b_scale + (static_cast<int64_t>(ti.group) * planes + kScaleBlocks * kb + h) *
                                                    static_cast<int64_t>(C.b_group_rows);
             ptx::bulk_load(s_dst + h * C.n_tile, plane + r0, C.b_box_rows, fb);
             if (EPI == kEpiSwiGLU)
@@ -662,8 +707,12 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
           failed = true;
         }
         if (failed) break;
-        decode_stage(sC_ptr + cs * kQStageCodeBytes, sS_ptr + cs * kQStageScaleBytes,
-                     sD_ptr + group * kStageBBytes, C.n_tile, ct);
+        if (FMT == kFmtNvfp4)
+          decode_stage_fp4(sC_ptr + cs * kQStageCodeBytes, sS_ptr + cs * kQStageScaleBytes,
+                           sD_ptr + group * kStageBBytes, C.n_tile, ct);
+        else
+          decode_stage(sC_ptr + cs * kQStageCodeBytes, sS_ptr + cs * kQStageScaleBytes,
+                       sD_ptr + group * kStageBBytes, C.n_tile, ct);
         // the decoded tile to the async proxy; the codes have been consumed
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -691,19 +740,27 @@ cudaError_t prepare_gemm_kernels() {
   const auto attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiF32>, attr, kGemmSmemBytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_kernel<kEpiSwiGLU>, attr, kGemmSmemBytes);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiF32>, attr, kGemmSmemBytesQ);
-  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiSwiGLU>, attr, kGemmSmemBytesQ);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiF32, kFmtMxfp8>, attr, kGemmSmemBytesQ);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiSwiGLU, kFmtMxfp8>, attr, kGemmSmemBytesQ);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiF32, kFmtNvfp4>, attr, kGemmSmemBytesQ);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(grouped_gemm_q_kernel<kEpiSwiGLU, kFmtNvfp4>, attr, kGemmSmemBytesQ);
   return e;
 }
 
-cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream, bool mxfp8) {
+cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream, int fmt) {
   if (grid <= 0) return cudaSuccess;
-  if (mxfp8) {
-    if (epilogue == kEpiSwiGLU)
-      grouped_gemm_q_kernel<kEpiSwiGLU><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+  const bool glu = epilogue == kEpiSwiGLU;
+  if (fmt == kFmtMxfp8) {
+    if (glu)
+      grouped_gemm_q_kernel<kEpiSwiGLU, kFmtMxfp8><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
     else
-      grouped_gemm_q_kernel<kEpiF32><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
-  } else if (epilogue == kEpiSwiGLU) {
+      grouped_gemm_q_kernel<kEpiF32, kFmtMxfp8><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+  } else if (fmt == kFmtNvfp4) {
+    if (glu)
+      grouped_gemm_q_kernel<kEpiSwiGLU, kFmtNvfp4><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+    else
+      grouped_gemm_q_kernel<kEpiF32, kFmtNvfp4><<<grid, kGemmThreadsQ, kGemmSmemBytesQ, stream>>>(p);
+  } else if (glu) {
     grouped_gemm_kernel<kEpiSwiGLU><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);
   } else {
     grouped_gemm_kernel<kEpiF32><<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(p);

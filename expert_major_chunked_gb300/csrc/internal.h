@@ -59,7 +59,7 @@ constexpr int kQStagesA = 3;
 constexpr int kQStagesC = 5;
 constexpr int kQStagesD = 2;
 constexpr int kQStageCodeBytes = kMaxN * kBlockK;  // 16 KB: up to 256 rows x 64 codes
-constexpr int kQStageScaleBytes = 2 * kMaxN;       // two 32-wide K blocks x up to 256 rows
+constexpr int kQStageScaleBytes = 4 * kMaxN;       // up to four scale blocks (NVFP4: 16-wide) x 256 rows
 constexpr int kGemmThreadsQ = 15 * 32;
 constexpr int kGemmSmemBytesQ = 1024 /*align slack*/ + kQStagesA * kStageABytes + kQStagesD * kStageBBytes +
                                 kQStagesC * (kQStageCodeBytes + kQStageScaleBytes) + 256 + kEpiStageBytes;
@@ -78,7 +78,7 @@ struct GemmClass {
   int32_t b_group_mod;    // > 0: B holds a ring of b_group_mod groups and group e lives in slot e % b_group_mod
   int64_t out_ld;         // output row stride in elements
   void* out;              // F32: float*, SwiGLU: bf16*
-  const uint8_t* b_scale; // MXFP8 B (kernel variant with converter warps): E8M0 scales [G][K/32][b_group_rows];
+  const uint8_t* b_scale; // quantised B: scales [G][K/block][b_group_rows] (one plane per scale block);
                           // nullptr: B is bf16
 };
 
@@ -102,9 +102,12 @@ struct GemmParams {
   uint64_t timeout_ns;        // bound on every mbarrier wait
 };
 
-// mxfp8: the variant whose classes may hold MXFP8 B (a class with b_scale != nullptr; its tmB is a uint8 map).
+// Routed expert weight formats. kFmtMxfp8: E4M3 codes, one E8M0 scale per 32 along K; kFmtNvfp4: E2M1 codes (two
+// per byte), one E4M3 scale per 16 along K. A quantised launch runs grouped_gemm_q_kernel on the tiles of classes
+// with b_scale (their tmB is a uint8 map of the codes).
+enum WeightFormat : int { kFmtBf16 = 0, kFmtMxfp8 = 1, kFmtNvfp4 = 2 };
 cudaError_t launch_grouped_gemm(const GemmParams& p, int epilogue, int grid, cudaStream_t stream,
-                                bool mxfp8 = false);
+                                int fmt = kFmtBf16);
 cudaError_t prepare_gemm_kernels();   // sets the dynamic shared memory attribute (once per device)
 
 // ------------------------------------------------------------------ routing

@@ -79,14 +79,15 @@ moe_status encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return MOE_OK;
 }
 
-// E4M3 code matrix [rows][cols] (one byte per element, row-major), boxes of box_rows x 64 codes, no swizzle (the
-// MXFP8 decoder warps read the rows densely), zero fill out of range.
-moe_status encode_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Code matrix [rows][cols] of bytes (row-major), boxes of box_rows x box_bytes, no swizzle (the decoder warps read
+// the rows densely), zero fill out of range.
+moe_status encode_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                        uint32_t box_bytes) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockK), box_rows};
+  const cuuint32_t box[2] = {box_bytes, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -135,7 +136,8 @@ constexpr int kRouteSpan = 16384;
 
 struct Shape {
   int H, E, I, k, Is, C, span_cap, slots, window;
-  int wbytes;  // bytes per routed expert weight: 2 (bf16) or 1 (MXFP8 code)
+  int fmt;     // routed expert weights: kFmtBf16, kFmtMxfp8 or kFmtNvfp4
+  int cb64;    // bytes per 64 weights along K: 128 (bf16), 64 (MXFP8 codes), 32 (NVFP4 codes)
   int gu_half, gu_half_s, bn_down, bn_router_narrow, bn_router_wide;
   int nt_gu, nt_gu_s, nt_down;
 };
@@ -150,7 +152,8 @@ Shape make_shape(const moe_dims& d) {
   s.C = d.max_chunk;
   s.span_cap = std::max(s.C, kRouteSpan);
   s.slots = d.offload_slots;
-  s.wbytes = 2;
+  s.fmt = kFmtBf16;
+  s.cb64 = 128;
   s.window = d.offload_slots / 2;
   s.gu_half = (s.I % 128 == 0) ? 128 : 64;
   s.gu_half_s = (s.Is % 128 == 0) ? 128 : 64;
@@ -200,8 +203,8 @@ Layout make_layout(const Shape& s) {
     L.tile_base[b] = take(2 * (E + 1) * 4);
   }
   const size_t S = static_cast<size_t>(s.slots);
-  L.ring_gu = take(S * 2 * I * H * s.wbytes);
-  L.ring_down = take(S * H * I * s.wbytes);
+  L.ring_gu = take(S * 2 * I * H / 64 * s.cb64);
+  L.ring_down = take(S * H * I / 64 * s.cb64);
   L.h = take(R * I * 2);
   L.hs = take(Is > 0 ? C * Is * 2 : 0);
   L.y = take(R * H * 4);
@@ -335,12 +338,12 @@ void set_last_error(const char* msg) { g_last_error = msg; }
 namespace {
 
 moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
-                     const void* ws_gu, const void* ws_down, const void* gu_scale, const void* down_scale,
+                     const void* ws_gu, const void* ws_down, const void* gu_scale, const void* down_scale, int fmt,
                      size_t* workspace_bytes, moe_plan_t* plan) {
   if (plan) *plan = nullptr;
   moe_status st = validate_dims(dims);
   if (st != MOE_OK) return st;
-  const bool mxfp8 = gu_scale != nullptr || down_scale != nullptr;
+  const bool mxfp8 = fmt != kFmtBf16;  // any block-scaled format
   if (mxfp8 && (!gu_scale || !down_scale)) return fail(MOE_ERR_INVALID_ARG, "both scale arrays are needed");
   if (mxfp8 && (!aligned16(gu_scale) || !aligned16(down_scale)))
     return fail(MOE_ERR_INVALID_ARG, "scale arrays must be 16-byte aligned");
@@ -359,7 +362,8 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
   moe_plan* p = new moe_plan();
   p->d = *dims;
   p->sh = make_shape(*dims);
-  if (mxfp8) p->sh.wbytes = 1;
+  p->sh.fmt = fmt;
+  p->sh.cb64 = fmt == kFmtNvfp4 ? 32 : (fmt == kFmtMxfp8 ? 64 : 128);
   p->lay = make_layout(p->sh);
   p->device = device;
   p->num_sms = num_sms;
@@ -410,9 +414,9 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
   if (st == MOE_OK && !p->offload && !mxfp8)
     st = encode_bf16_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
   if (st == MOE_OK && mxfp8 && !p->offload)
-    st = encode_u8_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H, s.gu_half);
+    st = encode_u8_2d(&p->tm_wgu, w_gu, static_cast<uint64_t>(s.E) * 2 * s.I, s.H / 64 * s.cb64, s.gu_half, s.cb64);
   if (st == MOE_OK && mxfp8 && !p->offload)
-    st = encode_u8_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, s.bn_down);
+    st = encode_u8_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I / 64 * s.cb64, s.bn_down, s.cb64);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
   if (st == MOE_OK) {
@@ -443,7 +447,7 @@ extern "C" {
 
 moe_status moe_prefill_plan(const moe_dims* dims, const void* w_router, const void* w_gu, const void* w_down,
                             const void* ws_gu, const void* ws_down, size_t* workspace_bytes, moe_plan_t* plan) {
-  return plan_impl(dims, w_router, w_gu, w_down, ws_gu, ws_down, nullptr, nullptr, workspace_bytes, plan);
+  return plan_impl(dims, w_router, w_gu, w_down, ws_gu, ws_down, nullptr, nullptr, kFmtBf16, workspace_bytes, plan);
 }
 
 moe_status moe_prefill_plan_mxfp8(const moe_dims* dims, const void* w_router, const uint8_t* w_gu_codes,
@@ -452,7 +456,17 @@ moe_status moe_prefill_plan_mxfp8(const moe_dims* dims, const void* w_router, co
                                   size_t* workspace_bytes, moe_plan_t* plan) {
   if (plan) *plan = nullptr;
   if (!w_gu_scales || !w_down_scales) return fail(MOE_ERR_INVALID_ARG, "scale arrays must not be NULL");
-  return plan_impl(dims, w_router, w_gu_codes, w_down_codes, ws_gu, ws_down, w_gu_scales, w_down_scales,
+  return plan_impl(dims, w_router, w_gu_codes, w_down_codes, ws_gu, ws_down, w_gu_scales, w_down_scales, kFmtMxfp8,
+                   workspace_bytes, plan);
+}
+
+moe_status moe_prefill_plan_nvfp4(const moe_dims* dims, const void* w_router, const uint8_t* w_gu_codes,
+                                  const uint8_t* w_gu_scales, const uint8_t* w_down_codes,
+                                  const uint8_t* w_down_scales, const void* ws_gu, const void* ws_down,
+                                  size_t* workspace_bytes, moe_plan_t* plan) {
+  if (plan) *plan = nullptr;
+  if (!w_gu_scales || !w_down_scales) return fail(MOE_ERR_INVALID_ARG, "scale arrays must not be NULL");
+  return plan_impl(dims, w_router, w_gu_codes, w_down_codes, ws_gu, ws_down, w_gu_scales, w_down_scales, kFmtNvfp4,
                    workspace_bytes, plan);
 }
 
@@ -516,11 +530,17 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_xp[1], ws + L.xp[1], R, s.H, kABoxRows);
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_h, h, R, s.I, kABoxRows);
     if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(&p->tm_hs, hs, s.C, s.Is, kABoxRows);
-    auto encode_w = s.wbytes == 1 ? encode_u8_2d : encode_bf16_2d;  // ring slots hold codes or bf16 weights
-    if (rc == MOE_OK && p->offload)
-      rc = encode_w(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
-    if (rc == MOE_OK && p->offload)
-      rc = encode_w(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I, s.bn_down);
+    // ring slots hold bf16 weights or codes
+    if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
+      rc = encode_bf16_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
+    if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
+      rc = encode_bf16_2d(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I, s.bn_down);
+    if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
+      rc = encode_u8_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H / 64 * s.cb64,
+                        s.gu_half, s.cb64);
+    if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
+      rc = encode_u8_2d(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I / 64 * s.cb64,
+                        s.bn_down, s.cb64);
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;
@@ -720,8 +740,8 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     auto copy_window = [&](int64_t cidx, int e0) -> moe_status {
       const int hb = (e0 / s.window) & 1;
       const size_t slot0 = static_cast<size_t>(e0 % s.slots);
-      const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H * s.wbytes;
-      const size_t dn_bytes = static_cast<size_t>(s.H) * s.I * s.wbytes;
+      const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64;
+      const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
       moe_status r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[hb], 0), "slot release wait");
       if (r2 == MOE_OK && p->offload_copy == MOE_OFFLOAD_COPY_ROUTED) {
         // only the experts this chunk routes rows to, decided on the device once its member lists exist
@@ -765,7 +785,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     // bf16 shared expert in the plain one, as a second launch on the same stream.
     auto grouped = [&](GemmParams prm, int epi, int cap, const int32_t* tb, const int32_t* n_tiles, int e0, int e1,
                        bool windowed, int kind, const char* what) -> moe_status {
-      const bool q = p->w_gu_scale != nullptr;
+      const bool q = s.fmt != kFmtBf16;
       if (!q) {
         if (windowed) {
           prm.range_lo = tb + e0;
@@ -778,11 +798,11 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       LaunchScope ls(p, kind, st, shared ? 2 : 1);
       prm.range_lo = windowed ? tb + e0 : nullptr;
       prm.range_hi = tb + std::min(e1, s.E);
-      moe_status r2 = cuda_status(launch_grouped_gemm(prm, epi, std::min(p->num_sms, cap), st, true), what);
+      moe_status r2 = cuda_status(launch_grouped_gemm(prm, epi, std::min(p->num_sms, cap), st, s.fmt), what);
       if (r2 == MOE_OK && shared) {
         prm.range_lo = tb + s.E;
         prm.range_hi = n_tiles;
-        r2 = cuda_status(launch_grouped_gemm(prm, epi, p->num_sms, st, false), what);
+        r2 = cuda_status(launch_grouped_gemm(prm, epi, p->num_sms, st, kFmtBf16), what);
       }
       return r2;
     };

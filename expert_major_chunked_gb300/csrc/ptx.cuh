@@ -109,6 +109,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   return out;
 }
 
+// Two E2M1 codes (one byte, low nibble -> low half) to two f16 values, exactly.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(out) : "r"(byte));
+  return out;
+}
+
 // L2 policy for data read once and not needed again soon (streamed expert weights).
 __device__ __forceinline__ uint64_t make_policy_evict_first() {
   uint64_t pol;

@@ -117,6 +117,23 @@ moe_status moe_prefill_plan_mxfp8(const moe_dims* dims, const void* w_router, co
                                   size_t* workspace_bytes, moe_plan_t* plan);
 
 /*
+ * moe_prefill_plan_nvfp4 — moe_prefill_plan for routed experts stored as block-scaled FP4 (NVFP4), the format the
+ * deep-prefill draft's review ("To land") names for prompt tiles: a quarter of the bf16 bytes.
+ *   w_gu_codes    device (or, with offload_slots > 0, pinned host) uint8 [E][2I][H/2]: E2M1 codes (1 sign, 2 exponent
+ *                 bits with bias 1, 1 fraction bit; values 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte, element 2j in
+ *                 the low nibble of byte j.
+ *   w_gu_scales   device uint8 [E][H/16][2I]: the E4M3 scale of each 16-wide K block (not NaN), one plane per block.
+ *   w_down_codes  uint8 [E][H][I/2];  w_down_scales: device uint8 [E][I/16][H].
+ *   Other arguments and behaviour as for moe_prefill_plan_mxfp8. No tensor-wide scale (it is 1). A code times its
+ *   scale (at most 2 x 4 significant bits, magnitude 2^-10 .. 2688) is always exactly a bf16 value, so the results
+ *   equal, byte for byte, moe_prefill_plan on the decoded bf16 weights.
+ */
+moe_status moe_prefill_plan_nvfp4(const moe_dims* dims, const void* w_router, const uint8_t* w_gu_codes,
+                                  const uint8_t* w_gu_scales, const uint8_t* w_down_codes,
+                                  const uint8_t* w_down_scales, const void* ws_gu, const void* ws_down,
+                                  size_t* workspace_bytes, moe_plan_t* plan);
+
+/*
  * moe_prefill_run — the layer over T tokens, in chunks of `chunk` tokens (the last chunk may be shorter).
  *   x               device bf16 [T][H].
  *   T               tokens (T == 0: no-op, MOE_OK).
