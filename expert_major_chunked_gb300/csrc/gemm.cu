@@ -97,15 +97,20 @@ __device__ __forceinline__ int tile_b_row(const GemmClass& C, int slot, int n_id
 }
 
 // Reads one tile's accumulator (columns [0, n_tile) at tbase) back from TMEM and stores the tile's outputs. Each of
-// the four epilogue warps owns a 32-row slab. A 32-column block of the accumulator arrives one row per lane; it is
-// staged in shared memory (odd row stride: no bank conflicts) and written back row-contiguously, so every store
-// instruction covers whole 128-byte lines instead of 32 different rows.
-template <int EPI>
-__device__ __forceinline__ void epilogue_tile(const GemmClass& C, const TileInfo& ti, uint32_t tbase,
-                                              uint32_t* stage, int lane, int q) {
+// the four epilogue warps owns a 32-row slab; a 32-column block of the accumulator arrives one row per lane.
+// SwiGLU: the bf16 results are staged in shared memory (odd row stride: no bank conflicts) and written back
+// row-contiguously, so every store instruction covers whole 128-byte lines.
+// F32: a block whose 32 rows all belong to the tile (or whose map clips the rest) is written into one of the warp's
+// NBUF staging buffers in the 128B-swizzled layout (16-byte chunk j of row r at chunk j ^ (r % 8): conflict-free)
+// and stored by a single TMA tensor store; the buffer is reused once that store has read it. Rows of a partial slab
+// are stored directly, one row per lane, since the rows after them belong to other tiles.
+template <int EPI, int NBUF>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const GemmClass& C, const TileInfo& ti,
+                                              uint32_t tbase, uint8_t* bufs, int lane, int q, uint32_t& blk) {
   const int slab_rows = ti.rows - q * 32;
   const int64_t slab_row0 = static_cast<int64_t>(ti.out_row0) + q * 32;
   if (EPI == kEpiSwiGLU) {
+    uint32_t* stage = reinterpret_cast<uint32_t*>(bufs);
     const int half = C.b_box_rows;
     const int64_t ldw = C.out_ld / 2;  // row stride in 32-bit words (two bf16 each)
     uint32_t* outw = reinterpret_cast<uint32_t*>(C.out) + (static_cast<int64_t>(ti.n_idx) * half) / 2;
@@ -130,45 +135,61 @@ __device__ __forceinline__ void epilogue_tile(const GemmClass& C, const TileInfo
       __syncwarp();
     }
   } else {
+    if (slab_rows <= 0) return;
     const int col0 = ti.n_idx * C.n_tile;
+    const bool tma = C.out_tma == 2 || (C.out_tma == 1 && slab_rows >= 32);
     float* outb = static_cast<float*>(C.out) + col0;
     const bool vec = (C.out_ld % 4) == 0;
     for (int c = 0; c < C.n_tile; c += 32) {
       uint32_t v[32];
       ptx::tmem_ld32(tbase + c, v);
       ptx::tmem_ld_wait();
+      if (tma) {
+        uint8_t* buf = bufs + (blk % NBUF) * kEpiBufBytes;
+        if (lane == 0) ptx::bulk_wait_group_read<NBUF - 1>();  // the store that last read this buffer is done
+        __syncwarp();
+        uint8_t* rowp = buf + lane * 128;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
-      __syncwarp();
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&p.tmOut[ti.cls], ptx::smem_u32(buf), col0 + c, static_cast<int32_t>(slab_row0));
+          ptx::bulk_commit_group();
+        }
+        ++blk;
+      } else if (lane < slab_rows) {
+        float* dst = outb + (slab_row0 + lane) * C.out_ld + c;
+        const int gc0 = col0 + c;
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int r = m * 4 + (lane >> 3), cc = (lane & 7) * 4;
-        if (r < slab_rows) {
-          const uint32_t* sr = stage + r * 33 + cc;
-          float* dst = outb + (slab_row0 + r) * C.out_ld + c + cc;
-          const int gc = col0 + c + cc;
+        for (int j = 0; j < 8; ++j) {
+          const int gc = gc0 + 4 * j;
           if (vec && gc + 4 <= C.out_cols) {
-            *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(sr[0]), __uint_as_float(sr[1]),
-                                                          __uint_as_float(sr[2]), __uint_as_float(sr[3]));
+            *reinterpret_cast<float4*>(dst + 4 * j) =
+                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                            __uint_as_float(v[4 * j + 3]));
           } else {
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-              if (gc + jj < C.out_cols) dst[jj] = __uint_as_float(sr[jj]);
+              if (gc + jj < C.out_cols) dst[4 * j + jj] = __uint_as_float(v[4 * j + jj]);
           }
         }
       }
-      __syncwarp();
     }
   }
 }
 
-// The epilogue role (warps 2..5) of both kernels: waits for each tile's accumulator, stores it, frees it.
-template <int EPI>
+// The epilogue role (warps 2..5) of both kernels: waits for each tile's accumulator, stores it, frees it. Before
+// the role ends, lane 0 waits for its TMA stores to complete (their shared-memory sources stay live until then).
+template <int EPI, int NBUF>
 __device__ __forceinline__ void epilogue_role(const GemmParams& p, int tfirst, int ntiles, uint32_t tmem_base,
-                                              uint32_t tfull0, uint32_t tempty0, uint32_t* stage, int warp, int lane,
+                                              uint32_t tfull0, uint32_t tempty0, uint8_t* bufs, int warp, int lane,
                                               volatile int* abort_flag) {
   const int q = warp & 3;
   int local = 0;
+  uint32_t blk = 0;
   for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
     const TileInfo ti = decode_tile(p, t);
     const int acc = local & 1;
@@ -181,18 +202,39 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, int tfirst, i
     }
     ptx::tc_fence_after();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kMaxN);
-    epilogue_tile<EPI>(p.cls[ti.cls], ti, tbase, stage, lane, q);
+    epilogue_tile<EPI, NBUF>(p, p.cls[ti.cls], ti, tbase, bufs, lane, q, blk);
     ptx::tc_fence_before();
     ptx::mbar_arrive(tempty0 + 8u * acc);
   }
+  if (lane == 0) ptx::bulk_wait_group_all();
+  __syncwarp();
 }
 
-// Two E4M3 codes times the scale f (a power of two) as two bf16 values; every step is exact (E4M3 -> f16 -> f32,
-// times a power of two, -> bf16 of a value bf16 holds).
-__device__ __forceinline__ uint32_t decode_pair(uint32_t codes16, float f) {
+// An exact f16x2 value whose significands need at most 7 fraction bits, as the bf16x2 bits of the same values times
+// 2^-112: f16 and bf16 share the sign bit and the leading fraction bits, and the 5-bit f16 exponent (bias 15) read
+// as a bf16 exponent (bias 127) scales by 2^-112. Zeros stay (signed) zeros; no f16 subnormal reaches here (E4M3
+// and E2M1 values are f16 normals).
+__device__ __forceinline__ uint32_t f16x2_as_bf16x2_m112(uint32_t h2) {
+  return ((h2 & 0x7FFF7FFFu) >> 3) | (h2 & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// bf16x2 with both halves 2^e (e + 127 in 1..254).
+__device__ __forceinline__ uint32_t bf16x2_pow2(int e) {
+  return static_cast<uint32_t>(e + 127) * 0x00800080u;
+}
+
+// Two E4M3 codes times 2^(s - 127) as two bf16 values: E4M3 -> f16 (one conversion, exact), the bits read as bf16
+// times 2^-112, then two exact multiplies by 2^ea and 2^eb (ea + eb = s - 15; each factor and every intermediate
+// stays a bf16 normal for s in [10, 246], where the products are bf16 values).
+__device__ __forceinline__ uint32_t decode_pair(uint32_t codes16, uint32_t fa, uint32_t fb) {
   const uint32_t h2 = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(codes16));
-  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  return pack_bf16(__fmul_rn(v.x, f), __fmul_rn(v.y, f));
+  return bf16x2_mul(bf16x2_mul(f16x2_as_bf16x2_m112(h2), fa), fb);
 }
 
 // Decodes one stage of MXFP8 weights: `rows` rows of 64 E4M3 codes (row-major, as TMA landed them) with scales
@@ -213,13 +255,15 @@ __device__ __forceinline__ void decode_stage(const uint8_t* codes, const uint8_t
     const int i = ct + 128 * j;
     if (i < items) {
       const int r = i >> 2, c = i & 3;
-      const float f = __uint_as_float(static_cast<uint32_t>(sc[(c >> 1) * rows + r]) << 23);  // 2^(s - 127)
+      const int e = static_cast<int>(sc[(c >> 1) * rows + r]) - 15;  // 2^(s - 127) = 2^-112 * 2^e
+      const int ea = e >> 1;
+      const uint32_t fa = bf16x2_pow2(ea), fb = bf16x2_pow2(e - ea);
       const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
       uint32_t o[8];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        o[2 * q] = decode_pair(w[q], f);
-        o[2 * q + 1] = decode_pair(w[q] >> 16, f);
+        o[2 * q] = decode_pair(w[q], fa, fb);
+        o[2 * q + 1] = decode_pair(w[q] >> 16, fa, fb);
       }
       uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
       *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -228,12 +272,11 @@ __device__ __forceinline__ void decode_stage(const uint8_t* codes, const uint8_t
   }
 }
 
-// Two E2M1 codes (one byte) times the scale f as two bf16 values; exact (E2M1 -> f16 -> f32, times an E4M3 value:
-// at most 2 x 4 significant bits, -> bf16 of a value bf16 holds).
-__device__ __forceinline__ uint32_t decode_pair_fp4(uint32_t byte, float f) {
-  const uint32_t h2 = ptx::e2m1x2_to_f16x2(byte & 0xFFu);
-  const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  return pack_bf16(__fmul_rn(v.x, f), __fmul_rn(v.y, f));
+// Two E2M1 codes (one byte) times the block scale as two bf16 values: E2M1 -> f16 (one conversion, exact), read as
+// bf16 times 2^-112, times f2 = the scale times 2^112 (a bf16 normal for every E4M3 scale but zero). Exact: a code
+// times an E4M3 value has at most 2 x 4 significant bits and magnitude 2^-10 .. 2688.
+__device__ __forceinline__ uint32_t decode_pair_fp4(uint32_t byte, uint32_t f2) {
+  return bf16x2_mul(f16x2_as_bf16x2_m112(ptx::e2m1x2_to_f16x2(byte & 0xFFu)), f2);
 }
 
 // Decodes one stage of NVFP4 weights: `rows` rows of 32 bytes (64 E2M1 codes, element 2j in the low nibble of byte
@@ -253,13 +296,14 @@ __device__ __forceinline__ void decode_stage_fp4(const uint8_t* codes, const uin
     if (i < items) {
       const int r = i >> 2, c = i & 3;
       const uint32_t sh = ptx::e4m3x2_to_f16x2(static_cast<uint16_t>(sc[c * rows + r]));
-      const float f = __half2float(*reinterpret_cast<const __half*>(&sh));  // the block's E4M3 scale
+      const float f = __half2float(*reinterpret_cast<const __half*>(&sh)) * 0x1p112f;  // the E4M3 scale x 2^112
+      const uint32_t f2 = pack_bf16(f, f);
       const uint32_t w[2] = {v[j].x, v[j].y};
       uint32_t o[8];
 #pragma unroll
       for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) o[4 * q + b] = decode_pair_fp4(w[q] >> (8 * b), f);
+        for (int b = 0; b < 4; ++b) o[4 * q + b] = decode_pair_fp4(w[q] >> (8 * b), f2);
       uint8_t* rowp = dst + (r >> 3) * 1024 + (r & 7) * 128;
       *reinterpret_cast<uint4*>(rowp + (((2 * c) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
       *reinterpret_cast<uint4*>(rowp + (((2 * c + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -440,8 +484,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
-    uint32_t* stage = reinterpret_cast<uint32_t*>(bars_ptr + 256) + (warp - 2) * (32 * 33);
-    epilogue_role<EPI>(p, tfirst, ntiles, tmem_base, tfull0, tempty0, stage, warp, lane, abort_flag);
+    uint8_t* bufs = bars_ptr + kBarRegionBytes + (warp - 2) * kEpiBufs * kEpiBufBytes;
+    epilogue_role<EPI, kEpiBufs>(p, tfirst, ntiles, tmem_base, tfull0, tempty0, bufs, warp, lane, abort_flag);
   }
 
   // ------------------------------------------------------------ teardown
@@ -681,8 +725,8 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
     __syncwarp();
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
-    uint32_t* stage = reinterpret_cast<uint32_t*>(bars_ptr + 256) + (warp - 2) * (32 * 33);
-    epilogue_role<EPI>(p, tfirst, ntiles, tmem_base, tfull0, tempty0, stage, warp, lane, abort_flag);
+    uint8_t* bufs = bars_ptr + kBarRegionBytes + (warp - 2) * kEpiBufs * kEpiBufBytes;
+    epilogue_role<EPI, kEpiBufs>(p, tfirst, ntiles, tmem_base, tfull0, tempty0, bufs, warp, lane, abort_flag);
   } else {
     // ------------------------------------------------------------ decoders (warps 6..13: groups 0 and 1)
     const int dt = static_cast<int>(threadIdx.x) - 6 * 32;

@@ -50,8 +50,15 @@ constexpr int kABoxRows = 32;       // A rows per TMA box (a tile loads ceil(row
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM alloc, warps 2..5 epilogue
 constexpr int kStageABytes = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBBytes = kMaxN * kBlockK * 2;     // 32 KB
-constexpr int kEpiStageBytes = 4 * 32 * 33 * 4;            // epilogue staging: a 32 x 33-word block per warp
-constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + 256 + kEpiStageBytes;
+constexpr int kEpiBufBytes = 32 * 128;   // epilogue staging buffer: 32 rows x 128 B (a 32 x 32 fp32 block)
+// One staging buffer per epilogue warp: a second one (overlapping a block's TMA store with the next block) measured
+// no faster, and the CTA's shared memory stays at 210 KB, which leaves room on each SM for the routing and combine
+// kernels that run beside the GEMMs on the other stream (at 226 KB they could not, and the gate/up launches started
+// late on the SMs they held: +13% gate/up time).
+constexpr int kEpiBufs = 1;
+constexpr int kBarRegionBytes = 1024;    // mbarriers and slots; keeps the staging buffers 1024-byte aligned
+constexpr int kGemmSmemBytes = 1024 /*align slack*/ + kStages * (kStageABytes + kStageBBytes) + kBarRegionBytes +
+                               4 * kEpiBufs * kEpiBufBytes;
 // Block-scaled FP8 weights (MXFP8), grouped_gemm_q_kernel: rings of activation rows (A), E4M3 codes with their
 // E8M0 scales (C) and decoded bf16 B tiles (D, one per decoder group). Warps: 0 codes TMA, 1 UMMA, 2..5 epilogue,
 // 6..13 two decoder groups of 4, 14 activation TMA.
@@ -62,9 +69,12 @@ constexpr int kQStageCodeBytes = kMaxN * kBlockK;  // 16 KB: up to 256 rows x 64
 constexpr int kQStageScaleBytes = 4 * kMaxN;       // up to four scale blocks (NVFP4: 16-wide) x 256 rows
 constexpr int kGemmThreadsQ = 15 * 32;
 constexpr int kGemmSmemBytesQ = 1024 /*align slack*/ + kQStagesA * kStageABytes + kQStagesD * kStageBBytes +
-                                kQStagesC * (kQStageCodeBytes + kQStageScaleBytes) + 256 + kEpiStageBytes;
+                                kQStagesC * (kQStageCodeBytes + kQStageScaleBytes) + kBarRegionBytes +
+                                4 * kEpiBufs * kEpiBufBytes;
 
 enum Epilogue : int { kEpiF32 = 0, kEpiSwiGLU = 1 };
+
+static_assert(kGemmSmemBytes <= 215040 && kGemmSmemBytesQ <= 232448, "shared memory per CTA");
 
 // One operand class of a grouped GEMM launch (class 0: routed experts, class 1: shared expert).
 struct GemmClass {
@@ -78,6 +88,10 @@ struct GemmClass {
   int32_t b_group_mod;    // > 0: B holds a ring of b_group_mod groups and group e lives in slot e % b_group_mod
   int64_t out_ld;         // output row stride in elements
   void* out;              // F32: float*, SwiGLU: bf16*
+  int32_t out_tma;        // F32: 0 plain stores; 1 full 32-row slabs through GemmParams::tmOut[cls] (partial slabs
+                          // stored directly: rows past a tile belong to other tiles); 2 every slab through the map
+                          // (its row bound is the valid rows, so TMA clips the rest)
+  int32_t pad_;
   const uint8_t* b_scale; // quantised B: scales [G][K/block][b_group_rows] (one plane per scale block);
                           // nullptr: B is bf16
 };
@@ -88,6 +102,7 @@ struct GemmClass {
 struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
+  CUtensorMap tmOut[2];       // F32 outputs with out_tma != 0: fp32 [rows][out_ld] map, box 32 x 32, 128B swizzle
   GemmClass cls[2];
   const int4* tiles;          // device tile list (nullptr: dense mode)
   const int32_t* num_tiles;   // device tile count (used when tiles != nullptr)

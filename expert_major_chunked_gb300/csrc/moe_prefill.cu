@@ -79,6 +79,23 @@ moe_status encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return MOE_OK;
 }
 
+// fp32 output matrix [rows][cols] with row stride ld elements (ld % 4 == 0), written by TMA stores of 32 x 32
+// blocks staged with 128-byte swizzle; stores past rows or cols are clipped.
+moe_status encode_f32_out(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, uint64_t ld) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu x %llu] fp32 output", (int)r,
+                (unsigned long long)rows, (unsigned long long)cols);
+  return MOE_OK;
+}
+
 // Code matrix [rows][cols] of bytes (row-major), boxes of box_rows x box_bytes, no swizzle (the decoder warps read
 // the rows densely), zero fill out of range.
 moe_status encode_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
@@ -225,6 +242,7 @@ struct moe_plan {
   // descriptors of workspace-resident activations, cached per workspace pointer
   const void* ws_cached = nullptr;
   CUtensorMap tm_xp[2], tm_h, tm_hs, tm_ring_gu, tm_ring_down;
+  CUtensorMap tm_y, tm_s;  // fp32 outputs of the down projection (routed rows, shared expert rows)
   // offloaded experts: w_gu / w_down are pinned host banks; the copy stream fills the ring (see moe_prefill_run)
   bool offload = false;
   // device-accessible addresses of the pinned banks (null when the device cannot read them directly)
@@ -530,6 +548,8 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_xp[1], ws + L.xp[1], R, s.H, kABoxRows);
     if (rc == MOE_OK) rc = encode_bf16_2d(&p->tm_h, h, R, s.I, kABoxRows);
     if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(&p->tm_hs, hs, s.C, s.Is, kABoxRows);
+    if (rc == MOE_OK) rc = encode_f32_out(&p->tm_y, y, R, s.H, s.H);
+    if (rc == MOE_OK && s.Is > 0) rc = encode_f32_out(&p->tm_s, sbuf, s.C, s.H, s.H);
     // ring slots hold bf16 weights or codes
     if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
       rc = encode_bf16_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
@@ -628,7 +648,13 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       rc0.out_cols = s.E;
       rc0.out_ld = s.E;
       rc0.out = logits + off * s.E;
+      rc0.out_tma = 2;  // the map's rows are the span's ng tokens
       g.cls[0] = g.cls[1] = rc0;
+      {
+        const moe_status r0 = encode_f32_out(&g.tmOut[0], logits + off * s.E, static_cast<uint64_t>(ng), s.E, s.E);
+        if (r0 != MOE_OK) return r0;
+        g.tmOut[1] = g.tmOut[0];
+      }
       g.tiles = nullptr;
       g.num_tiles = nullptr;
       g.dense_m = ng;
@@ -880,8 +906,10 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       d_r.b_group_mod = windowed ? s.slots : 0;
       d_r.out_ld = s.H;
       d_r.out = y;
+      d_r.out_tma = 1;
       d_r.b_scale = p->w_down_scale;
       dn.cls[0] = d_r;
+      dn.tmOut[0] = p->tm_y;
       if (s.Is > 0) {
         dn.tmA[1] = p->tm_hs;
         dn.tmB[1] = p->tm_wsdown;
@@ -893,10 +921,12 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
         d_s.b_group_mod = 0;
         d_s.out = sbuf;
         dn.cls[1] = d_s;
+        dn.tmOut[1] = p->tm_s;
       } else {
         dn.tmA[1] = dn.tmA[0];
         dn.tmB[1] = dn.tmB[0];
         dn.cls[1] = d_r;
+        dn.tmOut[1] = dn.tmOut[0];
       }
       dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down[par]);
       dn.num_tiles = num_tiles + 1;
@@ -1255,6 +1285,9 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
     cl.b_up_offset = 0;
     n_tiles = (n + cl.n_tile - 1) / cl.n_tile;
     st = encode_bf16_2d(&g.tmB[0], b, n, k_dim, cl.b_box_rows);
+    cl.out_tma = 2;  // TMA stores, clipped at the map's m rows and n columns
+    if (st == MOE_OK) st = encode_f32_out(&g.tmOut[0], c, m, n, n);
+    g.tmOut[1] = g.tmOut[0];
   } else {
     const int half = (n % 128 == 0) ? 128 : 64;
     cl.n_tile = 2 * half;
