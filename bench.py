@@ -51,6 +51,8 @@ def parse_args():
     ap.add_argument("--weights", choices=["bf16", "mxfp8", "nvfp4"], default="bf16",
                     help="routed expert weights: bf16, MXFP8 (E4M3 codes + E8M0 scale per 32 along K) or NVFP4 "
                          "(E2M1 codes + E4M3 scale per 16 along K)")
+    ap.add_argument("--hot-experts", type=int, default=0,
+                    help="offloaded experts: keep the N experts routed in the most chunks of the warm-up run resident")
     ap.add_argument("--offload-copy", choices=["routed", "all"], default="routed",
                     help="offloaded experts: stage only the routed experts (kernel) or every expert (copy engines)")
     return ap.parse_args()
@@ -379,6 +381,15 @@ def run_ours(args, dist: Dist):
     layer.raise_on_device_error()
     offs_host = offs.cpu().numpy()
     chunk_sizes = [min(chunk, T - c0) for c0 in range(0, T, chunk)]
+    hot = []
+    if wl.offload_slots and args.hot_experts > 0:
+        # popularity from the warm-up run: chunks an expert has rows in, then its rows, then the lower id
+        rows = np.diff(offs_host, axis=1)
+        order = np.lexsort((np.arange(wl.n_experts), -rows.sum(0), -(rows > 0).sum(0)))
+        hot = [int(e) for e in order[:args.hot_experts]]
+        layer.set_hot_experts(hot)
+        step(x, out)  # stages the set once
+        layer.raise_on_device_error()
 
     # ---------------------------------------------------------------- timed region (device-resident inputs)
     clocks = ClockSampler(gpu_selector(torch, dist.local_rank))
@@ -570,6 +581,8 @@ def run_ours(args, dist: Dist):
         achieved_link = h2d_bytes / (ms_per_step / 1e3) / 1e9
         offload = {"slots": wl.offload_slots, "copy": args.offload_copy, "h2d_bytes_per_step": h2d_bytes,
                    "experts_copied": route_stats["experts_copied"], "experts_skipped": route_stats["experts_skipped"],
+                   "hot_experts": len(hot), "experts_hot": route_stats.get("experts_hot", 0),
+                   "hot_set_bytes_once": len(hot) * per_expert,
                    "h2d_gbs": achieved_link,
                    "pinned_copy_gbs": link_gbs, "link_frac": achieved_link / link_gbs}
         kname = ("routed-expert staging kernel (reads the pinned banks)" if args.offload_copy == "routed"

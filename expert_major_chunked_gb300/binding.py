@@ -55,6 +55,8 @@ _SIGS = {
                                  _P, _P, _P], ctypes.c_int),
     "moe_prefill_set_combine": ([_P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_set_offload_copy": ([_P, ctypes.c_int32], ctypes.c_int),
+    "moe_prefill_set_hot_experts": ([_P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
+                                     ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "moe_prefill_check": ([_P, _P], ctypes.c_int),
     "moe_prefill_destroy": ([_P], None),
     "moe_prefill_last_error": ([], ctypes.c_char_p),
@@ -159,6 +161,15 @@ def moe_prefill_set_offload_copy(plan, mode: int):
     _check(lib().moe_prefill_set_offload_copy(plan, mode))
 
 
+def moe_prefill_set_hot_experts(plan, hot_ids) -> int:
+    """Names the offloaded experts kept resident; returns the workspace size later runs need."""
+    ids = [int(e) for e in hot_ids]
+    arr = (ctypes.c_int32 * max(1, len(ids)))(*ids)
+    ws = ctypes.c_size_t(0)
+    _check(lib().moe_prefill_set_hot_experts(plan, arr if ids else None, len(ids), ctypes.byref(ws)))
+    return ws.value
+
+
 def moe_prefill_set_combine(plan, mode: int):
     _check(lib().moe_prefill_set_combine(plan, mode))
 
@@ -192,7 +203,7 @@ def moe_prefill_set_wait_timeout(plan, timeout_ns: int):
 
 
 STATS_NAMES = ["chunks", "flagged", "by_float", "by_double", "by_sequential", "by_many", "experts_copied",
-               "experts_skipped"]
+               "experts_skipped", "experts_hot"]
 
 
 def moe_prefill_run_stats(workspace, stream=None) -> dict:
@@ -287,6 +298,14 @@ class MoePrefill:
     def set_offload_copy(self, mode: int):
         """OFFLOAD_COPY_ROUTED (stage only routed experts; default where available) or OFFLOAD_COPY_ALL."""
         moe_prefill_set_offload_copy(self.plan, mode)
+
+    def set_hot_experts(self, hot_ids):
+        """Keeps these offloaded experts resident (staged once); grows the workspace when the set needs it."""
+        import torch
+        need = moe_prefill_set_hot_experts(self.plan, hot_ids)
+        if need > self.workspace.numel():
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.workspace.device)
+        self.workspace_bytes = need
 
     def set_combine(self, mode: int):
         """COMBINE_F32 (canonical float32, ascending expert id; default) or COMBINE_F64_TREE."""

@@ -90,6 +90,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Where a group's B rows live: the group itself (resident weights), its ring slot e % b_group_mod (offloaded
+// experts), or the slot the map gives (offloaded experts with a resident hot set).
+__device__ __forceinline__ int b_slot(const GemmClass& C, int group) {
+  if (C.b_group_mod <= 0) return group;
+  return C.b_slot_map != nullptr ? __ldg(C.b_slot_map + group) : group % C.b_group_mod;
+}
+
 // First B row of a tile's (first) box: the group's (or ring slot's) row base plus the N tile's offset.
 template <int EPI>
 __device__ __forceinline__ int tile_b_row(const GemmClass& C, int slot, int n_idx) {
@@ -389,7 +396,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         const int nA = (ti.rows + kABoxRows - 1) / kABoxRows;
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
         const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * 128u;
-        const int slot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
+        const int slot = b_slot(C, ti.group);
         const int b_row0 = tile_b_row<EPI>(C, slot, ti.n_idx);
         const int b_row1 = b_row0 + C.b_up_offset;
         for (int kb = 0; kb < C.kblocks; ++kb) {
@@ -583,7 +590,7 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
         const void* tB = &p.tmB[ti.cls];
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
         const uint32_t bytes = b_loads * C.b_box_rows * (kCodeBytes + kScaleBlocks);
-        const int gslot = C.b_group_mod > 0 ? ti.group % C.b_group_mod : ti.group;
+        const int gslot = b_slot(C, ti.group);
         const int b_row0 = tile_b_row<EPI>(C, gslot, ti.n_idx);
         const int b_row1 = b_row0 + C.b_up_offset;
         const int r0 = b_row0 - gslot * C.b_group_rows;  // first row inside the group

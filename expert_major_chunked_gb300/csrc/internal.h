@@ -37,7 +37,8 @@ struct WsHeader {
   int32_t band_levels[4];      // flagged tokens decided by: float sums, double sums, sequential sums, many-candidate path
   int32_t experts_copied;      // offloaded experts staged into the ring (this run)
   int32_t experts_skipped;     // offloaded experts not staged: no row of their chunk was routed to them (this run)
-  int32_t pad[53];
+  int32_t experts_hot;         // offloaded experts with rows in a chunk served from the resident hot set (this run)
+  int32_t pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -94,6 +95,8 @@ struct GemmClass {
   int32_t pad_;
   const uint8_t* b_scale; // quantised B: scales [G][K/block][b_group_rows] (one plane per scale block);
                           // nullptr: B is bf16
+  const int32_t* b_slot_map;  // b_group_mod > 0 with a hot set: slot of each group [G] (a ring slot e % b_group_mod
+                              // or a hot slot >= b_group_mod); nullptr: slot e % b_group_mod
 };
 
 // Tile record: x = group | (cls << 15) | (n_idx << 16) | (stream << 31); y = first A row; z = valid rows (1..128);
@@ -221,6 +224,7 @@ struct RingCopyParams {
   WsHeader* hdr;
   int64_t gu16, dn16;        // one expert's gate/up and down bytes / 16
   int32_t e0, count, slots;  // experts [e0, e0 + count) into slots e % slots
+  const int32_t* slot_map;   // nullptr, or [E]: experts with slot_map[e] >= slots are resident (hot) and not staged
 };
 cudaError_t launch_ring_copy(const RingCopyParams& p, cudaStream_t stream);
 

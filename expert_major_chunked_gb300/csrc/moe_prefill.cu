@@ -143,7 +143,8 @@ struct Layout {
       total;
   // two sets (chunk parity): the member lists of chunk c+1 are built while chunk c's GEMMs still read chunk c's
   size_t token_row[2], num_tiles[2], tiles_gu[2], tiles_down[2], xp[2], tile_base[2];
-  size_t ring_gu, ring_down;  // offloaded experts: the HBM ring of expert slots
+  size_t ring_gu, ring_down;  // offloaded experts: the HBM ring of expert slots, then the hot set's slots
+  size_t slot_map;            // offloaded experts: slot of each expert [E] (used with a hot set)
   int cap_gu, cap_down;
 };
 
@@ -153,6 +154,7 @@ constexpr int kRouteSpan = 16384;
 
 struct Shape {
   int H, E, I, k, Is, C, span_cap, slots, window;
+  int hot;     // offloaded experts kept resident in slots [slots, slots + hot) (moe_prefill_set_hot_experts)
   int fmt;     // routed expert weights: kFmtBf16, kFmtMxfp8 or kFmtNvfp4
   int cb64;    // bytes per 64 weights along K: 128 (bf16), 64 (MXFP8 codes), 32 (NVFP4 codes)
   int gu_half, gu_half_s, bn_down, bn_router_narrow, bn_router_wide;
@@ -169,6 +171,7 @@ Shape make_shape(const moe_dims& d) {
   s.C = d.max_chunk;
   s.span_cap = std::max(s.C, kRouteSpan);
   s.slots = d.offload_slots;
+  s.hot = 0;
   s.fmt = kFmtBf16;
   s.cb64 = 128;
   s.window = d.offload_slots / 2;
@@ -219,9 +222,10 @@ Layout make_layout(const Shape& s) {
     L.xp[b] = take(R * H * 2);
     L.tile_base[b] = take(2 * (E + 1) * 4);
   }
-  const size_t S = static_cast<size_t>(s.slots);
+  const size_t S = static_cast<size_t>(s.slots) + static_cast<size_t>(s.hot);
   L.ring_gu = take(S * 2 * I * H / 64 * s.cb64);
   L.ring_down = take(S * H * I / 64 * s.cb64);
+  L.slot_map = take(s.slots > 0 ? E * 4 : 0);
   L.h = take(R * I * 2);
   L.hs = take(Is > 0 ? C * Is * 2 : 0);
   L.y = take(R * H * 4);
@@ -249,6 +253,10 @@ struct moe_plan {
   const void* bank_gu_dev = nullptr;
   const void* bank_down_dev = nullptr;
   int32_t offload_copy = MOE_OFFLOAD_COPY_ALL;
+  // resident hot set of offloaded experts: slot of every expert (e % S, or S + its place in the set), and whether
+  // the set still has to be staged into the cached workspace
+  std::vector<int32_t> slot_map_host;
+  bool hot_pending = false;
   // MXFP8 routed experts: w_gu / w_down hold E4M3 codes, these their E8M0 scales ([E][K/32][rows])
   const uint8_t* w_gu_scale = nullptr;
   const uint8_t* w_down_scale = nullptr;
@@ -551,16 +559,22 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     if (rc == MOE_OK) rc = encode_f32_out(&p->tm_y, y, R, s.H, s.H);
     if (rc == MOE_OK && s.Is > 0) rc = encode_f32_out(&p->tm_s, sbuf, s.C, s.H, s.H);
     // ring slots hold bf16 weights or codes
+    const uint64_t ring_slots = static_cast<uint64_t>(s.slots) + static_cast<uint64_t>(s.hot);
     if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
-      rc = encode_bf16_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H, s.gu_half);
+      rc = encode_bf16_2d(&p->tm_ring_gu, ws + L.ring_gu, ring_slots * 2 * s.I, s.H, s.gu_half);
     if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
-      rc = encode_bf16_2d(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I, s.bn_down);
+      rc = encode_bf16_2d(&p->tm_ring_down, ws + L.ring_down, ring_slots * s.H, s.I, s.bn_down);
     if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
-      rc = encode_u8_2d(&p->tm_ring_gu, ws + L.ring_gu, static_cast<uint64_t>(s.slots) * 2 * s.I, s.H / 64 * s.cb64,
-                        s.gu_half, s.cb64);
+      rc = encode_u8_2d(&p->tm_ring_gu, ws + L.ring_gu, ring_slots * 2 * s.I, s.H / 64 * s.cb64, s.gu_half, s.cb64);
     if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
-      rc = encode_u8_2d(&p->tm_ring_down, ws + L.ring_down, static_cast<uint64_t>(s.slots) * s.H, s.I / 64 * s.cb64,
-                        s.bn_down, s.cb64);
+      rc = encode_u8_2d(&p->tm_ring_down, ws + L.ring_down, ring_slots * s.H, s.I / 64 * s.cb64, s.bn_down, s.cb64);
+    // the slot map (read by the GEMMs and the staging kernel when a hot set exists), ahead of everything this run
+    // enqueues; the hot experts themselves are staged on the copy stream below
+    if (rc == MOE_OK && p->offload && s.hot > 0)
+      rc = cuda_status(cudaMemcpyAsync(ws + L.slot_map, p->slot_map_host.data(), sizeof(int32_t) * s.E,
+                                       cudaMemcpyHostToDevice, st),
+                       "slot map upload");
+    p->hot_pending = p->offload && s.hot > 0;
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;
@@ -581,6 +595,30 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     if (hio && cudaEventRecord(p->ev_join, p->host_io) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
     return r;
   };
+  // A new hot set (or a new workspace): stage the hot experts into their slots once, ahead of the first window's
+  // copies on the same stream (every GEMM waits for a window's copies, so for these too).
+  if (p->hot_pending) {
+    const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64;
+    const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
+    for (int e = 0; rc == MOE_OK && e < s.E; ++e) {
+      const int32_t slot = p->slot_map_host[e];
+      if (slot < s.slots) continue;
+      rc = cuda_status(cudaMemcpyAsync(ws + L.ring_gu + static_cast<size_t>(slot) * gu_bytes,
+                                       static_cast<const char*>(p->w_gu) + static_cast<size_t>(e) * gu_bytes,
+                                       gu_bytes, cudaMemcpyHostToDevice, cp),
+                       "hot expert gate/up copy");
+      if (rc == MOE_OK)
+        rc = cuda_status(cudaMemcpyAsync(ws + L.ring_down + static_cast<size_t>(slot) * dn_bytes,
+                                         static_cast<const char*>(p->w_down) + static_cast<size_t>(e) * dn_bytes,
+                                         dn_bytes, cudaMemcpyHostToDevice, cp),
+                         "hot expert down copy");
+    }
+    if (rc != MOE_OK) {
+      p->ws_cached = nullptr;  // stage again on the next run
+      return join(rc);
+    }
+    p->hot_pending = false;
+  }
   // A span is routed in two segments: its first chunk (on `compute`, before anything else) and the rest (on the
   // side stream, beside the first chunk's GEMMs). With host buffers the span's X rows go to the device in the same
   // two copies, each with its event, so each segment starts once its own rows have landed.
@@ -785,6 +823,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
         rp.e0 = e0;
         rp.count = s.window;
         rp.slots = s.slots;
+        rp.slot_map = s.hot > 0 ? reinterpret_cast<const int32_t*>(ws + L.slot_map) : nullptr;
         if (r2 == MOE_OK) r2 = cuda_status(launch_ring_copy(rp, cp), "expert staging launch");
         if (r2 == MOE_OK) ++p->launches;
         if (r2 == MOE_OK) r2 = cuda_status(cudaEventRecord(p->ev_copy[hb], cp), "copy event");
@@ -856,6 +895,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       c_r.out_cols = s.I;
       c_r.b_stream = 1;
       c_r.b_group_mod = windowed ? s.slots : 0;
+      c_r.b_slot_map = (windowed && s.hot > 0) ? reinterpret_cast<const int32_t*>(ws + L.slot_map) : nullptr;
       c_r.out_ld = s.I;
       c_r.out = h;
       c_r.b_scale = p->w_gu_scale;
@@ -904,6 +944,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       d_r.out_cols = s.H;
       d_r.b_stream = 1;
       d_r.b_group_mod = windowed ? s.slots : 0;
+      d_r.b_slot_map = c_r.b_slot_map;
       d_r.out_ld = s.H;
       d_r.out = y;
       d_r.out_tma = 1;
@@ -919,6 +960,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
         d_s.b_group_rows = 0;
         d_s.b_stream = 0;
         d_s.b_group_mod = 0;
+        d_s.b_slot_map = nullptr;
         d_s.out = sbuf;
         dn.cls[1] = d_s;
         dn.tmOut[1] = p->tm_s;
@@ -1162,6 +1204,29 @@ moe_status moe_prefill_set_offload_copy(moe_plan_t p, int32_t mode) {
   return MOE_OK;
 }
 
+moe_status moe_prefill_set_hot_experts(moe_plan_t p, const int32_t* hot_ids, int32_t n_hot,
+                                       size_t* workspace_bytes) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (!p->offload) return fail(MOE_ERR_INVALID_ARG, "the plan has no offloaded experts");
+  const int E = p->sh.E;
+  if (n_hot < 0 || n_hot > E) return fail(MOE_ERR_INVALID_ARG, "n_hot must be in [0, %d] (got %d)", E, n_hot);
+  if (n_hot > 0 && !hot_ids) return fail(MOE_ERR_INVALID_ARG, "hot_ids is NULL");
+  std::vector<int32_t> map(static_cast<size_t>(E));
+  for (int e = 0; e < E; ++e) map[e] = e % p->sh.slots;
+  for (int32_t h = 0; h < n_hot; ++h) {
+    const int32_t e = hot_ids[h];
+    if (e < 0 || e >= E) return fail(MOE_ERR_INVALID_ARG, "hot expert id %d out of range [0, %d)", e, E);
+    if (map[e] >= p->sh.slots) return fail(MOE_ERR_INVALID_ARG, "hot expert id %d given twice", e);
+    map[e] = p->sh.slots + h;
+  }
+  p->slot_map_host.swap(map);
+  p->sh.hot = n_hot;
+  p->lay = make_layout(p->sh);
+  p->ws_cached = nullptr;  // new layout: re-encode the workspace maps and stage the set on the next run
+  if (workspace_bytes) *workspace_bytes = p->lay.total;
+  return MOE_OK;
+}
+
 moe_status moe_prefill_set_combine(moe_plan_t p, int32_t mode) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
   if (mode != MOE_COMBINE_F32 && mode != MOE_COMBINE_F64_TREE)
@@ -1192,7 +1257,7 @@ moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* 
   CUDA_TRY(cudaMemcpy(&hdr, workspace, sizeof hdr, cudaMemcpyDeviceToHost));
   const int32_t all[MOE_STATS_COUNT] = {hdr.chunks_done,       hdr.band_tokens,       hdr.band_levels[0],
                                         hdr.band_levels[1],   hdr.band_levels[2],   hdr.band_levels[3],
-                                        hdr.experts_copied, hdr.experts_skipped};
+                                        hdr.experts_copied, hdr.experts_skipped, hdr.experts_hot};
   for (int32_t i = 0; i < n_stats; ++i) stats[i] = i < MOE_STATS_COUNT ? all[i] : 0;
   return MOE_OK;
 }

@@ -30,9 +30,13 @@ __device__ __forceinline__ void copy16(const uint4* __restrict__ src, uint4* __r
 }
 
 __global__ void __launch_bounds__(kRingThreads) ring_copy_kernel(RingCopyParams p) {
-  int copied = 0;
+  int copied = 0, hot = 0;
   for (int e = p.e0; e < p.e0 + p.count; ++e) {
     if (p.tile_base[e + 1] <= p.tile_base[e]) continue;  // no row of this chunk goes to expert e
+    if (p.slot_map != nullptr && p.slot_map[e] >= p.slots) {  // resident in the hot set
+      ++hot;
+      continue;
+    }
     ++copied;
     const int64_t slot = e % p.slots;
     copy16(p.bank_gu + e * p.gu16, p.ring_gu + slot * p.gu16, p.gu16);
@@ -40,7 +44,8 @@ __global__ void __launch_bounds__(kRingThreads) ring_copy_kernel(RingCopyParams 
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     atomicAdd(&p.hdr->experts_copied, copied);
-    atomicAdd(&p.hdr->experts_skipped, p.count - copied);
+    atomicAdd(&p.hdr->experts_skipped, p.count - copied - hot);
+    atomicAdd(&p.hdr->experts_hot, hot);
   }
 }
 

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(256) router_norms_kernel(const uint16_t* w, in
     for (int i = 0; i < 4; ++i) hdr->band_levels[i] = 0;
     hdr->experts_copied = 0;
     hdr->experts_skipped = 0;
+    hdr->experts_hot = 0;
   }
   if (e >= E) return;
   const float ss = row_sumsq(w + static_cast<int64_t>(e) * H, H, lane);

@@ -249,6 +249,26 @@ moe_status moe_prefill_combine_f64(const float* y, const float* w, const int32_t
 enum { MOE_OFFLOAD_COPY_ALL = 0, MOE_OFFLOAD_COPY_ROUTED = 1 };
 moe_status moe_prefill_set_offload_copy(moe_plan_t plan, int32_t mode);
 
+/*
+ * moe_prefill_set_hot_experts — keep n_hot offloaded experts resident ("hot set") in extra slots after the ring,
+ * for plans with offload_slots > 0. Umbrella PR #1113: "Persistent expert-profile checkpoint" keeps per-expert use
+ * counts as placement priors that warm resident expert lines at startup, and "Latest measured follow-up" accounts
+ * the copied bytes by category (demand, initial prefetch, cross-layer prefetch); the plain reading here: the caller
+ * names the most used experts (e.g. by the expert_offsets of an earlier run), they are staged once per workspace,
+ * and no chunk stages them again.
+ *   hot_ids          host int32 [n_hot], distinct expert ids in [0, E); copied, the caller keeps ownership.
+ *   n_hot            0 .. E; 0 removes the set.
+ *   workspace_bytes  out (may be NULL): the workspace size later runs need (the set's slots are part of it:
+ *                    n_hot x one expert's gate/up + down bytes more than without a set).
+ * The hot experts are copied from the pinned banks on the copy stream at the start of the next run (and of the first
+ * run on any other workspace); the routed staging kernel skips them (counted in MOE_STATS_EXPERTS_HOT) and the
+ * GEMMs read them from their slots. With MOE_OFFLOAD_COPY_ALL every window is still copied whole. Output bytes are
+ * the same with and without a set. Errors: MOE_ERR_INVALID_ARG for a NULL plan, a plan without offloaded experts,
+ * n_hot out of range, hot_ids NULL with n_hot > 0, an id out of range or given twice (the plan is then unchanged).
+ */
+moe_status moe_prefill_set_hot_experts(moe_plan_t plan, const int32_t* hot_ids, int32_t n_hot,
+                                       size_t* workspace_bytes);
+
 /* Combine of the layer: the float32 canonical reduction (default) or the float64 tree above. */
 enum { MOE_COMBINE_F32 = 0, MOE_COMBINE_F64_TREE = 1 };
 /* moe_prefill_set_combine — select the combine of later runs of this plan. */
@@ -336,7 +356,8 @@ enum {
   MOE_STATS_BY_MANY = 5,      /* ... with more candidates than the recheck list holds (sequential sums) */
   MOE_STATS_EXPERTS_COPIED = 6,  /* offloaded experts staged into the ring, summed over chunks (routed mode) */
   MOE_STATS_EXPERTS_SKIPPED = 7, /* offloaded experts left out: their chunk routed no row to them (routed mode) */
-  MOE_STATS_COUNT = 8
+  MOE_STATS_EXPERTS_HOT = 8,     /* offloaded experts with rows in a chunk, read from the hot set (routed mode) */
+  MOE_STATS_COUNT = 9
 };
 /* Writes min(n_stats, ...) entries of the list above to stats (entries past MOE_STATS_COUNT are 0). */
 moe_status moe_prefill_run_stats(void* workspace, moe_stream_t stream, int32_t* stats, int32_t n_stats);

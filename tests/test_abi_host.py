@@ -147,6 +147,14 @@ def test_float64_combine_rejects_bad_arguments(L):
     assert b"plan" in L.moe_prefill_last_error()
 
 
+def test_hot_experts_reject_a_missing_plan(L):
+    ids = (ctypes.c_int32 * 2)(1, 2)
+    ws = ctypes.c_size_t(7)
+    assert L.moe_prefill_set_hot_experts(None, ids, 2, ctypes.byref(ws)) == -1
+    assert b"plan" in L.moe_prefill_last_error()
+    assert ws.value == 7  # untouched on error
+
+
 def test_last_error_is_per_thread(L):
     L.moe_prefill_combine(None, None, None, None, 4, 0, 64, None, None)
     main_msg = L.moe_prefill_last_error()
