@@ -53,6 +53,8 @@ def parse_args():
                          "(E2M1 codes + E4M3 scale per 16 along K)")
     ap.add_argument("--hot-experts", type=int, default=0,
                     help="offloaded experts: keep the N experts routed in the most chunks of the warm-up run resident")
+    ap.add_argument("--prefetch", action="store_true",
+                    help="offloaded experts: after each run, stage the next run's first window (cross-layer prefetch)")
     ap.add_argument("--offload-copy", choices=["routed", "all"], default="routed",
                     help="offloaded experts: stage only the routed experts (kernel) or every expert (copy engines)")
     return ap.parse_args()
@@ -370,8 +372,12 @@ def run_ours(args, dist: Dist):
     n_chunks = (T + chunk - 1) // chunk
     offs = torch.empty((n_chunks, wl.n_experts + 1), dtype=torch.int32, device="cuda")
 
+    prefetch = bool(wl.offload_slots) and args.prefetch
+
     def step(xd, od, ch=chunk, offs_buf=None):
         layer.run(xd, ch, out=od, expert_offsets=offs_buf)
+        if prefetch:  # the same layer stands in for the next one: its first window moves during this run's tail
+            layer.prefetch()
 
     # warm-up (also records the per-chunk expert offsets for the byte/FLOP accounting)
     step(x, out, offs_buf=offs)
@@ -582,6 +588,7 @@ def run_ours(args, dist: Dist):
         offload = {"slots": wl.offload_slots, "copy": args.offload_copy, "h2d_bytes_per_step": h2d_bytes,
                    "experts_copied": route_stats["experts_copied"], "experts_skipped": route_stats["experts_skipped"],
                    "hot_experts": len(hot), "experts_hot": route_stats.get("experts_hot", 0),
+                   "prefetch": prefetch,
                    "hot_set_bytes_once": len(hot) * per_expert,
                    "h2d_gbs": achieved_link,
                    "pinned_copy_gbs": link_gbs, "link_frac": achieved_link / link_gbs}

@@ -57,6 +57,7 @@ _SIGS = {
     "moe_prefill_set_offload_copy": ([_P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_set_hot_experts": ([_P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+    "moe_prefill_prefetch": ([_P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "moe_prefill_check": ([_P, _P], ctypes.c_int),
     "moe_prefill_destroy": ([_P], None),
     "moe_prefill_last_error": ([], ctypes.c_char_p),
@@ -306,6 +307,11 @@ class MoePrefill:
         if need > self.workspace.numel():
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.workspace.device)
         self.workspace_bytes = need
+
+    def prefetch(self, copy_stream=None):
+        """Stages the first window of experts of this layer's next run now (offloaded experts only)."""
+        _check(lib().moe_prefill_prefetch(self.plan, self.workspace.data_ptr(), self.workspace_bytes,
+                                          copy_stream.cuda_stream if copy_stream is not None else None))
 
     def set_combine(self, mode: int):
         """COMBINE_F32 (canonical float32, ascending expert id; default) or COMBINE_F64_TREE."""

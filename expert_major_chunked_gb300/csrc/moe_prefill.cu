@@ -262,6 +262,9 @@ struct moe_plan {
   const uint8_t* w_down_scale = nullptr;
   cudaStream_t own_copy = nullptr;
   cudaEvent_t ev_copy[2] = {}, ev_rel[2] = {};
+  // cross-layer prefetch (moe_prefill_prefetch): the first window of the next run, staged ahead on a copy stream
+  cudaEvent_t ev_prefetch = nullptr;
+  const void* prefetch_ws = nullptr;  // the workspace it was staged into (consumed by the next run)
   // Each chunk's member lists (count, scan, permute) run on a side stream so that they overlap the previous chunk's
   // GEMMs; events order the two streams (see moe_prefill_run).
   cudaStream_t side = nullptr;
@@ -453,7 +456,7 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->host_io, cudaStreamNonBlocking);
     cudaEvent_t* evs[] = {&p->ev_fork,    &p->ev_span,    &p->ev_join,    &p->ev_ready[0], &p->ev_ready[1],
                           &p->ev_down,    &p->ev_comb,    &p->ev_copy[0], &p->ev_copy[1], &p->ev_rel[0],
-                          &p->ev_rel[1],  &p->ev_x_head,  &p->ev_x_rest};
+                          &p->ev_rel[1],  &p->ev_x_head,  &p->ev_x_rest,  &p->ev_prefetch};
     for (cudaEvent_t* ev : evs)
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) st = fail(MOE_ERR_CUDA, "stream/event creation: %s", cudaGetErrorString(e));
@@ -619,6 +622,9 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     }
     p->hot_pending = false;
   }
+  // the first window of the first chunk was staged ahead by moe_prefill_prefetch into this workspace
+  const bool prefetched = p->offload && p->prefetch_ws == workspace;
+  p->prefetch_ws = nullptr;
   // A span is routed in two segments: its first chunk (on `compute`, before anything else) and the rest (on the
   // side stream, beside the first chunk's GEMMs). With host buffers the span's X rows go to the device in the same
   // two copies, each with its event, so each segment starts once its own rows have landed.
@@ -807,6 +813,11 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64;
       const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
       moe_status r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[hb], 0), "slot release wait");
+      if (r2 == MOE_OK && prefetched && cidx == 0 && e0 == 0) {  // every expert of the window is already there
+        r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_prefetch, 0), "prefetch wait");
+        if (r2 == MOE_OK) r2 = cuda_status(cudaEventRecord(p->ev_copy[hb], cp), "copy event");
+        return r2;
+      }
       if (r2 == MOE_OK && p->offload_copy == MOE_OFFLOAD_COPY_ROUTED) {
         // only the experts this chunk routes rows to, decided on the device once its member lists exist
         const int par = static_cast<int>(cidx & 1);
@@ -1221,10 +1232,41 @@ moe_status moe_prefill_set_hot_experts(moe_plan_t p, const int32_t* hot_ids, int
   }
   p->slot_map_host.swap(map);
   p->sh.hot = n_hot;
+  p->prefetch_ws = nullptr;  // the ring's down slots may move: a staged first window no longer counts
   p->lay = make_layout(p->sh);
   p->ws_cached = nullptr;  // new layout: re-encode the workspace maps and stage the set on the next run
   if (workspace_bytes) *workspace_bytes = p->lay.total;
   return MOE_OK;
+}
+
+moe_status moe_prefill_prefetch(moe_plan_t p, void* workspace, size_t workspace_bytes, moe_stream_t copy) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (!p->offload) return fail(MOE_ERR_INVALID_ARG, "the plan has no offloaded experts");
+  if (!workspace || workspace_bytes < p->lay.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace needs %zu bytes (got %zu)", p->lay.total, workspace_bytes);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(MOE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  if (dev != p->device) return fail(MOE_ERR_INVALID_ARG, "current device %d differs from the plan's %d", dev, p->device);
+  const Shape& s = p->sh;
+  const Layout& L = p->lay;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t cp = copy ? reinterpret_cast<cudaStream_t>(copy) : p->own_copy;
+  const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64;
+  const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
+  // window 0 = experts [0, W) in slots [0, W), once the last run's use of the ring's first half is over
+  p->prefetch_ws = nullptr;
+  moe_status r = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[0], 0), "slot release wait");
+  if (r == MOE_OK)
+    r = cuda_status(cudaMemcpyAsync(ws + L.ring_gu, p->w_gu, gu_bytes * s.window, cudaMemcpyHostToDevice, cp),
+                    "prefetch gate/up copy");
+  if (r == MOE_OK)
+    r = cuda_status(cudaMemcpyAsync(ws + L.ring_down, p->w_down, dn_bytes * s.window, cudaMemcpyHostToDevice, cp),
+                    "prefetch down copy");
+  if (r == MOE_OK) r = cuda_status(cudaEventRecord(p->ev_prefetch, cp), "prefetch event");
+  if (r == MOE_OK) p->prefetch_ws = workspace;
+  return r;
 }
 
 moe_status moe_prefill_set_combine(moe_plan_t p, int32_t mode) {
@@ -1267,7 +1309,7 @@ void moe_prefill_destroy(moe_plan_t p) {
   if (p->host_io) cudaStreamDestroy(p->host_io);
   for (cudaEvent_t e : {p->ev_x_head, p->ev_x_rest}) if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : {p->ev_fork, p->ev_span, p->ev_join, p->ev_ready[0], p->ev_ready[1], p->ev_down, p->ev_comb,
-                        p->ev_copy[0], p->ev_copy[1], p->ev_rel[0], p->ev_rel[1]})
+                        p->ev_copy[0], p->ev_copy[1], p->ev_rel[0], p->ev_rel[1], p->ev_prefetch})
     if (e) cudaEventDestroy(e);
   if (p->side) cudaStreamDestroy(p->side);
   if (p->own_copy) cudaStreamDestroy(p->own_copy);

@@ -269,6 +269,23 @@ moe_status moe_prefill_set_offload_copy(moe_plan_t plan, int32_t mode);
 moe_status moe_prefill_set_hot_experts(moe_plan_t plan, const int32_t* hot_ids, int32_t n_hot,
                                        size_t* workspace_bytes);
 
+/*
+ * moe_prefill_prefetch — cross-layer prefetch for plans with offload_slots > 0: stages, on `copy`, the first window
+ * of experts (ids 0 .. offload_slots/2 − 1, every one of them: the next run's routing is not known yet) into the
+ * ring of `workspace`, so that the next moe_prefill_run on that workspace starts its first chunk's GEMMs without
+ * waiting for that window's copy. Umbrella PR #1113, "Latest measured follow-up": copies are accounted as demand,
+ * initial prefetch and cross-layer prefetch; the plain reading: while one layer computes, the next layer's first
+ * experts move. Call it once the previous layer's run (or this plan's own last run) is enqueued.
+ *   workspace, workspace_bytes  the workspace the next run of this plan will use (at least the plan's size).
+ *   copy                        stream for the copies (NULL: the plan's own copy stream).
+ * The copy waits for the release of the ring's first half by this plan's last run. The next run consumes the
+ * prefetch if it runs on the same workspace (a run on another workspace drops it; so does
+ * moe_prefill_set_hot_experts); the prefetched window is not counted in the staging statistics. Output bytes do
+ * not change. Errors: MOE_ERR_INVALID_ARG (NULL plan, plan without offloaded experts, misaligned workspace, wrong
+ * device), MOE_ERR_WORKSPACE (workspace too small), MOE_ERR_CUDA.
+ */
+moe_status moe_prefill_prefetch(moe_plan_t plan, void* workspace, size_t workspace_bytes, moe_stream_t copy);
+
 /* Combine of the layer: the float32 canonical reduction (default) or the float64 tree above. */
 enum { MOE_COMBINE_F32 = 0, MOE_COMBINE_F64_TREE = 1 };
 /* moe_prefill_set_combine — select the combine of later runs of this plan. */

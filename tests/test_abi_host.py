@@ -153,6 +153,8 @@ def test_hot_experts_reject_a_missing_plan(L):
     assert L.moe_prefill_set_hot_experts(None, ids, 2, ctypes.byref(ws)) == -1
     assert b"plan" in L.moe_prefill_last_error()
     assert ws.value == 7  # untouched on error
+    assert L.moe_prefill_prefetch(None, ctypes.c_void_p(0x1000), 1 << 20, None) == -1
+    assert b"plan" in L.moe_prefill_last_error()
 
 
 def test_last_error_is_per_thread(L):
