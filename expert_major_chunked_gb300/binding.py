@@ -245,20 +245,22 @@ class MoePrefill:
         import torch
         wr = weights["w_router"]
         wsg, wsd = weights.get("ws_gu"), weights.get("ws_down")
-        self.mxfp8 = "w_gu_q" in weights
-        self.weight_format = weight_format or ("mxfp8" if self.mxfp8 else "bf16")
-        if self.mxfp8:
+        self.block_scaled = "w_gu_q" in weights
+        self.weight_format = weight_format or ("mxfp8" if self.block_scaled else "bf16")
+        if self.weight_format not in ("bf16", "mxfp8", "nvfp4") or (self.weight_format != "bf16") != self.block_scaled:
+            raise ValueError("weight_format must be 'mxfp8' or 'nvfp4' with w_gu_q/... weights, 'bf16' without")
+        if self.block_scaled:
             wgu, wd = weights["w_gu_q"], weights["w_down_q"]
             for t in (weights["w_gu_s"], weights["w_down_s"]) + (() if offload_slots else (wgu, wd)):
                 if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous():
                     raise ValueError("block-scaled codes and scales must be contiguous uint8 CUDA tensors")
         else:
             wgu, wd = weights["w_gu"], weights["w_down"]
-        for t in (wr, wsg, wsd) + (() if (offload_slots or self.mxfp8) else (wgu, wd)):
+        for t in (wr, wsg, wsd) + (() if (offload_slots or self.block_scaled) else (wgu, wd)):
             if t is not None and (t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous()):
                 raise ValueError("weights must be contiguous bf16 CUDA tensors")
         if offload_slots:
-            want = torch.uint8 if self.mxfp8 else torch.bfloat16
+            want = torch.uint8 if self.block_scaled else torch.bfloat16
             for t in (wgu, wd):
                 if t.dtype != want or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
                     raise ValueError("offloaded expert banks must be contiguous pinned CPU tensors")
@@ -267,7 +269,7 @@ class MoePrefill:
         Is = wsg.shape[0] // 2 if wsg is not None else 0
         self.dims = moe_dims(H, E, I, top_k, Is, 1, max_chunk, offload_slots)
         self.weights = weights  # keep alive: the plan points at them
-        if self.mxfp8:
+        if self.block_scaled:
             self.plan, self.workspace_bytes = moe_prefill_plan_mxfp8(
                 self.dims, wr.data_ptr(), wgu.data_ptr(), weights["w_gu_s"].data_ptr(), wd.data_ptr(),
                 weights["w_down_s"].data_ptr(), _ptr(wsg), _ptr(wsd), fmt=self.weight_format)
