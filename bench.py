@@ -287,6 +287,15 @@ def decoded_weights(inp, q, fmt):
     return dict(inp, w_gu=dec(q["w_gu_q"], q["w_gu_s"]), w_down=dec(q["w_down_q"], q["w_down_s"]))
 
 
+def popular_experts(expert_offsets, n):
+    """The n experts to keep resident, from a run's per-chunk expert offsets [chunks][E+1]: most chunks with rows
+    first (each such chunk would stage the expert once), then most rows, then the lower id."""
+    import numpy as np
+    rows = np.diff(np.asarray(expert_offsets, dtype=np.int64), axis=1)
+    order = np.lexsort((np.arange(rows.shape[1]), -rows.sum(0), -(rows > 0).sum(0)))
+    return [int(e) for e in order[:n]]
+
+
 def gate_up_bytes_and_flops(wl, offs_per_chunk, chunk_sizes, wb=2.0):
     """Algorithmic DRAM bytes and useful FLOPs of one gate/up launch (per chunk, averaged over the chunks):
     weights of the touched experts (wb bytes per routed weight, WEIGHT_BYTES: codes and scales)
@@ -389,10 +398,7 @@ def run_ours(args, dist: Dist):
     chunk_sizes = [min(chunk, T - c0) for c0 in range(0, T, chunk)]
     hot = []
     if wl.offload_slots and args.hot_experts > 0:
-        # popularity from the warm-up run: chunks an expert has rows in, then its rows, then the lower id
-        rows = np.diff(offs_host, axis=1)
-        order = np.lexsort((np.arange(wl.n_experts), -rows.sum(0), -(rows > 0).sum(0)))
-        hot = [int(e) for e in order[:args.hot_experts]]
+        hot = popular_experts(offs_host, args.hot_experts)
         layer.set_hot_experts(hot)
         step(x, out)  # stages the set once
         layer.raise_on_device_error()

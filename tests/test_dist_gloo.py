@@ -46,3 +46,17 @@ def test_aggregate_rate_single():
     import bench
     assert bench.aggregate_rate([50], [0.5]) == 100.0
     assert bench.aggregate_rate([10, 10, 10], [1.0, 2.0, 4.0]) == pytest.approx(7.5)
+
+
+def test_popular_experts_order():
+    """Hot-set choice from expert offsets: chunks with rows first, then rows, then the lower id."""
+    import bench
+    # 3 chunks, 5 experts: rows per (chunk, expert)
+    rows = [[0, 4, 1, 0, 2],
+            [3, 0, 1, 0, 2],
+            [0, 0, 1, 7, 0]]
+    offs = [[0] + list(__import__("itertools").accumulate(r)) for r in rows]
+    # chunks with rows: e0 1, e1 1, e2 3, e3 1, e4 2; rows: e0 3, e1 4, e2 3, e3 7, e4 4
+    assert bench.popular_experts(offs, 5) == [2, 4, 3, 1, 0]
+    assert bench.popular_experts(offs, 2) == [2, 4]
+    assert bench.popular_experts(offs, 0) == []
