@@ -171,3 +171,29 @@ def test_last_error_is_per_thread(L):
     t.join()
     assert seen["msg"] == b""
     assert L.moe_prefill_last_error() == main_msg
+
+
+def declared_parameter_counts():
+    """Number of parameters of every function the headers declare ("(void)" counts as none)."""
+    counts = {}
+    for fn in sorted(os.listdir(HEADER_DIR)):
+        if not fn.endswith(".h"):
+            continue
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(HEADER_DIR, fn)).read(), flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z0-9_]+)\s*\(([^)]*)\)\s*;",
+                             text, flags=re.M):
+            params = " ".join(m.group(2).split())
+            counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_signatures_match_the_header():
+    """The Python binding marshals every declared entry point with as many arguments as the header declares, and
+    declares nothing the header does not."""
+    from expert_major_chunked_gb300 import binding
+    counts = declared_parameter_counts()
+    assert set(counts) == set(declared_functions())
+    sigs = binding._SIGS
+    assert set(sigs) == set(counts), sorted(set(sigs) ^ set(counts))
+    for name, (argtypes, _) in sigs.items():
+        assert len(argtypes) == counts[name], (name, len(argtypes), counts[name])
