@@ -21,6 +21,10 @@ _lock = threading.Lock()
 _lib = None
 
 
+CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared", "-Wall",
+          "-Wextra"]
+
+
 def build(force: bool = False) -> str:
     """Compile oracle.c into oracle/lib/liboracle.so (gcc, OpenMP, no floating-point contraction)."""
     os.makedirs(_LIB_DIR, exist_ok=True)
@@ -28,11 +32,40 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest_src:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-           "-Wall", "-Wextra", "-o", tmp] + _SOURCES + ["-lm"]
+    cmd = ["gcc", *CFLAGS, "-o", tmp] + _SOURCES + ["-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
+
+
+def bind(L):
+    """Declare the C signatures on a loaded oracle library (this one, or a test's rebuilt copy of oracle.c)."""
+    P = ctypes.c_void_p
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    L.oracle_num_threads.restype = ctypes.c_int
+    L.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+    L.oracle_bf16_from_double.restype = ctypes.c_uint16
+    L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    L.oracle_bf16_to_double.restype = ctypes.c_double
+    L.oracle_bf16_round_array.argtypes = [P, P, i64]
+    L.oracle_router_logits.argtypes = [P, P, i64, i32, i32, P]
+    L.oracle_topk.argtypes = [P, i64, i32, i32, P, P]
+    L.oracle_swiglu_ffn.argtypes = [P, P, P, i32, i32, P, P]
+    L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, P, i64, P, i64, P, P, P, P]
+    L.oracle_permutation.argtypes = [P, i64, i32, i32, i32, P, P, P]
+    L.oracle_combine_f64.argtypes = [P, P, P, P, i64, i32, i32, P, P]
+    L.oracle_combine_f32_canonical.argtypes = [P, P, P, P, i64, i32, i32, P]
+    L.oracle_combine_tree_partial_f64.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, P]
+    L.oracle_combine_tree_finish_f64.argtypes = [P, i32, P, i64, i32, P, P]
+    L.oracle_dequant_mxfp8.argtypes = [P, P, i64, i64, P]
+    L.oracle_dequant_nvfp4.argtypes = [P, P, i64, i64, P]
+    for name in ("oracle_bf16_round_array", "oracle_router_logits", "oracle_topk", "oracle_swiglu_ffn",
+                 "oracle_moe_forward", "oracle_permutation", "oracle_combine_f64",
+                 "oracle_combine_f32_canonical", "oracle_combine_tree_partial_f64",
+                 "oracle_combine_tree_finish_f64", "oracle_dequant_mxfp8",
+                 "oracle_dequant_nvfp4"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
 
 
 def lib():
@@ -40,33 +73,7 @@ def lib():
     with _lock:
         if _lib is None:
             build()
-            L = ctypes.CDLL(_LIB_PATH)
-            P = ctypes.c_void_p
-            i32, i64 = ctypes.c_int32, ctypes.c_int64
-            L.oracle_num_threads.restype = ctypes.c_int
-            L.oracle_bf16_from_double.argtypes = [ctypes.c_double]
-            L.oracle_bf16_from_double.restype = ctypes.c_uint16
-            L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
-            L.oracle_bf16_to_double.restype = ctypes.c_double
-            L.oracle_bf16_round_array.argtypes = [P, P, i64]
-            L.oracle_router_logits.argtypes = [P, P, i64, i32, i32, P]
-            L.oracle_topk.argtypes = [P, i64, i32, i32, P, P]
-            L.oracle_swiglu_ffn.argtypes = [P, P, P, i32, i32, P, P]
-            L.oracle_moe_forward.argtypes = [P, P, P, P, P, P, P, i64, P, i64, P, P, P, P]
-            L.oracle_permutation.argtypes = [P, i64, i32, i32, i32, P, P, P]
-            L.oracle_combine_f64.argtypes = [P, P, P, P, i64, i32, i32, P, P]
-            L.oracle_combine_f32_canonical.argtypes = [P, P, P, P, i64, i32, i32, P]
-            L.oracle_combine_tree_partial_f64.argtypes = [P, P, P, P, i64, i32, i32, i32, i32, i32, P]
-            L.oracle_combine_tree_finish_f64.argtypes = [P, i32, P, i64, i32, P, P]
-            L.oracle_dequant_mxfp8.argtypes = [P, P, i64, i64, P]
-            L.oracle_dequant_nvfp4.argtypes = [P, P, i64, i64, P]
-            for name in ("oracle_bf16_round_array", "oracle_router_logits", "oracle_topk", "oracle_swiglu_ffn",
-                         "oracle_moe_forward", "oracle_permutation", "oracle_combine_f64",
-                         "oracle_combine_f32_canonical", "oracle_combine_tree_partial_f64",
-                         "oracle_combine_tree_finish_f64", "oracle_dequant_mxfp8",
-                         "oracle_dequant_nvfp4"):
-                getattr(L, name).restype = ctypes.c_int
-            _lib = L
+            _lib = bind(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 
