@@ -4,11 +4,15 @@
 #include "internal.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <memory>
 #include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 using namespace moe;
@@ -234,6 +238,78 @@ Layout make_layout(const Shape& s) {
   return L;
 }
 
+// ------------------------------------------------------------------ what a workspace holds between runs
+// Layers may share one workspace (one scratch for a whole stack of layers, or the library's built-in array of
+// moe_prefill_run_noalloc), so what a run leaves in it for later runs belongs to the workspace, not to a plan: the
+// hot set's slots and the slot map (valid only for the plan, and the hot-set version of that plan, that staged
+// them), the ring's first window staged ahead by moe_prefill_prefetch, and the points on the GPU after which the
+// last run no longer reads the ring (for a prefetch that overlaps the end of that run). One record per (device,
+// workspace address), created by the first run or prefetch that names the workspace.
+struct RingSig {  // where the ring's first window lies in a plan's layout
+  size_t ring_gu, ring_down, gu_bytes, dn_bytes;
+  int window;
+  bool operator==(const RingSig& o) const {
+    return ring_gu == o.ring_gu && ring_down == o.ring_down && gu_bytes == o.gu_bytes && dn_bytes == o.dn_bytes &&
+           window == o.window;
+  }
+};
+
+struct WsRecord {
+  uint64_t owner = 0;        // id of the plan whose run was enqueued last on the workspace (0: none known)
+  uint64_t owner_hot = 0;    // that plan's hot-set version at that run (the hot slots and slot map it left)
+  bool owner_offload = false;
+  RingSig owner_ring{};      // that run's ring layout (offloaded plans)
+  cudaEvent_t ev_end = nullptr;    // end of that run (all of its work, every stream)
+  cudaEvent_t ev_ring0 = nullptr;  // that run's last release of the ring's first half (offloaded plans)
+  bool ring0_recorded = false;
+  bool pf_pending = false;   // a prefetch was enqueued and no run has consumed or dropped it yet
+  uint64_t pf_plan = 0, pf_hot = 0;
+  cudaEvent_t ev_prefetch = nullptr;
+  uint64_t last_use = 0;
+  ~WsRecord() {
+    for (cudaEvent_t e : {ev_end, ev_ring0, ev_prefetch})
+      if (e) cudaEventDestroy(e);
+  }
+};
+
+std::mutex g_ws_mu;
+std::map<std::pair<int, uintptr_t>, std::shared_ptr<WsRecord>> g_ws;
+uint64_t g_ws_clock = 0;
+constexpr size_t kMaxWsRecords = 256;
+std::atomic<uint64_t> g_plan_ids{0};
+
+// The record of `workspace` on `device` (created, with its events, when new). With more than kMaxWsRecords
+// workspaces the least recently used record without a pending prefetch is dropped after its events have completed,
+// so forgetting it loses nothing: a later run on that workspace restages what it needs.
+moe_status ws_record(int device, const void* workspace, std::shared_ptr<WsRecord>* out) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  const auto key = std::make_pair(device, reinterpret_cast<uintptr_t>(workspace));
+  auto it = g_ws.find(key);
+  if (it == g_ws.end()) {
+    if (g_ws.size() >= kMaxWsRecords) {
+      auto victim = g_ws.end();
+      for (auto j = g_ws.begin(); j != g_ws.end(); ++j)
+        if (!j->second->pf_pending && (victim == g_ws.end() || j->second->last_use < victim->second->last_use))
+          victim = j;
+      if (victim != g_ws.end()) {
+        for (cudaEvent_t e : {victim->second->ev_end, victim->second->ev_ring0})
+          if (e && cudaEventSynchronize(e) != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "workspace record eviction: %s", cudaGetErrorString(cudaGetLastError()));
+        g_ws.erase(victim);
+      }
+    }
+    auto rec = std::make_shared<WsRecord>();
+    for (cudaEvent_t* e : {&rec->ev_end, &rec->ev_ring0, &rec->ev_prefetch}) {
+      const cudaError_t ce = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+      if (ce != cudaSuccess) return fail(MOE_ERR_CUDA, "workspace record events: %s", cudaGetErrorString(ce));
+    }
+    it = g_ws.emplace(key, std::move(rec)).first;
+  }
+  it->second->last_use = ++g_ws_clock;
+  *out = it->second;
+  return MOE_OK;
+}
+
 }  // namespace
 
 struct moe_plan {
@@ -256,15 +332,13 @@ struct moe_plan {
   // resident hot set of offloaded experts: slot of every expert (e % S, or S + its place in the set), and whether
   // the set still has to be staged into the cached workspace
   std::vector<int32_t> slot_map_host;
-  bool hot_pending = false;
+  uint64_t id = 0;            // unique over the process (a workspace record names the plan that last ran on it)
+  uint64_t hot_version = 1;   // changes with every moe_prefill_set_hot_experts (new set, new ring layout)
   // MXFP8 routed experts: w_gu / w_down hold E4M3 codes, these their E8M0 scales ([E][K/32][rows])
   const uint8_t* w_gu_scale = nullptr;
   const uint8_t* w_down_scale = nullptr;
   cudaStream_t own_copy = nullptr;
   cudaEvent_t ev_copy[2] = {}, ev_rel[2] = {};
-  // cross-layer prefetch (moe_prefill_prefetch): the first window of the next run, staged ahead on a copy stream
-  cudaEvent_t ev_prefetch = nullptr;
-  const void* prefetch_ws = nullptr;  // the workspace it was staged into (consumed by the next run)
   // Each chunk's member lists (count, scan, permute) run on a side stream so that they overlap the previous chunk's
   // GEMMs; events order the two streams (see moe_prefill_run).
   cudaStream_t side = nullptr;
@@ -389,6 +463,7 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
   if (st != MOE_OK) return st;
 
   moe_plan* p = new moe_plan();
+  p->id = ++g_plan_ids;
   p->d = *dims;
   p->sh = make_shape(*dims);
   p->sh.fmt = fmt;
@@ -456,7 +531,7 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->host_io, cudaStreamNonBlocking);
     cudaEvent_t* evs[] = {&p->ev_fork,    &p->ev_span,    &p->ev_join,    &p->ev_ready[0], &p->ev_ready[1],
                           &p->ev_down,    &p->ev_comb,    &p->ev_copy[0], &p->ev_copy[1], &p->ev_rel[0],
-                          &p->ev_rel[1],  &p->ev_x_head,  &p->ev_x_rest,  &p->ev_prefetch};
+                          &p->ev_rel[1],  &p->ev_x_head,  &p->ev_x_rest};
     for (cudaEvent_t* ev : evs)
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     if (e != cudaSuccess) st = fail(MOE_ERR_CUDA, "stream/event creation: %s", cudaGetErrorString(e));
@@ -571,13 +646,6 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       rc = encode_u8_2d(&p->tm_ring_gu, ws + L.ring_gu, ring_slots * 2 * s.I, s.H / 64 * s.cb64, s.gu_half, s.cb64);
     if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
       rc = encode_u8_2d(&p->tm_ring_down, ws + L.ring_down, ring_slots * s.H, s.I / 64 * s.cb64, s.bn_down, s.cb64);
-    // the slot map (read by the GEMMs and the staging kernel when a hot set exists), ahead of everything this run
-    // enqueues; the hot experts themselves are staged on the copy stream below
-    if (rc == MOE_OK && p->offload && s.hot > 0)
-      rc = cuda_status(cudaMemcpyAsync(ws + L.slot_map, p->slot_map_host.data(), sizeof(int32_t) * s.E,
-                                       cudaMemcpyHostToDevice, st),
-                       "slot map upload");
-    p->hot_pending = p->offload && s.hot > 0;
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;
@@ -585,9 +653,27 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     p->ws_cached = workspace;
   }
 
+  // What this workspace holds from earlier runs (of any plan) and which copies are in flight into it.
+  std::shared_ptr<WsRecord> rec;
+  rc = ws_record(p->device, workspace, &rec);
+  if (rc != MOE_OK) return rc;
+  const RingSig my_ring{L.ring_gu, L.ring_down, static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64,
+                        static_cast<size_t>(s.H) * s.I / 64 * s.cb64, s.window};
+  // The hot set's slots and the slot map are valid only if this plan, with this hot set, was the last to run here.
+  const bool stage_hot = p->offload && s.hot > 0 && !(rec->owner == p->id && rec->owner_hot == p->hot_version);
+  // A prefetch into this workspace is consumed if this plan, with this hot set, made it: only the first window's
+  // GEMMs wait for its copies. Any other run drops it, and all of that run's work waits for its copies.
+  const bool pf_waiting = rec->pf_pending;
+  const bool prefetched = pf_waiting && p->offload && rec->pf_plan == p->id && rec->pf_hot == p->hot_version;
+  rec->pf_pending = false;
+  // From here on the run may leave the workspace part-written: until it is fully enqueued, the record names no owner.
+  rec->owner = 0;
+  rec->ring0_recorded = false;
+
   // The side stream starts after everything the caller enqueued on `compute` before this call, and every return
   // after this point first makes `compute` wait for all side work (join), so the run is one unit on `compute`.
-  rc = cuda_status(cudaEventRecord(p->ev_fork, st), "fork event");
+  if (pf_waiting && !prefetched) rc = cuda_status(cudaStreamWaitEvent(st, rec->ev_prefetch, 0), "prefetch wait");
+  if (rc == MOE_OK) rc = cuda_status(cudaEventRecord(p->ev_fork, st), "fork event");
   if (rc == MOE_OK) rc = cuda_status(cudaStreamWaitEvent(side, p->ev_fork, 0), "fork wait");
   if (rc == MOE_OK && p->offload) rc = cuda_status(cudaStreamWaitEvent(cp, p->ev_fork, 0), "fork wait");
   if (rc == MOE_OK && hio) rc = cuda_status(cudaStreamWaitEvent(p->host_io, p->ev_fork, 0), "fork wait");
@@ -596,13 +682,24 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     if (cudaEventRecord(p->ev_join, side) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
     if (p->offload && cudaEventRecord(p->ev_join, cp) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
     if (hio && cudaEventRecord(p->ev_join, p->host_io) == cudaSuccess) cudaStreamWaitEvent(st, p->ev_join, 0);
+    const bool ended = cudaEventRecord(rec->ev_end, st) == cudaSuccess;
+    if (r == MOE_OK && ended) {
+      rec->owner = p->id;
+      rec->owner_hot = p->hot_version;
+      rec->owner_offload = p->offload;
+      rec->owner_ring = my_ring;
+    }
     return r;
   };
-  // A new hot set (or a new workspace): stage the hot experts into their slots once, ahead of the first window's
-  // copies on the same stream (every GEMM waits for a window's copies, so for these too).
-  if (p->hot_pending) {
-    const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64;
-    const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
+  // The hot set: upload the slot map (read by the GEMMs and the staging kernel) ahead of everything this run
+  // enqueues, and stage the hot experts into their slots on the copy stream ahead of the first window's copies
+  // (every GEMM waits for a window's copies, so for these too).
+  if (stage_hot) {
+    rc = cuda_status(cudaMemcpyAsync(ws + L.slot_map, p->slot_map_host.data(), sizeof(int32_t) * s.E,
+                                     cudaMemcpyHostToDevice, st),
+                     "slot map upload");
+    const size_t gu_bytes = my_ring.gu_bytes;
+    const size_t dn_bytes = my_ring.dn_bytes;
     for (int e = 0; rc == MOE_OK && e < s.E; ++e) {
       const int32_t slot = p->slot_map_host[e];
       if (slot < s.slots) continue;
@@ -616,15 +713,8 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
                                          dn_bytes, cudaMemcpyHostToDevice, cp),
                          "hot expert down copy");
     }
-    if (rc != MOE_OK) {
-      p->ws_cached = nullptr;  // stage again on the next run
-      return join(rc);
-    }
-    p->hot_pending = false;
+    if (rc != MOE_OK) return join(rc);
   }
-  // the first window of the first chunk was staged ahead by moe_prefill_prefetch into this workspace
-  const bool prefetched = p->offload && p->prefetch_ws == workspace;
-  p->prefetch_ws = nullptr;
   // A span is routed in two segments: its first chunk (on `compute`, before anything else) and the rest (on the
   // side stream, beside the first chunk's GEMMs). With host buffers the span's X rows go to the device in the same
   // two copies, each with its event, so each segment starts once its own rows have landed.
@@ -814,7 +904,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
       moe_status r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[hb], 0), "slot release wait");
       if (r2 == MOE_OK && prefetched && cidx == 0 && e0 == 0) {  // every expert of the window is already there
-        r2 = cuda_status(cudaStreamWaitEvent(cp, p->ev_prefetch, 0), "prefetch wait");
+        r2 = cuda_status(cudaStreamWaitEvent(cp, rec->ev_prefetch, 0), "prefetch wait");
         if (r2 == MOE_OK) r2 = cuda_status(cudaEventRecord(p->ev_copy[hb], cp), "copy event");
         return r2;
       }
@@ -883,7 +973,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       return r2;
     };
 
-    auto gemms = [&](int64_t cidx, int e0, int e1) -> moe_status {
+    auto gemms = [&](int64_t cidx, int e0, int e1, bool last_chunk) -> moe_status {
       const int par = static_cast<int>(cidx & 1);
       const int32_t* num_tiles = reinterpret_cast<const int32_t*>(ws + L.num_tiles[par]);
       const int32_t* tbase = reinterpret_cast<const int32_t*>(ws + L.tile_base[par]);
@@ -990,6 +1080,11 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       if (r2 != MOE_OK) return r2;
       if (windowed) {
         r2 = cuda_status(cudaEventRecord(p->ev_rel[hb], st), "slot release event");
+        // the run's last release of the ring's first half: a prefetch into this workspace may start after it
+        if (r2 == MOE_OK && hb == 0 && last_chunk) {
+          r2 = cuda_status(cudaEventRecord(rec->ev_ring0, st), "ring release event");
+          if (r2 == MOE_OK) rec->ring0_recorded = true;
+        }
         if (r2 != MOE_OK) return r2;
       }
       return cuda_status(cudaEventRecord(p->ev_down, st), "down event");
@@ -1048,12 +1143,13 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     if (rc == MOE_OK && hio && s0 + span < T) rc = copy_x_span(s0 + span);
     if (rc != MOE_OK) return join(rc);
     for (int64_t c0 = s0; c0 < s0 + ns; c0 += chunk, ++chunk_idx) {
+      const bool last_chunk = c0 + chunk >= T;
       if (!p->offload) {
-        rc = gemms(chunk_idx, 0, s.E);
+        rc = gemms(chunk_idx, 0, s.E, last_chunk);
       } else {
         for (int e0 = 0; rc == MOE_OK && e0 < s.E; e0 += s.window) {
           rc = copy_window(chunk_idx, e0);
-          if (rc == MOE_OK) rc = gemms(chunk_idx, e0, e0 + s.window);
+          if (rc == MOE_OK) rc = gemms(chunk_idx, e0, e0 + s.window, last_chunk);
         }
       }
       if (rc == MOE_OK && c0 + chunk < s0 + ns) rc = lists(c0 + chunk, chunk_idx + 1);
@@ -1232,9 +1328,11 @@ moe_status moe_prefill_set_hot_experts(moe_plan_t p, const int32_t* hot_ids, int
   }
   p->slot_map_host.swap(map);
   p->sh.hot = n_hot;
-  p->prefetch_ws = nullptr;  // the ring's down slots may move: a staged first window no longer counts
+  // a new version: the next run on any workspace stages the set again, and a prefetch made under the old layout
+  // (the ring's down slots may move) is dropped by that run
+  ++p->hot_version;
   p->lay = make_layout(p->sh);
-  p->ws_cached = nullptr;  // new layout: re-encode the workspace maps and stage the set on the next run
+  p->ws_cached = nullptr;  // new layout: re-encode the workspace maps
   if (workspace_bytes) *workspace_bytes = p->lay.total;
   return MOE_OK;
 }
@@ -1253,19 +1351,45 @@ moe_status moe_prefill_prefetch(moe_plan_t p, void* workspace, size_t workspace_
   const Layout& L = p->lay;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t cp = copy ? reinterpret_cast<cudaStream_t>(copy) : p->own_copy;
-  const size_t gu_bytes = static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64;
-  const size_t dn_bytes = static_cast<size_t>(s.H) * s.I / 64 * s.cb64;
-  // window 0 = experts [0, W) in slots [0, W), once the last run's use of the ring's first half is over
-  p->prefetch_ws = nullptr;
-  moe_status r = cuda_status(cudaStreamWaitEvent(cp, p->ev_rel[0], 0), "slot release wait");
-  if (r == MOE_OK)
-    r = cuda_status(cudaMemcpyAsync(ws + L.ring_gu, p->w_gu, gu_bytes * s.window, cudaMemcpyHostToDevice, cp),
+  const RingSig my_ring{L.ring_gu, L.ring_down, static_cast<size_t>(2) * s.I * s.H / 64 * s.cb64,
+                        static_cast<size_t>(s.H) * s.I / 64 * s.cb64, s.window};
+  std::shared_ptr<WsRecord> rec;
+  moe_status r = ws_record(p->device, workspace, &rec);
+  if (r != MOE_OK) return r;
+  // Window 0 = experts [0, W) into slots [0, W), once nothing enqueued earlier reads or writes those bytes: after an
+  // earlier prefetch into this workspace, and after the last run on it has read them. When that run's ring lies
+  // where this plan's does, its last release of the ring's first half is enough (the copy overlaps its tail);
+  // otherwise (another layout: the bytes may hold anything of that run) the copy waits for the end of that run.
+  if (rec->pf_pending) r = cuda_status(cudaStreamWaitEvent(cp, rec->ev_prefetch, 0), "prefetch order wait");
+  const bool same_ring = rec->owner != 0 && rec->owner_offload && rec->owner_ring == my_ring;
+  if (r == MOE_OK && same_ring && rec->ring0_recorded) {
+    r = cuda_status(cudaStreamWaitEvent(cp, rec->ev_ring0, 0), "ring release wait");
+  } else if (r == MOE_OK) {
+    // another layout, a run that failed part-way, or none known: wait for whatever was enqueued last on the workspace
+    r = cuda_status(cudaStreamWaitEvent(cp, rec->ev_end, 0), "run end wait");
+  }
+  // Under another layout these copies can land on what the last run's plan keeps here (its hot slots, its slot
+  // map): that plan must stage them again.
+  if (r == MOE_OK && rec->owner != p->id && !same_ring) rec->owner = 0;
+  bool enqueued = false;  // a copy may be in flight from here on
+  if (r == MOE_OK) {
+    r = cuda_status(cudaMemcpyAsync(ws + L.ring_gu, p->w_gu, my_ring.gu_bytes * s.window, cudaMemcpyHostToDevice, cp),
                     "prefetch gate/up copy");
+    enqueued = true;
+  }
   if (r == MOE_OK)
-    r = cuda_status(cudaMemcpyAsync(ws + L.ring_down, p->w_down, dn_bytes * s.window, cudaMemcpyHostToDevice, cp),
+    r = cuda_status(cudaMemcpyAsync(ws + L.ring_down, p->w_down, my_ring.dn_bytes * s.window, cudaMemcpyHostToDevice,
+                                    cp),
                     "prefetch down copy");
-  if (r == MOE_OK) r = cuda_status(cudaEventRecord(p->ev_prefetch, cp), "prefetch event");
-  if (r == MOE_OK) p->prefetch_ws = workspace;
+  if (enqueued) {
+    // the record's event covers every copy enqueued so far; a failed prefetch stays pending (later runs on the
+    // workspace wait for it) but no run consumes it
+    const moe_status re = cuda_status(cudaEventRecord(rec->ev_prefetch, cp), "prefetch event");
+    if (r == MOE_OK) r = re;
+    rec->pf_pending = rec->pf_pending || re == MOE_OK;
+    rec->pf_plan = r == MOE_OK ? p->id : 0;
+    rec->pf_hot = p->hot_version;
+  }
   return r;
 }
 
@@ -1309,7 +1433,7 @@ void moe_prefill_destroy(moe_plan_t p) {
   if (p->host_io) cudaStreamDestroy(p->host_io);
   for (cudaEvent_t e : {p->ev_x_head, p->ev_x_rest}) if (e) cudaEventDestroy(e);
   for (cudaEvent_t e : {p->ev_fork, p->ev_span, p->ev_join, p->ev_ready[0], p->ev_ready[1], p->ev_down, p->ev_comb,
-                        p->ev_copy[0], p->ev_copy[1], p->ev_rel[0], p->ev_rel[1], p->ev_prefetch})
+                        p->ev_copy[0], p->ev_copy[1], p->ev_rel[0], p->ev_rel[1]})
     if (e) cudaEventDestroy(e);
   if (p->side) cudaStreamDestroy(p->side);
   if (p->own_copy) cudaStreamDestroy(p->own_copy);

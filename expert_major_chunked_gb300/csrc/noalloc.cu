@@ -73,9 +73,11 @@ extern "C" moe_status moe_prefill_run_noalloc(moe_plan_t plan, const void* x, in
     moe::set_last_error(g_msg);
     return MOE_ERR_CUDA;
   }
-  // The run itself resets the status word and counters at the head of the scratch before any other work, and every
-  // other scratch byte whose value can reach an output is written earlier in the same run (stale bytes are read only
-  // as padding rows of a GEMM tile, whose results are never stored), so what the previous call left does not matter.
+  // The run itself resets the status word and counters at the head of the scratch before any other work, and writes
+  // every per-run byte whose value can reach an output earlier in the same run (stale bytes are read only as padding
+  // rows of a GEMM tile, whose results are never stored). The bytes an offloaded plan keeps between runs (its hot
+  // set's slots and slot map) are tracked per workspace address by moe_prefill_run: since every call here passes
+  // the same address, a plan that was not the last one to run on the array stages them again.
   moe_status st = moe_prefill_run(plan, x, T, chunk, scratch, MOE_NOALLOC_WORKSPACE_BYTES, out, topk_id, topk_w,
                                   expert_offsets, row_token, stream, nullptr);
   if (st != MOE_OK || !device_status) return st;

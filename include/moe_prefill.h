@@ -135,11 +135,19 @@ moe_status moe_prefill_plan_nvfp4(const moe_dims* dims, const void* w_router, co
 
 /*
  * moe_prefill_run — the layer over T tokens, in chunks of `chunk` tokens (the last chunk may be shorter).
+ * "Flash Next EXL3: exact deep prefill" (introduction): prompt rows are run expert-major in chunks of consecutive
+ * tokens; "Completed final functional audit": the output bytes are the same at chunks 256/1,024/2,048 and equal to
+ * one batched pass. Steps 1-7 of the file comment, per chunk.
  *   x               device bf16 [T][H].
  *   T               tokens (T == 0: no-op, MOE_OK).
  *   chunk           1..max_chunk tokens per chunk; chunk >= T is one single pass.
  *   workspace       device buffer of at least workspace_bytes (moe_prefill_plan), 256-byte aligned. It holds the
- *                   device error word of the most recent run; two runs must not share it concurrently.
+ *                   device error word of the most recent run. Several plans (the layers of a model) may share one
+ *                   workspace if their runs on it are ordered on the GPU (for example all on one stream); runs
+ *                   that overlap on the GPU race on it. What a run leaves in it for later runs (an offloaded
+ *                   plan's hot set and slot map, a prefetched first window) is recorded per workspace address and
+ *                   device: a run uses it only if that plan, with that hot set, put it there, and stages it again
+ *                   otherwise.
  *   out             device bf16 [T][H] (may not alias x).
  *   topk_id         device int32 [T][k] or NULL: selected expert ids per token, ascending.
  *   topk_w          device float [T][k] or NULL: their weights (same order).
@@ -149,9 +157,10 @@ moe_status moe_prefill_plan_nvfp4(const moe_dims* dims, const void* w_router, co
  *   compute         stream for all kernels.
  *   copy            resident weights: must be NULL. Offloaded experts: the stream for the host-to-device expert
  *                   copies, or NULL for one owned by the plan. For every chunk the experts are staged in windows of
- *                   S/2 consecutive experts (two copies per window: gate/up and down) into alternate halves of the
- *                   ring; a window's GEMMs wait for its copies and a copy waits until the GEMMs of the window
- *                   that last used its half have finished. Every expert is staged for every chunk.
+ *                   S/2 consecutive experts into alternate halves of the ring; a window's GEMMs wait for its copies
+ *                   and a copy waits until the GEMMs of the window that last used its half have finished. Which
+ *                   experts of a window are staged depends on the staging mode (moe_prefill_set_offload_copy): by
+ *                   default only those the chunk routes rows to; with MOE_OFFLOAD_COPY_ALL every expert.
  * Returns after enqueueing; call moe_prefill_check(workspace, compute) for device-side errors.
  */
 moe_status moe_prefill_run(moe_plan_t plan, const void* x, int64_t T, int32_t chunk, void* workspace,
@@ -177,7 +186,9 @@ moe_status moe_prefill_run_host(moe_plan_t plan, const void* x_host, int64_t T, 
                                 moe_stream_t copy);
 
 /*
- * moe_prefill_combine — the canonical combine alone (the same kernel run uses).
+ * moe_prefill_combine — the canonical combine alone (the same kernel run uses). "Flash Next EXL3: exact deep
+ * prefill" (introduction): each token's expert contributions are reduced in one canonical, fixed order, which is
+ * what makes the output independent of the chunk size; here: ascending expert id, float32, shared expert last.
  *   y          device float [R][H]: per-row expert outputs.
  *   w          device float [n][k]: weights, slot order = ascending expert id.
  *   token_row  device int32 [n][k]: row of y for each (token, slot); every value in [0, R).
@@ -254,14 +265,15 @@ moe_status moe_prefill_set_offload_copy(moe_plan_t plan, int32_t mode);
  * for plans with offload_slots > 0. Umbrella PR #1113: "Persistent expert-profile checkpoint" keeps per-expert use
  * counts as placement priors that warm resident expert lines at startup, and "Latest measured follow-up" accounts
  * the copied bytes by category (demand, initial prefetch, cross-layer prefetch); the plain reading here: the caller
- * names the most used experts (e.g. by the expert_offsets of an earlier run), they are staged once per workspace,
- * and no chunk stages them again.
+ * names the most used experts (e.g. by the expert_offsets of an earlier run), they are staged into a workspace by
+ * the first run of this plan there, and no chunk stages them again.
  *   hot_ids          host int32 [n_hot], distinct expert ids in [0, E); copied, the caller keeps ownership.
  *   n_hot            0 .. E; 0 removes the set.
  *   workspace_bytes  out (may be NULL): the workspace size later runs need (the set's slots are part of it:
  *                    n_hot x one expert's gate/up + down bytes more than without a set).
- * The hot experts are copied from the pinned banks on the copy stream at the start of the next run (and of the first
- * run on any other workspace); the routed staging kernel skips them (counted in MOE_STATS_EXPERTS_HOT) and the
+ * The hot experts are copied from the pinned banks on the copy stream at the start of the next run on a workspace,
+ * and again at the start of a later run there whenever another plan (or this plan with another set) ran on that
+ * workspace in between; the routed staging kernel skips them (counted in MOE_STATS_EXPERTS_HOT) and the
  * GEMMs read them from their slots. With MOE_OFFLOAD_COPY_ALL every window is still copied whole. Output bytes are
  * the same with and without a set. Errors: MOE_ERR_INVALID_ARG for a NULL plan, a plan without offloaded experts,
  * n_hot out of range, hot_ids NULL with n_hot > 0, an id out of range or given twice (the plan is then unchanged).
@@ -278,10 +290,13 @@ moe_status moe_prefill_set_hot_experts(moe_plan_t plan, const int32_t* hot_ids, 
  * experts move. Call it once the previous layer's run (or this plan's own last run) is enqueued.
  *   workspace, workspace_bytes  the workspace the next run of this plan will use (at least the plan's size).
  *   copy                        stream for the copies (NULL: the plan's own copy stream).
- * The copy waits for the release of the ring's first half by this plan's last run. The next run consumes the
- * prefetch if it runs on the same workspace (a run on another workspace drops it; so does
- * moe_prefill_set_hot_experts); the prefetched window is not counted in the staging statistics. Output bytes do
- * not change. Errors: MOE_ERR_INVALID_ARG (NULL plan, plan without offloaded experts, misaligned workspace, wrong
+ * The copy waits for an earlier prefetch into the same workspace and for the last run enqueued on it (of any plan):
+ * if that run's ring lies at the same place as this plan's (same sizes, slots and hot-set size), for its last
+ * release of the ring's first half, so the copy overlaps that run's tail; otherwise for its end. The next run of
+ * this plan on that workspace consumes the prefetch (its first window's GEMMs wait for these copies) unless
+ * moe_prefill_set_hot_experts was called in between; a run of any other plan there drops it, and all of that run's
+ * work waits for these copies first. The prefetched window is not counted in the staging statistics. Output bytes
+ * do not change. Not available for moe_prefill_run_noalloc (its array has no address the caller can pass). Errors: MOE_ERR_INVALID_ARG (NULL plan, plan without offloaded experts, misaligned workspace, wrong
  * device), MOE_ERR_WORKSPACE (workspace too small), MOE_ERR_CUDA.
  */
 moe_status moe_prefill_prefetch(moe_plan_t plan, void* workspace, size_t workspace_bytes, moe_stream_t copy);
@@ -321,9 +336,13 @@ const char* moe_prefill_last_error(void);
  *     with a message (use a smaller max_chunk, or moe_prefill_run).
  *   - Every GPU that loads the library holds the array until the process exits.
  *   - The array is shared by all calls on a device and keeps the last call's contents. Each run first clears the
- *     part that must start at zero (error word, counters) and writes every other byte whose value reaches an
- *     output before reading it. Calls whose work overlaps on the GPU (e.g. on different streams) race on the
- *     array: serialise them.
+ *     part that must start at zero (error word, counters) and writes the per-run bytes whose values reach an
+ *     output before reading them. What an offloaded plan keeps between runs (its hot set's slots and slot map) is
+ *     recorded as for any shared workspace: a plan whose last run here was not the last run on the array stages
+ *     them again. Calls whose work overlaps on the GPU (e.g. on different streams) race on the array: serialise
+ *     them.
+ *   - moe_prefill_prefetch and moe_prefill_check take a workspace address and so do not apply to these runs;
+ *     device_status takes the place of moe_prefill_check.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress) with that device
  *     current; make that first call before any stream capture.
  */

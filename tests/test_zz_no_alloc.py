@@ -91,3 +91,38 @@ def test_noalloc_rejects_plans_larger_than_its_array():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     assert _noalloc(L, layer.plan, dev["x"], 64, 64, out, ids, w, status) == -3
     assert b"scratch" in L.moe_prefill_last_error()
+
+
+def test_noalloc_offloaded_plans_take_turns():
+    """Two offloaded layers with different weights and different hot sets, called A, B, A, B through the built-in
+    array: each run must find its own hot experts and slot map there, not the other layer's. Each output equals the
+    same plan's run on a workspace of its own, byte for byte."""
+    from expert_major_chunked_gb300 import binding
+    L = binding.lib()
+    k, chunk, T = 4, 64, 300
+    layers, refs, xs = [], [], []
+    for seed, hot in ((11, [0, 3, 9, 17, 40]), (12, [3, 0, 50])):
+        inp = _inputs(seed, T=T, H=256, E=64, I=128, Is=128, std=0.05)
+        dev = {n: inp[n].cuda() for n in ("w_router", "ws_gu", "ws_down")}
+        host = dict(dev, w_gu=inp["w_gu"].pin_memory(), w_down=inp["w_down"].pin_memory())
+        layer = binding.MoePrefill(host, top_k=k, max_chunk=chunk, offload_slots=8)
+        layer.set_hot_experts(hot)
+        assert layer.workspace_bytes <= (64 << 20)
+        x = inp["x"].cuda()
+        ref = layer.run(x, chunk)
+        layer.raise_on_device_error()
+        layers.append(layer)
+        refs.append(ref.cpu())
+        xs.append(x)
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    for i in range(4):
+        j = i % 2
+        out = torch.empty_like(xs[j])
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        w = torch.empty((T, k), device="cuda")
+        status.fill_(-1)
+        assert _noalloc(L, layers[j].plan, xs[j], T, chunk, out, ids, w, status) == 0, binding.moe_prefill_last_error()
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        assert _close(out.cpu(), refs[j])
+        assert torch.equal(out.cpu().view(torch.int16), refs[j].view(torch.int16))
