@@ -58,6 +58,7 @@ _SIGS = {
     "moe_prefill_set_hot_experts": ([_P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
     "moe_prefill_prefetch": ([_P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "moe_prefill_forget_workspace": ([_P], ctypes.c_int),
     "moe_prefill_check": ([_P, _P], ctypes.c_int),
     "moe_prefill_destroy": ([_P], None),
     "moe_prefill_last_error": ([], ctypes.c_char_p),
@@ -171,6 +172,10 @@ def moe_prefill_set_hot_experts(plan, hot_ids) -> int:
     return ws.value
 
 
+def moe_prefill_forget_workspace(workspace):
+    _check(lib().moe_prefill_forget_workspace(workspace))
+
+
 def moe_prefill_set_combine(plan, mode: int):
     _check(lib().moe_prefill_set_combine(plan, mode))
 
@@ -276,10 +281,29 @@ class MoePrefill:
         else:
             self.plan, self.workspace_bytes = moe_prefill_plan(self.dims, wr.data_ptr(), wgu.data_ptr(),
                                                                wd.data_ptr(), _ptr(wsg), _ptr(wsd))
+        self._workspace = None
         self.workspace = torch.empty(self.workspace_bytes, dtype=torch.uint8, device=wr.device)
         self.hidden, self.n_experts, self.top_k = H, E, top_k
 
+    @property
+    def workspace(self):
+        return self._workspace
+
+    @workspace.setter
+    def workspace(self, ws):
+        # the library's record of the workspace being replaced is dropped before torch may reuse its memory
+        old = getattr(self, "_workspace", None)
+        if old is not None and old is not ws:
+            moe_prefill_forget_workspace(old.data_ptr())
+        self._workspace = ws
+
     def __del__(self):
+        ws = getattr(self, "_workspace", None)
+        if ws is not None and _lib is not None:
+            try:
+                moe_prefill_forget_workspace(ws.data_ptr())
+            except Exception:
+                pass
         plan = getattr(self, "plan", None)
         if plan:
             moe_prefill_destroy(plan)

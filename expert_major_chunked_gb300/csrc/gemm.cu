@@ -34,10 +34,14 @@ struct TileInfo {
   int cls, group, n_idx, a_row0, rows, out_row0, stream;
 };
 
-__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t) {
+// Tile t of a launch's walk over [lo, ntiles), its range of the list. The CTAs walk the range from its end: the
+// shared expert's tiles (after the routed ones in the list, and the longest ones when I_s > I) start first and the
+// last wave is made of the shortest tiles. Every tile is computed whole by one CTA, so the order changes no result.
+// The tile read is ntiles - 1 - (t - lo), in the same range.
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int t, int ntiles, int lo) {
   TileInfo ti;
   if (p.tiles != nullptr) {
-    const int4 r = __ldg(p.tiles + t);
+    const int4 r = __ldg(p.tiles + (ntiles - 1 - (t - lo)));
     const uint32_t x = static_cast<uint32_t>(r.x);
     ti.group = static_cast<int>(x & 0x7FFFu);
     ti.cls = static_cast<int>((x >> 15) & 1u);
@@ -197,8 +201,9 @@ __device__ __forceinline__ void epilogue_role(const GemmParams& p, int tfirst, i
   const int q = warp & 3;
   int local = 0;
   uint32_t blk = 0;
+  const int lo = tfirst - static_cast<int>(blockIdx.x);
   for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
-    const TileInfo ti = decode_tile(p, t);
+    const TileInfo ti = decode_tile(p, t, ntiles, lo);
     const int acc = local & 1;
     const uint32_t use = static_cast<uint32_t>(local >> 1);
     bool ok = ptx::wait_bounded(tfull0 + 8u * acc, use & 1u, p.timeout_ns, abort_flag);
@@ -389,7 +394,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         }
       }
       for (int t = tfirst; !failed && t < ntiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile(p, t, ntiles, trange.x);
         const GemmClass& C = p.cls[ti.cls];
         const void* tA = &p.tmA[ti.cls];
         const void* tB = &p.tmB[ti.cls];
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
       uint32_t phase = 0;
       bool failed = false, issued_any = false;
       for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile(p, t, ntiles, trange.x);
         const GemmClass& C = p.cls[ti.cls];
         const int acc = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -585,7 +590,7 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
       bool failed = false;
       const uint64_t pol_stream = ptx::make_policy_evict_first();
       for (int t = tfirst; !failed && t < ntiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile(p, t, ntiles, trange.x);
         const GemmClass& C = p.cls[ti.cls];
         const void* tB = &p.tmB[ti.cls];
         const uint32_t b_loads = (EPI == kEpiSwiGLU) ? 2u : 1u;
@@ -647,7 +652,7 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
       uint32_t phase = 0, issued = 0;
       bool failed = false;
       for (int t = tfirst; !failed && t < ntiles; t += gridDim.x) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile(p, t, ntiles, trange.x);
         const GemmClass& C = p.cls[ti.cls];
         const void* tA = &p.tmA[ti.cls];
         const int nA = (ti.rows + kABoxRows - 1) / kABoxRows;
@@ -688,7 +693,7 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
       uint32_t i = 0;
       bool failed = false, issued_any = false;
       for (int t = tfirst; t < ntiles; t += gridDim.x, ++local) {
-        const TileInfo ti = decode_tile(p, t);
+        const TileInfo ti = decode_tile(p, t, ntiles, trange.x);
         const GemmClass& C = p.cls[ti.cls];
         const int acc = local & 1;
         const uint32_t use = static_cast<uint32_t>(local >> 1);
@@ -741,7 +746,7 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
     uint32_t i = 0;
     bool failed = false;
     for (int t = tfirst; t < ntiles; t += gridDim.x) {
-      const TileInfo ti = decode_tile(p, t);
+      const TileInfo ti = decode_tile(p, t, ntiles, trange.x);
       const GemmClass& C = p.cls[ti.cls];
       for (int kb = 0; kb < C.kblocks; ++kb, ++i) {
         if (static_cast<int>(i % kQStagesD) != group) continue;

@@ -1393,6 +1393,23 @@ moe_status moe_prefill_prefetch(moe_plan_t p, void* workspace, size_t workspace_
   return r;
 }
 
+moe_status moe_prefill_forget_workspace(void* workspace) {
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+  int dev = -1;
+  CUDA_TRY(cudaGetDevice(&dev));
+  std::shared_ptr<WsRecord> rec;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mu);
+    auto it = g_ws.find(std::make_pair(dev, reinterpret_cast<uintptr_t>(workspace)));
+    if (it == g_ws.end()) return MOE_OK;
+    rec = it->second;
+    g_ws.erase(it);
+  }
+  // the copies and runs the record knows of finish before the caller may reuse the memory
+  for (cudaEvent_t e : {rec->ev_end, rec->ev_ring0, rec->ev_prefetch}) CUDA_TRY(cudaEventSynchronize(e));
+  return MOE_OK;
+}
+
 moe_status moe_prefill_set_combine(moe_plan_t p, int32_t mode) {
   if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
   if (mode != MOE_COMBINE_F32 && mode != MOE_COMBINE_F64_TREE)

@@ -147,7 +147,9 @@ moe_status moe_prefill_plan_nvfp4(const moe_dims* dims, const void* w_router, co
  *                   that overlap on the GPU race on it. What a run leaves in it for later runs (an offloaded
  *                   plan's hot set and slot map, a prefetched first window) is recorded per workspace address and
  *                   device: a run uses it only if that plan, with that hot set, put it there, and stages it again
- *                   otherwise.
+ *                   otherwise. The library keeps these records for the 256 most recently used workspaces; a run on
+ *                   a workspace whose record was dropped stages what it needs again. Before freeing a workspace or
+ *                   reusing its memory, call moe_prefill_forget_workspace.
  *   out             device bf16 [T][H] (may not alias x).
  *   topk_id         device int32 [T][k] or NULL: selected expert ids per token, ascending.
  *   topk_w          device float [T][k] or NULL: their weights (same order).
@@ -300,6 +302,16 @@ moe_status moe_prefill_set_hot_experts(moe_plan_t plan, const int32_t* hot_ids, 
  * device), MOE_ERR_WORKSPACE (workspace too small), MOE_ERR_CUDA.
  */
 moe_status moe_prefill_prefetch(moe_plan_t plan, void* workspace, size_t workspace_bytes, moe_stream_t copy);
+
+/*
+ * moe_prefill_forget_workspace — drop what the library remembers about `workspace` on the current device (the
+ * plan that ran there last, its hot set, a pending prefetch: see moe_prefill_run). Call it before the workspace's
+ * memory is freed or used for anything else: the records are keyed by address, so memory reused at the same address
+ * would otherwise be trusted to hold what a plan staged there. Waits (host-side) until the runs and copies the record
+ * knows of have finished. A workspace the library does not know is ignored (MOE_OK). Errors: MOE_ERR_INVALID_ARG
+ * (NULL), MOE_ERR_CUDA. No counterpart in the pages: a convenience of this library's workspace records.
+ */
+moe_status moe_prefill_forget_workspace(void* workspace);
 
 /* Combine of the layer: the float32 canonical reduction (default) or the float64 tree above. */
 enum { MOE_COMBINE_F32 = 0, MOE_COMBINE_F64_TREE = 1 };

@@ -178,3 +178,43 @@ def test_full_offload_workload_two_hot_sets_on_one_workspace(oracle_lib):
     _, ref_bf, _, _ = oracle_lib.moe_forward(inp, wl.top_k, token_idx=sample)
     max_abs, rel = compare_out(outs[-1][sample], ref_bf, oracle_lib)
     assert max_abs <= MAX_ABS and rel <= REL_L2
+
+
+def test_forgotten_workspace_is_restaged():
+    """The library remembers the most recently used workspaces (256); a plan that returns to a workspace whose record
+    was dropped, after another plan ran there, must stage its hot set again."""
+    k, T, chunk = 4, 130, 64
+    ra, oa = _pair(_weights(81), k, chunk, 8, hot=[2, 40])
+    rb, ob = _pair(_weights(82), k, chunk, 8, hot=[40, 2])
+    x = _x(83, T)
+    ref_a, ref_b = _run(ra, x, chunk), _run(rb, x, chunk)
+    ws = _share([oa, ob])
+    np.testing.assert_array_equal(_run(oa, x, chunk), ref_a)
+    np.testing.assert_array_equal(_run(ob, x, chunk), ref_b)   # B's hot set now in the shared workspace
+    # 300 other workspaces (kept alive, so that each has its own address) push the shared one's record out
+    n = oa.workspace_bytes
+    others = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in range(300)]
+    from expert_major_chunked_gb300 import binding
+    for w in others:
+        binding.moe_prefill_run(oa.plan, x.data_ptr(), T, chunk, w.data_ptr(), n, torch.empty_like(x).data_ptr())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_run(oa, x, chunk), ref_a)   # must not trust the slots it staged long ago
+    np.testing.assert_array_equal(_run(ob, x, chunk), ref_b)
+    for w in others:
+        binding.moe_prefill_forget_workspace(w.data_ptr())
+
+
+def test_forget_workspace_before_reuse():
+    """A workspace's memory reused for something else after moe_prefill_forget_workspace: the next run of the same
+    plan there stages its hot set again instead of trusting what it left."""
+    from expert_major_chunked_gb300 import binding
+    k, T, chunk = 4, 130, 64
+    ra, oa = _pair(_weights(91), k, chunk, 8, hot=[3, 9])
+    x = _x(92, T)
+    ref = _run(ra, x, chunk)
+    ws = oa.workspace
+    np.testing.assert_array_equal(_run(oa, x, chunk), ref)
+    binding.moe_prefill_forget_workspace(ws.data_ptr())
+    ws.fill_(0x7F)                          # someone else's data at the same address
+    np.testing.assert_array_equal(_run(oa, x, chunk), ref)
+    assert binding.lib().moe_prefill_forget_workspace(None) == -1
