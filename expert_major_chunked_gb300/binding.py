@@ -64,6 +64,7 @@ _SIGS = {
     "moe_prefill_last_error": ([], ctypes.c_char_p),
     "moe_prefill_set_profiling": ([_P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_kernel_times": ([_P, _P, _P], ctypes.c_int),
+    "moe_prefill_kernel_trace": ([_P, _P, _P, _P, ctypes.c_int32, _P], ctypes.c_int),
     "moe_prefill_launch_count": ([_P], ctypes.c_int64),
     "moe_prefill_set_wait_timeout": ([_P, ctypes.c_uint64], ctypes.c_int),
     "moe_prefill_run_stats": ([_P, _P, _P, ctypes.c_int32], ctypes.c_int),
@@ -198,6 +199,16 @@ def moe_prefill_kernel_times(plan):
     n = (ctypes.c_int64 * KERNEL_KINDS)()
     _check(lib().moe_prefill_kernel_times(plan, ms, n))
     return {KERNEL_NAMES[i]: (ms[i], n[i]) for i in range(KERNEL_KINDS)}
+
+
+def moe_prefill_kernel_trace(plan, capacity: int = 4096):
+    """[(kind name, start ms, end ms)] of the launches timed since the last call, in enqueue order."""
+    kinds = (ctypes.c_int32 * capacity)()
+    t0 = (ctypes.c_float * capacity)()
+    t1 = (ctypes.c_float * capacity)()
+    n = ctypes.c_int32(0)
+    _check(lib().moe_prefill_kernel_trace(plan, kinds, t0, t1, capacity, ctypes.byref(n)))
+    return [(KERNEL_NAMES[kinds[i]], t0[i], t1[i]) for i in range(min(n.value, capacity))]
 
 
 def moe_prefill_launch_count(plan) -> int:

@@ -1495,6 +1495,39 @@ moe_status moe_prefill_kernel_times(moe_plan_t p, double* ms, int64_t* launches)
   return st;
 }
 
+moe_status moe_prefill_kernel_trace(moe_plan_t p, int32_t* kinds, float* start_ms, float* end_ms, int32_t capacity,
+                                    int32_t* count) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (capacity < 0 || (capacity > 0 && (!kinds || !start_ms || !end_ms)) || !count)
+    return fail(MOE_ERR_INVALID_ARG, "output arrays missing");
+  moe_status st = MOE_OK;
+  int32_t n = 0;
+  cudaEvent_t origin = nullptr;
+  for (auto& t : p->pending) {
+    if (t.a && t.b) {
+      cudaError_t e = cudaEventSynchronize(t.b);
+      if (!origin) origin = t.a;
+      float t0 = 0.0f, t1 = 0.0f;
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&t0, origin, t.a);
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&t1, origin, t.b);
+      if (e != cudaSuccess && st == MOE_OK) st = fail(MOE_ERR_CUDA, "event timing: %s", cudaGetErrorString(e));
+      if (n < capacity) {
+        kinds[n] = t.kind;
+        start_ms[n] = t0;
+        end_ms[n] = t1;
+      }
+      ++n;
+    }
+  }
+  for (auto& t : p->pending) {
+    if (t.a) p->pool.push_back(t.a);
+    if (t.b) p->pool.push_back(t.b);
+  }
+  p->pending.clear();
+  *count = n;
+  return st;
+}
+
 int64_t moe_prefill_launch_count(moe_plan_t p) { return p ? p->launches : 0; }
 
 moe_status moe_prefill_set_wait_timeout(moe_plan_t p, uint64_t timeout_ns) {

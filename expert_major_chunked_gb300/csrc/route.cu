@@ -36,17 +36,26 @@ __device__ __forceinline__ int warp_sum_i(int v) {
   return v;
 }
 
-// Sum of squares of a bf16 row in fp32 (8 elements per lane per step; H is a multiple of 64).
+// Sum of squares of a bf16 row in fp32 (8 elements per lane per step; H is a multiple of 64). The loads of up to 8
+// steps are issued before their arithmetic, so a row costs about one memory round trip, not one per step.
 __device__ __forceinline__ float row_sumsq(const uint16_t* row, int H, int lane) {
   float ss = 0.0f;
-  for (int i = lane * 8; i < H; i += 256) {
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + i));
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  for (int i0 = lane * 8; i0 < H; i0 += 8 * 256) {
+    uint4 q[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
+    for (int m = 0; m < 8; ++m) {
+      const int i = i0 + 256 * m;
+      q[m] = i < H ? __ldg(reinterpret_cast<const uint4*>(row + i)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const uint32_t w[4] = {q[m].x, q[m].y, q[m].z, q[m].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
+      }
     }
   }
   return warp_sum(ss);
@@ -360,54 +369,43 @@ __device__ __forceinline__ double band_bound(int H, double u) {
 }
 
 template <int EPL>
-__global__ void __launch_bounds__(256, 2) topk_kernel(RouteParams p) {
-  __shared__ BandScratch band_scratch[8];
+__global__ void __launch_bounds__(256) topk_kernel(RouteParams p) {
+  __shared__ float wm_warp[8];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int t = blockIdx.x * 8 + warp;
-  if (t >= p.n) return;
   const int E = p.E, k = p.k, H = p.H;
+  // max_e ||w_e|| once per block (every thread of the block loads a few norms at once)
+  float wm = 0.0f;
+  for (int e = threadIdx.x; e < E; e += 256) wm = fmaxf(wm, p.wnorm[e]);
+  wm = warp_max(wm);
+  if (lane == 0) wm_warp[warp] = wm;
+  __syncthreads();
+  wm = wm_warp[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) wm = fmaxf(wm, wm_warp[i]);
+  if (t >= p.n) return;
   float v[EPL];
   load_logits(p.logits + static_cast<int64_t>(t) * E, E, lane, v);
   const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
   const float xnorm = sqrtf(row_sumsq(xrow, H, lane)) * 1.001f;
-  float wm = 0.0f;
-  for (int e = lane; e < E; e += 32) wm = fmaxf(wm, p.wnorm[e]);
-  wm = warp_max(wm);
   const double tau = static_cast<double>(p.tau_coef) * static_cast<double>(xnorm) * static_cast<double>(wm);
   uint32_t sel;
   float vk, vk1;
   select_top(v, E, k, lane, &sel, &vk, &vk1);
   int flag = 0;
   if ((k < E) && !(static_cast<double>(vk) - static_cast<double>(vk1) > 2.0 * tau)) {
-    // not certain: try to decide the last places on float sums of the exact products
-    BandScratch& B = band_scratch[warp];
-    uint32_t sure, cand;
-    int cidx[EPL];
-    int need;
-    const int ncand = band_candidates(v, E, k, lane, tau, vk, vk1, B, &sure, &cand, cidx, &need);
-    int certified = 0;
-    if (ncand <= kMaxCand) {
-      band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);
-      if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-24));
-      certified = __shfl_sync(0xffffffffu, certified, 0);
-    }
-    if (certified) {
-      sel = sure | chosen_mask(B, cand, cidx);
-      flag = 1;
-      if (lane == 0) atomicAdd(&p.hdr->band_levels[0], 1);  // diagnostic counter only
-    } else {
-      flag = 2;  // band_kernel decides this token
-      if (lane == 0) p.band_info[t] = BandInfo{tau, static_cast<double>(vk), static_cast<double>(vk1), 0.0};
-    }
-    __syncwarp();
+    // not certain: band_kernel decides the last places of this token
+    flag = 2;
+    if (lane == 0) p.band_info[t] = BandInfo{tau, static_cast<double>(vk), static_cast<double>(vk1), 0.0};
   }
   if (flag != 2) write_selection(p, t, lane, sel, v);
   if (lane == 0) p.band_flag[t] = static_cast<uint8_t>(flag);
 }
 
-// Tokens the float sums could not decide (flag 2), on double sums and, when those cannot separate the last places
-// either, on the sequential float64 sums themselves (the reference definition, bit for bit). A grid of one CTA per
-// SM strides over the chunk's tokens.
+// Tokens whose fp32 selection was not certain (flag 2): their last places are decided on float sums of the exact
+// products, then, when those cannot separate them, on double sums, and finally on the sequential float64 sums
+// themselves (the reference definition, bit for bit). A grid of one CTA per SM strides over the chunk's tokens, so
+// the few flagged tokens (a few percent) are spread over every SM and the top-k kernel stays light.
 template <int EPL>
 __global__ void __launch_bounds__(256) band_kernel(RouteParams p) {
   __shared__ BandScratch band_scratch[8];
@@ -426,12 +424,19 @@ __global__ void __launch_bounds__(256) band_kernel(RouteParams p) {
     const int ncand = band_candidates(v, E, k, lane, bi.tau, bi.vk, bi.vk1, B, &sure, &cand, cidx, &need);
     uint32_t chosen = 0;
     if (ncand <= kMaxCand) {
-      band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);  // S for the bounds
-      band_values<double>(B, ncand, xrow, p.w_router, H, lane, false);
+      // level 0: float sums of the exact products (also S for every level's bound)
+      band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);
       int certified = 0;
-      if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-53));
+      if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-24));
       certified = __shfl_sync(0xffffffffu, certified, 0);
-      int level = 1;
+      int level = 0;
+      if (!certified) {
+        // level 1: double sums
+        level = 1;
+        band_values<double>(B, ncand, xrow, p.w_router, H, lane, false);
+        if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-53));
+        certified = __shfl_sync(0xffffffffu, certified, 0);
+      }
       if (!certified) {
         level = 2;
         for (int c = lane; c < ncand; c += 32)
@@ -512,9 +517,10 @@ __global__ void __launch_bounds__(kCountWarps * 32) count_kernel(PermuteParams p
   if (lane == 0) p.block_band[b] = __popc(bb);
 }
 
-// Exclusive scan across a block of 1024 threads; returns the thread's exclusive prefix, *total gets the sum.
+// Exclusive scan across the block (blockDim.x a multiple of 32, at most 1024); returns the thread's exclusive prefix,
+// *total gets the sum.
 __device__ int block_exclusive_scan(int v, int* total, int* smem32) {
-  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32, warp = threadIdx.x / 32, nwarps = blockDim.x / 32;
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -525,7 +531,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* smem32) {
   if (lane == 31) smem32[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    const int ws = smem32[lane];
+    const int ws = lane < nwarps ? smem32[lane] : 0;
     int wi = ws;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -542,73 +548,95 @@ __device__ int block_exclusive_scan(int v, int* total, int* smem32) {
   return r;
 }
 
-// One CTA of 1024 threads, thread e = expert e: per-expert totals, expert offsets, per-(block, expert) row bases,
-// and the tile lists of the gate/up and down GEMMs (expert-major: expert, then N tile, then M tile).
-__global__ void __launch_bounds__(1024) scan_tiles_kernel(PermuteParams p) {
-  __shared__ int sm[33];
-  const int e = threadIdx.x;
-  const int E = p.E, nblk = p.nblk;
-  // pass 1: per-expert totals; thread e reads column e of counts[nblk][E] (coalesced across the warp), 16 blocks
-  // per batch so that 16 loads are in flight per thread
+// Column e of counts[nblk][E] (coalesced across the warp), 16 blocks per batch so that 16 loads are in flight.
+__device__ __forceinline__ int column_total(const int32_t* counts, int e, int E, int nblk) {
   int total = 0;
-  if (e < E) {
-    for (int b0 = 0; b0 < nblk; b0 += 16) {
-      int c[16];
+  for (int b0 = 0; b0 < nblk; b0 += 16) {
+    int c[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? p.counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
+    for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) total += c[j];
+    for (int j = 0; j < 16; ++j) total += c[j];
+  }
+  return total;
+}
+
+// Row base of every (block, expert e): off + the counts of the earlier blocks.
+__device__ __forceinline__ void column_bases(const int32_t* counts, int32_t* base, int e, int E, int nblk, int off) {
+  int run = off;
+  for (int b0 = 0; b0 < nblk; b0 += 16) {
+    int c[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (b0 + j < nblk) base[static_cast<int64_t>(b0 + j) * E + e] = run;
+      run += c[j];
     }
   }
+}
+
+// One CTA of 512 threads; thread i owns experts 2i and 2i + 1 (contiguous, so one scan value covers both): per-expert
+// totals, expert offsets, per-(block, expert) row bases, and the tile lists of the gate/up and down GEMMs
+// (expert-major: expert, then N tile, then M tile). 512 threads of at most 64 registers leave room on an SM for a
+// GEMM CTA beside it: this kernel runs while the previous chunk's GEMMs hold every SM.
+constexpr int kScanThreads = 512;
+__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(PermuteParams p) {
+  __shared__ int sm[33];
+  const int E = p.E, nblk = p.nblk;
+  const int e0 = 2 * static_cast<int>(threadIdx.x);
+  int tot[2] = {0, 0};
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    if (e0 + h < E) tot[h] = column_total(p.counts, e0 + h, E, nblk);
   int R = 0;
-  const int off = block_exclusive_scan(e < E ? total : 0, &R, sm);
-  if (e < E) {
-    p.offsets[e] = off;
-    if (p.offsets_out) p.offsets_out[e] = off;
-    // pass 2: row base of every (block, expert)
-    int run = off;
-    for (int b0 = 0; b0 < nblk; b0 += 16) {
-      int c[16];
+  const int off0 = block_exclusive_scan(tot[0] + tot[1], &R, sm);
+  const int off[2] = {off0, off0 + tot[0]};
 #pragma unroll
-      for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? p.counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        if (b0 + j < nblk) p.base[static_cast<int64_t>(b0 + j) * E + e] = run;
-        run += c[j];
-      }
-    }
+  for (int h = 0; h < 2; ++h) {
+    const int e = e0 + h;
+    if (e >= E) continue;
+    p.offsets[e] = off[h];
+    if (p.offsets_out) p.offsets_out[e] = off[h];
+    column_bases(p.counts, p.base, e, E, nblk, off[h]);
   }
-  if (e == 0) {
+  if (threadIdx.x == 0) {
     p.offsets[E] = R;
     if (p.offsets_out) p.offsets_out[E] = R;
   }
-  const int mt = (e < E) ? (total + kBlockM - 1) / kBlockM : 0;
+  int mt[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) mt[h] = (e0 + h < E) ? (tot[h] + kBlockM - 1) / kBlockM : 0;
   int n_gu = 0, n_dn = 0;
-  const int gu_base = block_exclusive_scan(mt * p.nt_gu, &n_gu, sm);
-  const int dn_base = block_exclusive_scan(mt * p.nt_down, &n_dn, sm);
+  const int gu0 = block_exclusive_scan((mt[0] + mt[1]) * p.nt_gu, &n_gu, sm);
+  const int dn0 = block_exclusive_scan((mt[0] + mt[1]) * p.nt_down, &n_dn, sm);
+  const int gu_base[2] = {gu0, gu0 + mt[0] * p.nt_gu};
+  const int dn_base[2] = {dn0, dn0 + mt[0] * p.nt_down};
   const int mts = (p.n + kBlockM - 1) / kBlockM;
   const int n_gu_all = n_gu + (p.nt_gu_shared > 0 ? mts * p.nt_gu_shared : 0);
   const int n_dn_all = n_dn + (p.nt_down_shared > 0 ? mts * p.nt_down_shared : 0);
   const bool fits = n_gu_all <= p.cap_gu && n_dn_all <= p.cap_down;
-  if (e < E) {
-    p.tile_base[e] = gu_base;
-    p.tile_base[E + 1 + e] = dn_base;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int e = e0 + h;
+    if (e >= E) continue;
+    p.tile_base[e] = gu_base[h];
+    p.tile_base[E + 1 + e] = dn_base[h];
+    if (!fits) continue;
+    // an expert with a single M tile is the only reader of its weight tiles: mark them for streaming
+    const int stream = (mt[h] == 1) ? static_cast<int>(1u << 31) : 0;
+    for (int nn = 0; nn < p.nt_gu; ++nn)
+      for (int m = 0; m < mt[h]; ++m)
+        p.tiles_gu[gu_base[h] + nn * mt[h] + m] = make_int4(e | (nn << 16) | stream, off[h] + m * kBlockM,
+                                                            min(kBlockM, tot[h] - m * kBlockM), off[h] + m * kBlockM);
+    for (int nn = 0; nn < p.nt_down; ++nn)
+      for (int m = 0; m < mt[h]; ++m)
+        p.tiles_down[dn_base[h] + nn * mt[h] + m] = make_int4(e | (nn << 16) | stream, off[h] + m * kBlockM,
+                                                              min(kBlockM, tot[h] - m * kBlockM), off[h] + m * kBlockM);
   }
   if (threadIdx.x == 0) {
     p.tile_base[E] = n_gu;
     p.tile_base[E + 1 + E] = n_dn;
-  }
-  if (fits && e < E) {
-    // an expert with a single M tile is the only reader of its weight tiles: mark them for streaming
-    const int stream = (mt == 1) ? static_cast<int>(1u << 31) : 0;
-    for (int nn = 0; nn < p.nt_gu; ++nn)
-      for (int m = 0; m < mt; ++m)
-        p.tiles_gu[gu_base + nn * mt + m] = make_int4(e | (nn << 16) | stream, off + m * kBlockM,
-                                                      min(kBlockM, total - m * kBlockM), off + m * kBlockM);
-    for (int nn = 0; nn < p.nt_down; ++nn)
-      for (int m = 0; m < mt; ++m)
-        p.tiles_down[dn_base + nn * mt + m] = make_int4(e | (nn << 16) | stream, off + m * kBlockM,
-                                                        min(kBlockM, total - m * kBlockM), off + m * kBlockM);
   }
   if (fits) {
     // shared expert (class 1): gate/up reads the chunk's rows of X, down reads the shared h rows
@@ -707,7 +735,7 @@ cudaError_t launch_count(const PermuteParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_scan_tiles(const PermuteParams& p, cudaStream_t stream) {
-  scan_tiles_kernel<<<1, 1024, 0, stream>>>(p);
+  scan_tiles_kernel<<<1, kScanThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -388,6 +388,13 @@ moe_status moe_prefill_set_profiling(moe_plan_t plan, int32_t enable);
    of launches timed since the last call (arrays of MOE_KERNEL_KINDS entries; either may be NULL). Clears them. */
 moe_status moe_prefill_kernel_times(moe_plan_t plan, double* ms, int64_t* launches);
 
+/* The launches timed since the last call (profiling enabled), in the order they were enqueued: kind, start and end
+   in milliseconds from the start of the first one (CUDA events on each launch's stream). Writes min(count,
+   capacity) entries, sets *count to the number of timed launches, synchronises on the events and clears them (as
+   moe_prefill_kernel_times does). */
+moe_status moe_prefill_kernel_trace(moe_plan_t plan, int32_t* kinds, float* start_ms, float* end_ms, int32_t capacity,
+                                    int32_t* count);
+
 /* Total kernels launched by this plan since it was created. */
 int64_t moe_prefill_launch_count(moe_plan_t plan);
 
