@@ -576,50 +576,49 @@ __device__ __forceinline__ void column_bases(const int32_t* counts, int32_t* bas
   }
 }
 
-// One CTA of 512 threads; thread i owns experts 2i and 2i + 1 (contiguous, so one scan value covers both): per-expert
-// totals, expert offsets, per-(block, expert) row bases, and the tile lists of the gate/up and down GEMMs
-// (expert-major: expert, then N tile, then M tile). 512 threads of at most 64 registers leave room on an SM for a
-// GEMM CTA beside it: this kernel runs while the previous chunk's GEMMs hold every SM.
+// One CTA of 512 threads; thread i owns expert i and, when E > 512, expert i + 512: per-expert totals, expert offsets,
+// per-(block, expert) row bases, and the tile lists of the gate/up and down GEMMs (expert-major: expert, then N tile,
+// then M tile). 512 threads of at most 64 registers leave room on an SM for a GEMM CTA beside it: this kernel runs
+// while the previous chunk's GEMMs hold every SM.
 constexpr int kScanThreads = 512;
-__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(PermuteParams p) {
+__global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermuteParams p) {
   __shared__ int sm[33];
   const int E = p.E, nblk = p.nblk;
-  const int e0 = 2 * static_cast<int>(threadIdx.x);
-  int tot[2] = {0, 0};
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-    if (e0 + h < E) tot[h] = column_total(p.counts, e0 + h, E, nblk);
-  int R = 0;
-  const int off0 = block_exclusive_scan(tot[0] + tot[1], &R, sm);
-  const int off[2] = {off0, off0 + tot[0]};
+  const int halves = (E + kScanThreads - 1) / kScanThreads;  // 1, or 2 for E > 512
+  int tot[2] = {0, 0}, off[2] = {0, 0}, mt[2] = {0, 0}, gu_base[2] = {0, 0}, dn_base[2] = {0, 0};
+  int R = 0, n_gu = 0, n_dn = 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int e = e0 + h;
-    if (e >= E) continue;
-    p.offsets[e] = off[h];
-    if (p.offsets_out) p.offsets_out[e] = off[h];
-    column_bases(p.counts, p.base, e, E, nblk, off[h]);
+    if (h >= halves) break;
+    const int e = static_cast<int>(threadIdx.x) + h * kScanThreads;
+    if (e < E) tot[h] = column_total(p.counts, e, E, nblk);
+    // exclusive scans over the experts of this half, after those of the half before
+    int sum = 0;
+    off[h] = R + block_exclusive_scan(tot[h], &sum, sm);
+    R += sum;
+    mt[h] = (e < E) ? (tot[h] + kBlockM - 1) / kBlockM : 0;
+    gu_base[h] = n_gu + block_exclusive_scan(mt[h] * p.nt_gu, &sum, sm);
+    n_gu += sum;
+    dn_base[h] = n_dn + block_exclusive_scan(mt[h] * p.nt_down, &sum, sm);
+    n_dn += sum;
   }
   if (threadIdx.x == 0) {
     p.offsets[E] = R;
     if (p.offsets_out) p.offsets_out[E] = R;
+    p.tile_base[E] = n_gu;
+    p.tile_base[E + 1 + E] = n_dn;
   }
-  int mt[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) mt[h] = (e0 + h < E) ? (tot[h] + kBlockM - 1) / kBlockM : 0;
-  int n_gu = 0, n_dn = 0;
-  const int gu0 = block_exclusive_scan((mt[0] + mt[1]) * p.nt_gu, &n_gu, sm);
-  const int dn0 = block_exclusive_scan((mt[0] + mt[1]) * p.nt_down, &n_dn, sm);
-  const int gu_base[2] = {gu0, gu0 + mt[0] * p.nt_gu};
-  const int dn_base[2] = {dn0, dn0 + mt[0] * p.nt_down};
   const int mts = (p.n + kBlockM - 1) / kBlockM;
   const int n_gu_all = n_gu + (p.nt_gu_shared > 0 ? mts * p.nt_gu_shared : 0);
   const int n_dn_all = n_dn + (p.nt_down_shared > 0 ? mts * p.nt_down_shared : 0);
   const bool fits = n_gu_all <= p.cap_gu && n_dn_all <= p.cap_down;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int e = e0 + h;
-    if (e >= E) continue;
+    const int e = static_cast<int>(threadIdx.x) + h * kScanThreads;
+    if (h >= halves || e >= E) continue;
+    p.offsets[e] = off[h];
+    if (p.offsets_out) p.offsets_out[e] = off[h];
+    column_bases(p.counts, p.base, e, E, nblk, off[h]);
     p.tile_base[e] = gu_base[h];
     p.tile_base[E + 1 + e] = dn_base[h];
     if (!fits) continue;
@@ -633,10 +632,6 @@ __global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(PermuteParams 
       for (int m = 0; m < mt[h]; ++m)
         p.tiles_down[dn_base[h] + nn * mt[h] + m] = make_int4(e | (nn << 16) | stream, off[h] + m * kBlockM,
                                                               min(kBlockM, tot[h] - m * kBlockM), off[h] + m * kBlockM);
-  }
-  if (threadIdx.x == 0) {
-    p.tile_base[E] = n_gu;
-    p.tile_base[E + 1 + E] = n_dn;
   }
   if (fits) {
     // shared expert (class 1): gate/up reads the chunk's rows of X, down reads the shared h rows
