@@ -181,7 +181,8 @@ def load_peaks() -> dict:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("expert_major_chunked_gb300/csrc/gemm.cu", "expert_major_chunked_gb300/csrc/ptx.cuh",
+    for rel in ("expert_major_chunked_gb300/csrc/gemm.cu", "expert_major_chunked_gb300/csrc/gemm_pair.cu",
+                "expert_major_chunked_gb300/csrc/swiglu.cuh", "expert_major_chunked_gb300/csrc/ptx.cuh",
                 "expert_major_chunked_gb300/csrc/internal.h", "expert_major_chunked_gb300/csrc/route.cu"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())

@@ -54,6 +54,8 @@ _SIGS = {
     "moe_prefill_combine_f64": ([_P, _P, _P, _P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                  _P, _P, _P], ctypes.c_int),
     "moe_prefill_set_combine": ([_P, ctypes.c_int32], ctypes.c_int),
+    "moe_prefill_set_cta_pairs": ([_P, ctypes.c_int32], ctypes.c_int),
+    "moe_prefill_cta_pairs": ([_P], ctypes.c_int32),
     "moe_prefill_set_offload_copy": ([_P, ctypes.c_int32], ctypes.c_int),
     "moe_prefill_set_hot_experts": ([_P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32,
                                      ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
@@ -179,6 +181,17 @@ def moe_prefill_forget_workspace(workspace):
 
 def moe_prefill_set_combine(plan, mode: int):
     _check(lib().moe_prefill_set_combine(plan, mode))
+
+
+PAIRS_GATE_UP, PAIRS_DOWN = 1, 2
+
+
+def moe_prefill_set_cta_pairs(plan, which: int):
+    _check(lib().moe_prefill_set_cta_pairs(plan, int(which)))
+
+
+def moe_prefill_cta_pairs(plan) -> int:
+    return int(lib().moe_prefill_cta_pairs(plan))
 
 
 def moe_prefill_check(workspace, stream=None) -> int:
@@ -353,6 +366,16 @@ class MoePrefill:
     def set_combine(self, mode: int):
         """COMBINE_F32 (canonical float32, ascending expert id; default) or COMBINE_F64_TREE."""
         moe_prefill_set_combine(self.plan, mode)
+
+    @property
+    def cta_pairs(self) -> int:
+        """Mask of the projections on CTA pairs (PAIRS_GATE_UP | PAIRS_DOWN; PAIRS_GATE_UP by default where the
+        dimensions allow it); settable."""
+        return moe_prefill_cta_pairs(self.plan)
+
+    @cta_pairs.setter
+    def cta_pairs(self, which: int):
+        moe_prefill_set_cta_pairs(self.plan, which)
 
     def run_host(self, x_host, chunk: int, x_dev, out_dev, out_host, topk_id=None, topk_w=None,
                  expert_offsets=None, row_token=None, stream=None, copy_stream=None):

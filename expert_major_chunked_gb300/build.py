@@ -18,8 +18,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmoe_prefill.so")
-SOURCES = ["gemm.cu", "route.cu", "combine.cu", "combine_f64.cu", "ring.cu", "moe_prefill.cu", "noalloc.cu"]
-HEADERS = ["internal.h", "ptx.cuh"]
+SOURCES = ["gemm.cu", "gemm_pair.cu", "route.cu", "combine.cu", "combine_f64.cu", "ring.cu", "moe_prefill.cu", "noalloc.cu"]
+HEADERS = ["internal.h", "ptx.cuh", "swiglu.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 _lock = threading.Lock()
 

@@ -23,6 +23,7 @@
 // accumulation order is that of the bf16 path. Warp 14 issues the activation loads.
 #include "internal.h"
 #include "ptx.cuh"
+#include "swiglu.cuh"
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -81,17 +82,6 @@ __device__ __forceinline__ int2 tile_range(const GemmParams& p) {
 __device__ __forceinline__ void raise_error(const GemmParams& p, volatile int* abort_flag, int site) {
   *abort_flag = 1;
   atomicCAS(p.err, 0, dev_error_code(kDevErrTimeout, site, static_cast<int>(blockIdx.x)));
-}
-
-__device__ __forceinline__ float swiglu(float g, float u) {
-  // silu(g) * u with silu(z) = z / (1 + exp(-z)); IEEE-rounded division and products.
-  const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-  return __fmul_rn(s, u);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Where a group's B rows live: the group itself (resident weights), its ring slot e % b_group_mod (offloaded
@@ -358,9 +348,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&p.tmA[0]);
-    ptx::tma_prefetch_desc(&p.tmB[0]);
     ptx::tma_prefetch_desc(&p.tmA[1]);
-    ptx::tma_prefetch_desc(&p.tmB[1]);
+    ptx::tma_prefetch_desc(EPI == kEpiSwiGLU ? &p.tmBg[0] : &p.tmB[0]);
+    ptx::tma_prefetch_desc(EPI == kEpiSwiGLU ? &p.tmBg[1] : &p.tmB[1]);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 2 * kMaxN);
@@ -403,7 +393,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
         const uint32_t bytes = static_cast<uint32_t>(nA * kABoxRows * 128) + b_loads * C.b_box_rows * 128u;
         const int slot = b_slot(C, ti.group);
         const int b_row0 = tile_b_row<EPI>(C, slot, ti.n_idx);
-        const int b_row1 = b_row0 + C.b_up_offset;
         for (int kb = 0; kb < C.kblocks; ++kb) {
           if (!ptx::wait_bounded(empty0 + 8u * stage, phase ^ 1u, tmo, abort_flag)) {
             raise_error(p, abort_flag, kSiteProducerEmpty);
@@ -417,12 +406,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) grouped_gemm_kernel(const __g
           const int kc = kb * kBlockK;
           for (int j = 0; j < nA; ++j)
             ptx::tma_load_2d(a_dst + j * (kABoxRows * 128), tA, kc, ti.a_row0 + j * kABoxRows, fb);
-          if (C.b_stream && ti.stream) {
+          const bool stream = C.b_stream && ti.stream;
+          if (EPI == kEpiSwiGLU) {
+            // the tile's gate rows and up rows in one box of the (K, j, 2 x slot + half) view, gate rows first
+            const void* tBg = &p.tmBg[ti.cls];
+            const int j0 = ti.n_idx * C.b_box_rows;
+            if (stream)
+              ptx::tma_load_3d_hint(b_dst, tBg, kc, j0, 2 * slot, fb, pol_stream);
+            else
+              ptx::tma_load_3d(b_dst, tBg, kc, j0, 2 * slot, fb);
+          } else if (stream) {
             ptx::tma_load_2d_hint(b_dst, tB, kc, b_row0, fb, pol_stream);
-            if (EPI == kEpiSwiGLU) ptx::tma_load_2d_hint(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb, pol_stream);
           } else {
             ptx::tma_load_2d(b_dst, tB, kc, b_row0, fb);
-            if (EPI == kEpiSwiGLU) ptx::tma_load_2d(b_dst + C.b_box_rows * 128, tB, kc, b_row1, fb);
           }
           ++issued;
           if (++stage == kStages) {

@@ -47,7 +47,9 @@ constexpr int kBlockM = 128;        // UMMA M (rows of a tile)
 constexpr int kBlockK = 64;         // bf16 elements per 128-byte swizzle row
 constexpr int kStages = 4;          // smem pipeline depth
 constexpr int kMaxN = 256;          // widest UMMA N (TMEM columns per accumulator)
-constexpr int kABoxRows = 32;       // A rows per TMA box (a tile loads ceil(rows/32) boxes)
+// A rows per TMA box: a tile's rows in one box (rows past the tile are loaded and not used). A stage costs about the
+// same per TMA operation whatever the box size, so fewer, larger boxes make a stage shorter.
+constexpr int kABoxRows = 128;
 constexpr int kGemmThreads = 192;   // warp 0 TMA, warp 1 MMA + TMEM alloc, warps 2..5 epilogue
 constexpr int kStageABytes = kBlockM * kBlockK * 2;   // 16 KB
 constexpr int kStageBBytes = kMaxN * kBlockK * 2;     // 32 KB
@@ -105,6 +107,8 @@ struct GemmClass {
 struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
+  CUtensorMap tmBg[2];        // SwiGLU, bf16 weights: the fused gate/up weights as (K, I, 2 x groups), box 64 x
+                              // b_box_rows x 2: a tile's gate rows and up rows in one load
   CUtensorMap tmOut[2];       // F32 outputs with out_tma != 0: fp32 [rows][out_ld] map, box 32 x 32, 128B swizzle
   GemmClass cls[2];
   const int4* tiles;          // device tile list (nullptr: dense mode)
@@ -119,6 +123,67 @@ struct GemmParams {
   const int32_t* stall_flag;  // test hook: producer waits for *stall_flag != 0 before any load (nullptr: none)
   uint64_t timeout_ns;        // bound on every mbarrier wait
 };
+
+// CTA-pair grouped GEMM (grouped_pair_kernel, gemm_pair.cu): a cluster of two CTAs computes one tile with
+// tcgen05.mma.cta_group::2, M = 256 rows of weights (128 in each CTA's shared memory and TMEM lanes) times N tokens
+// (N = the tile's token count rounded up to 32, at most 256; each CTA loads N/2 of the token rows). The output is
+// the transpose of the single-CTA kernel's tile: TMEM lane = weight row (an output column), TMEM column = token.
+constexpr int kPairStages = 6;
+constexpr int kPairWBoxRows = 64;         // gate/up: 64 gate and 64 up rows per CTA in one 3-D box
+constexpr int kPairDownBoxRows = 128;     // down: 128 weight rows per CTA in one box
+constexpr int kPairTBoxRows = 128;        // token rows per box (one box: a CTA's N/2 <= 128 rows, and the rest unused)
+constexpr int kPairTBoxRowsSmall = 32;    // token rows per box for tiles with N/2 <= 32
+constexpr int kPairMaxTokens = 256;       // UMMA N limit
+constexpr int kPairStageWBytes = 128 * kBlockK * 2;                  // 16 KB: 128 weight rows
+constexpr int kPairStageTBytes = (kPairMaxTokens / 2) * kBlockK * 2; // 16 KB: up to 128 token rows
+constexpr int kPairThreads = 320;          // warp 0 TMA, warp 1 MMA (+ TMEM alloc), warps 2..9 epilogue (two groups)
+constexpr int kPairXchgBytes = 2 * 8192;   // per epilogue group: a 16-column slice staged in shared memory
+constexpr int kPairSmemBytes = 1024 /*align slack*/ + kPairStages * (kPairStageWBytes + kPairStageTBytes) +
+                               kBarRegionBytes + kPairXchgBytes;
+static_assert(kPairSmemBytes <= 215040, "shared memory per CTA");
+
+// Token tiles of an expert with `rows` member rows: ceil(rows / 256) tiles of equal width rounded up to 32.
+__host__ __device__ inline int pair_tile_width(int rows) {
+  if (rows <= 0) return 0;
+  const int nt = (rows + kPairMaxTokens - 1) / kPairMaxTokens;
+  return ((rows + nt - 1) / nt + 31) / 32 * 32;
+}
+__host__ __device__ inline int pair_tile_count(int rows) {
+  const int w = pair_tile_width(rows);
+  return w > 0 ? (rows + w - 1) / w : 0;
+}
+
+struct PairClass {
+  int32_t kblocks;        // K / 64
+  int32_t w_group_rows;   // weight rows per group (expert): 2I (gate/up) or H (down)
+  int32_t w_up_offset;    // SwiGLU: row offset of the up rows inside a group (= I)
+  int32_t w_stream;       // 1: honour the tile's stream bit (expert weights)
+  int32_t w_group_mod;    // > 0: the weights are a ring of w_group_mod slots (offloaded experts)
+  int32_t pad_;
+  const int32_t* w_slot_map;  // ring with a hot set: slot of each group [G]; nullptr: slot e % w_group_mod
+  void* out;              // SwiGLU: bf16 [rows][out_ld]; F32: float [rows][out_ld]
+  int64_t out_ld;
+};
+
+// Pair tile record: x = group | (cls << 15) | (weight block << 16) | (stream << 31); y = first token row of the
+// operand; z = tokens (1..256); w = first output row. A weight block is 128 values of j (gate/up: 64 gate and 64 up
+// rows per CTA) or 256 output columns (down: 128 per CTA).
+struct PairParams {
+  CUtensorMap tmW[2];         // weights, bf16: gate/up as (K, I, 2 x groups) with box 64 x 64 x 2; down box 128 x 64
+  CUtensorMap tmT[2];         // token rows (gathered rows or X; h or shared h), bf16, box 128 rows x 64
+  CUtensorMap tmTs[2];        // the same, box 32 rows x 64
+  PairClass cls[2];
+  const int4* tiles;
+  const int32_t* num_tiles;
+  const int32_t* range_lo;
+  const int32_t* range_hi;
+  int32_t* err;
+  const int32_t* stall_flag;  // test hook, as GemmParams::stall_flag
+  uint64_t timeout_ns;
+};
+cudaError_t launch_grouped_pair(const PairParams& p, int epilogue, int max_tiles, cudaStream_t stream);
+cudaError_t prepare_pair_kernels();  // shared memory attribute and the co-resident clusters (once per device)
+int pair_cluster_slots();     // co-resident clusters of two of grouped_pair_kernel (0 before prepare_pair_kernels)
 
 // Routed expert weight formats. kFmtMxfp8: E4M3 codes, one E8M0 scale per 32 along K; kFmtNvfp4: E2M1 codes (two
 // per byte), one E4M3 scale per 16 along K. A quantised launch runs grouped_gemm_q_kernel on the tiles of classes
@@ -176,6 +241,7 @@ struct PermuteParams {
   int32_t cap_gu, cap_down;
   int32_t nt_gu, nt_down;     // N tiles per routed expert (GU: I / half, down: H / bn_down)
   int32_t nt_gu_shared, nt_down_shared;  // N tiles of the shared expert (0 = no shared expert)
+  int32_t pair_gu, pair_dn;   // 1: that GEMM's tile list is for grouped_pair_kernel (its nt_* count weight blocks)
 };
 cudaError_t launch_count(const PermuteParams& p, cudaStream_t stream);
 cudaError_t launch_scan_tiles(const PermuteParams& p, cudaStream_t stream);

@@ -83,6 +83,26 @@ moe_status encode_bf16_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64
   return MOE_OK;
 }
 
+// Fused gate/up weights of `groups` groups, each [2][half_rows][cols] bf16 (its gate rows, then its up rows), as
+// the 3-D tensor (cols, half_rows, 2 x groups): a box of 64 x box_rows x 2 at (k, j, 2g) holds rows j..j+box_rows-1
+// of group g's gate half followed by the same rows of its up half. 128-byte swizzle, zero fill out of range.
+moe_status encode_bf16_halves(CUtensorMap* m, const void* ptr, uint64_t groups, uint64_t half_rows, uint64_t cols,
+                              uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {cols, half_rows, 2 * groups};
+  const cuuint64_t strides[2] = {cols * 2, half_rows * cols * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llu groups of 2 x [%llu x %llu], box %u rows",
+                (int)r, (unsigned long long)groups, (unsigned long long)half_rows, (unsigned long long)cols, box_rows);
+  return MOE_OK;
+}
+
 // fp32 output matrix [rows][cols] with row stride ld elements (ld % 4 == 0), written by TMA stores of 32 x 32
 // blocks staged with 128-byte swizzle; stores past rows or cols are clipped.
 moe_status encode_f32_out(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, uint64_t ld) {
@@ -136,6 +156,10 @@ moe_status check_device(int* device, int* num_sms) {
     if (e == cudaErrorNoKernelImageForDevice || e == cudaErrorInvalidDeviceFunction)
       return fail(MOE_ERR_ARCH, "kernels do not load on device %d: %s", *device, cudaGetErrorString(e));
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    // CTA pairs: without room for a cluster of two (pair_cluster_slots() == 0) plans use the single-CTA kernel
+    e = prepare_pair_kernels();
+    if (e == cudaErrorInvalidConfiguration) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "CTA-pair kernel setup: %s", cudaGetErrorString(e));
     prepared.push_back(*device);
   }
   return MOE_OK;
@@ -319,9 +343,19 @@ struct moe_plan {
   int device, num_sms;
   const void *w_router, *w_gu, *w_down, *ws_gu, *ws_down;
   CUtensorMap tm_wr_narrow, tm_wr_wide, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
+  CUtensorMap tm_wgu3, tm_wsgu3;  // the gate/up weights as gate/up halves (one load per tile and K step)
   // descriptors of workspace-resident activations, cached per workspace pointer
   const void* ws_cached = nullptr;
-  CUtensorMap tm_xp[2], tm_h, tm_hs, tm_ring_gu, tm_ring_down;
+  CUtensorMap tm_xp[2], tm_h, tm_hs, tm_ring_gu, tm_ring_down, tm_ring_gu3;
+  // The expert GEMMs on CTA pairs (grouped_pair_kernel): bf16 weights whose I, I_s are multiples of 128 and H of
+  // 256. pair_ok: the plan's dimensions allow it; pairs: which projections use it (MOE_PAIRS_* bits, set by
+  // moe_prefill_set_cta_pairs; the gate/up projection by default). Its descriptors: gate/up weights as gate/up
+  // halves, down weights in 128-row boxes, token rows in 128-row and 32-row boxes.
+  bool pair_ok = false;
+  int32_t pairs = 0;
+  CUtensorMap tm_wgu_p, tm_wdown_p, tm_wsgu_p, tm_wsdown_p;
+  CUtensorMap tm_xp_p[2], tm_h_p, tm_hs_p, tm_ring_gu_p, tm_ring_down_p;
+  CUtensorMap tm_xp_ps[2], tm_h_ps, tm_hs_ps;  // token rows in 32-row boxes (tiles of at most 64 tokens)
   CUtensorMap tm_y, tm_s;  // fp32 outputs of the down projection (routed rows, shared expert rows)
   // offloaded experts: w_gu / w_down are pinned host banks; the copy stream fills the ring (see moe_prefill_run)
   bool offload = false;
@@ -523,6 +557,17 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
     st = encode_u8_2d(&p->tm_wdown, w_down, static_cast<uint64_t>(s.E) * s.H, s.I / 64 * s.cb64, s.bn_down, s.cb64);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
+  if (st == MOE_OK && !p->offload && !mxfp8) st = encode_bf16_halves(&p->tm_wgu3, w_gu, s.E, s.I, s.H, s.gu_half);
+  if (st == MOE_OK && s.Is > 0) st = encode_bf16_halves(&p->tm_wsgu3, ws_gu, 1, s.Is, s.H, s.gu_half_s);
+  p->pair_ok = fmt == kFmtBf16 && s.I % 128 == 0 && s.Is % 128 == 0 && s.H % 256 == 0 && pair_cluster_slots() > 0;
+  if (st == MOE_OK && p->pair_ok && !p->offload)
+    st = encode_bf16_halves(&p->tm_wgu_p, w_gu, s.E, s.I, s.H, kPairWBoxRows);
+  if (st == MOE_OK && p->pair_ok && !p->offload)
+    st = encode_bf16_2d(&p->tm_wdown_p, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, kPairDownBoxRows);
+  if (st == MOE_OK && p->pair_ok && s.Is > 0) st = encode_bf16_halves(&p->tm_wsgu_p, ws_gu, 1, s.Is, s.H, kPairWBoxRows);
+  if (st == MOE_OK && p->pair_ok && s.Is > 0)
+    st = encode_bf16_2d(&p->tm_wsdown_p, ws_down, s.H, s.Is, kPairDownBoxRows);
+  p->pairs = p->pair_ok ? MOE_PAIRS_GATE_UP : 0;
   if (st == MOE_OK) {
     int lo = 0, hi = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
@@ -625,8 +670,11 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
   float* sbuf = reinterpret_cast<float*>(ws + L.s);
 
   // activation descriptors: X per run; workspace-resident ones cached per workspace address
-  CUtensorMap tm_x;
+  CUtensorMap tm_x, tm_x_p, tm_x_ps;
   moe_status rc = encode_bf16_2d(&tm_x, x, static_cast<uint64_t>(T), s.H, kABoxRows);
+  if (rc == MOE_OK && p->pair_ok) rc = encode_bf16_2d(&tm_x_p, x, static_cast<uint64_t>(T), s.H, kPairTBoxRows);
+  if (rc == MOE_OK && p->pair_ok)
+    rc = encode_bf16_2d(&tm_x_ps, x, static_cast<uint64_t>(T), s.H, kPairTBoxRowsSmall);
   if (rc != MOE_OK) return rc;
   if (p->ws_cached != workspace) {
     const uint64_t R = static_cast<uint64_t>(s.C) * s.k;
@@ -646,6 +694,20 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       rc = encode_u8_2d(&p->tm_ring_gu, ws + L.ring_gu, ring_slots * 2 * s.I, s.H / 64 * s.cb64, s.gu_half, s.cb64);
     if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
       rc = encode_u8_2d(&p->tm_ring_down, ws + L.ring_down, ring_slots * s.H, s.I / 64 * s.cb64, s.bn_down, s.cb64);
+    if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
+      rc = encode_bf16_halves(&p->tm_ring_gu3, ws + L.ring_gu, ring_slots, s.I, s.H, s.gu_half);
+    for (int b = 0; b < 2 && p->pair_ok; ++b) {
+      const uint32_t box = b == 0 ? kPairTBoxRows : kPairTBoxRowsSmall;
+      CUtensorMap* xp = b == 0 ? p->tm_xp_p : p->tm_xp_ps;
+      if (rc == MOE_OK) rc = encode_bf16_2d(&xp[0], ws + L.xp[0], R, s.H, box);
+      if (rc == MOE_OK) rc = encode_bf16_2d(&xp[1], ws + L.xp[1], R, s.H, box);
+      if (rc == MOE_OK) rc = encode_bf16_2d(b == 0 ? &p->tm_h_p : &p->tm_h_ps, h, R, s.I, box);
+      if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(b == 0 ? &p->tm_hs_p : &p->tm_hs_ps, hs, s.C, s.Is, box);
+    }
+    if (rc == MOE_OK && p->pair_ok && p->offload)
+      rc = encode_bf16_halves(&p->tm_ring_gu_p, ws + L.ring_gu, ring_slots, s.I, s.H, kPairWBoxRows);
+    if (rc == MOE_OK && p->pair_ok && p->offload)
+      rc = encode_bf16_2d(&p->tm_ring_down_p, ws + L.ring_down, ring_slots * s.H, s.I, kPairDownBoxRows);
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;
@@ -875,6 +937,8 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       q.nt_down = s.nt_down;
       q.nt_gu_shared = s.nt_gu_s;
       q.nt_down_shared = s.Is > 0 ? s.nt_down : 0;
+      q.pair_gu = (p->pairs & MOE_PAIRS_GATE_UP) ? 1 : 0;
+      q.pair_dn = (p->pairs & MOE_PAIRS_DOWN) ? 1 : 0;
       moe_status r2;
       {
         LaunchScope ls(p, MOE_KERNEL_COUNT, side);
@@ -973,20 +1037,109 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       return r2;
     };
 
-    auto gemms = [&](int64_t cidx, int e0, int e1, bool last_chunk) -> moe_status {
-      const int par = static_cast<int>(cidx & 1);
-      const int32_t* num_tiles = reinterpret_cast<const int32_t*>(ws + L.num_tiles[par]);
-      const int32_t* tbase = reinterpret_cast<const int32_t*>(ws + L.tile_base[par]);
-      const bool windowed = p->offload;
-      const int hb = windowed ? (e0 / s.window) & 1 : 0;
-      moe_status r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_ready[par], 0), "ready wait");
-      if (r2 == MOE_OK && windowed) r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_copy[hb], 0), "copy wait");
-      if (r2 != MOE_OK) return r2;
-      // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
+    // The same on CTA pairs (bf16 weights only).
+    auto pair_grouped = [&](PairParams prm, int epi, int cap, const int32_t* tb, const int32_t* n_tiles, int e0,
+                            int e1, bool windowed, int kind, const char* what) -> moe_status {
+      if (windowed) {
+        prm.range_lo = tb + e0;
+        prm.range_hi = (e1 >= s.E) ? n_tiles : tb + e1;
+      }
+      LaunchScope ls(p, kind, st);
+      return cuda_status(launch_grouped_pair(prm, epi, cap, st), what);
+    };
+
+    // The grouped GEMMs of one chunk on CTA pairs: weights are the 256-row M operand, the tile's token rows
+    // (gathered rows or X; h or the shared h) the N operand. Gate/up + SwiGLU:
+    auto pair_gate_up = [&](int par, const int32_t* num_tiles, const int32_t* tbase, int e0, int e1,
+                            bool windowed) -> moe_status {
+      const int32_t* slot_map = (windowed && s.hot > 0) ? reinterpret_cast<const int32_t*>(ws + L.slot_map) : nullptr;
+      PairParams gu;
+      memset(&gu, 0, sizeof gu);
+      gu.tmW[0] = windowed ? p->tm_ring_gu_p : p->tm_wgu_p;
+      gu.tmT[0] = p->tm_xp_p[par];
+      gu.tmTs[0] = p->tm_xp_ps[par];
+      PairClass c_r{};
+      c_r.kblocks = s.H / kBlockK;
+      c_r.w_group_rows = 2 * s.I;
+      c_r.w_up_offset = s.I;
+      c_r.w_stream = 1;
+      c_r.w_group_mod = windowed ? s.slots : 0;
+      c_r.w_slot_map = slot_map;
+      c_r.out = h;
+      c_r.out_ld = s.I;
+      gu.cls[0] = c_r;
+      gu.tmW[1] = gu.tmW[0];
+      gu.tmT[1] = gu.tmT[0];
+      gu.tmTs[1] = gu.tmTs[0];
+      gu.cls[1] = c_r;
+      if (s.Is > 0) {
+        gu.tmW[1] = p->tm_wsgu_p;
+        gu.tmT[1] = tm_x_p;
+        gu.tmTs[1] = tm_x_ps;
+        PairClass c_s{};
+        c_s.kblocks = s.H / kBlockK;
+        c_s.w_up_offset = s.Is;
+        c_s.out = hs;
+        c_s.out_ld = s.Is;
+        gu.cls[1] = c_s;
+      }
+      gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu[par]);
+      gu.num_tiles = num_tiles;
+      gu.err = &hdr->err;
+      gu.timeout_ns = p->timeout_ns;
+      return pair_grouped(gu, kEpiSwiGLU, L.cap_gu, tbase, num_tiles, e0, e1, windowed, MOE_KERNEL_GATE_UP,
+                          "gate/up launch");
+    };
+
+    // down:
+    auto pair_down = [&](int par, const int32_t* num_tiles, const int32_t* tbase, int e0, int e1,
+                         bool windowed) -> moe_status {
+      const int32_t* slot_map = (windowed && s.hot > 0) ? reinterpret_cast<const int32_t*>(ws + L.slot_map) : nullptr;
+      PairParams dn;
+      memset(&dn, 0, sizeof dn);
+      dn.tmW[0] = windowed ? p->tm_ring_down_p : p->tm_wdown_p;
+      dn.tmT[0] = p->tm_h_p;
+      dn.tmTs[0] = p->tm_h_ps;
+      PairClass d_r{};
+      d_r.kblocks = s.I / kBlockK;
+      d_r.w_group_rows = s.H;
+      d_r.w_stream = 1;
+      d_r.w_group_mod = windowed ? s.slots : 0;
+      d_r.w_slot_map = slot_map;
+      d_r.out = y;
+      d_r.out_ld = s.H;
+      dn.cls[0] = d_r;
+      dn.tmW[1] = dn.tmW[0];
+      dn.tmT[1] = dn.tmT[0];
+      dn.tmTs[1] = dn.tmTs[0];
+      dn.cls[1] = d_r;
+      if (s.Is > 0) {
+        dn.tmW[1] = p->tm_wsdown_p;
+        dn.tmT[1] = p->tm_hs_p;
+        dn.tmTs[1] = p->tm_hs_ps;
+        PairClass d_s{};
+        d_s.kblocks = s.Is / kBlockK;
+        d_s.out = sbuf;
+        d_s.out_ld = s.H;
+        dn.cls[1] = d_s;
+      }
+      dn.tiles = reinterpret_cast<const int4*>(ws + L.tiles_down[par]);
+      dn.num_tiles = num_tiles + 1;
+      dn.err = &hdr->err;
+      dn.timeout_ns = p->timeout_ns;
+      return pair_grouped(dn, kEpiF32, L.cap_down, tbase + (s.E + 1), num_tiles + 1, e0, e1, windowed,
+                          MOE_KERNEL_DOWN, "down launch");
+    };
+
+    // The grouped GEMMs of one chunk on single CTAs: the tile's rows are the 128-row M operand, the weights the N
+    // operand. Gate/up + SwiGLU:
+    auto single_gate_up = [&](int par, const int32_t* num_tiles, const int32_t* tbase, int e0, int e1,
+                              bool windowed) -> moe_status {
       GemmParams gu;
       memset(&gu, 0, sizeof gu);
       gu.tmA[0] = p->tm_xp[par];
       gu.tmB[0] = windowed ? p->tm_ring_gu : p->tm_wgu;
+      gu.tmBg[0] = windowed ? p->tm_ring_gu3 : p->tm_wgu3;
       GemmClass c_r{};
       c_r.kblocks = s.H / kBlockK;
       c_r.n_tile = 2 * s.gu_half;
@@ -1004,6 +1157,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       if (s.Is > 0) {
         gu.tmA[1] = tm_x;
         gu.tmB[1] = p->tm_wsgu;
+        gu.tmBg[1] = p->tm_wsgu3;
         GemmClass c_s{};
         c_s.kblocks = s.H / kBlockK;
         c_s.n_tile = 2 * s.gu_half_s;
@@ -1019,19 +1173,22 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       } else {
         gu.tmA[1] = gu.tmA[0];
         gu.tmB[1] = gu.tmB[0];
+        gu.tmBg[1] = gu.tmBg[0];
         gu.cls[1] = c_r;
       }
+      if (s.fmt != kFmtBf16) gu.tmBg[0] = gu.tmBg[1];  // routed tiles run in the decoding kernel: no bf16 view
       gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu[par]);
       gu.num_tiles = num_tiles;
       gu.err = &hdr->err;
       gu.timeout_ns = p->timeout_ns;
-      r2 = grouped(gu, kEpiSwiGLU, L.cap_gu, tbase, num_tiles, e0, e1, windowed, MOE_KERNEL_GATE_UP, "gate/up launch");
-      if (r2 != MOE_OK) return r2;
+      moe_status r2 =
+          grouped(gu, kEpiSwiGLU, L.cap_gu, tbase, num_tiles, e0, e1, windowed, MOE_KERNEL_GATE_UP, "gate/up launch");
+      return r2;
+    };
 
-      // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s), once the previous chunk's combine
-      // has read y and s
-      r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_comb, 0), "combine wait");
-      if (r2 != MOE_OK) return r2;
+    // down (class 0 routed h rows -> y, class 1 shared h rows -> s):
+    auto single_down = [&](int par, const int32_t* num_tiles, const int32_t* tbase, int e0, int e1,
+                           bool windowed) -> moe_status {
       GemmParams dn;
       memset(&dn, 0, sizeof dn);
       dn.tmA[0] = p->tm_h;
@@ -1045,7 +1202,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       d_r.out_cols = s.H;
       d_r.b_stream = 1;
       d_r.b_group_mod = windowed ? s.slots : 0;
-      d_r.b_slot_map = c_r.b_slot_map;
+      d_r.b_slot_map = (windowed && s.hot > 0) ? reinterpret_cast<const int32_t*>(ws + L.slot_map) : nullptr;
       d_r.out_ld = s.H;
       d_r.out = y;
       d_r.out_tma = 1;
@@ -1075,8 +1232,28 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       dn.num_tiles = num_tiles + 1;
       dn.err = &hdr->err;
       dn.timeout_ns = p->timeout_ns;
-      r2 = grouped(dn, kEpiF32, L.cap_down, tbase + (s.E + 1), num_tiles + 1, e0, e1, windowed, MOE_KERNEL_DOWN,
-                   "down launch");
+      return grouped(dn, kEpiF32, L.cap_down, tbase + (s.E + 1), num_tiles + 1, e0, e1, windowed, MOE_KERNEL_DOWN,
+                     "down launch");
+    };
+
+    auto gemms = [&](int64_t cidx, int e0, int e1, bool last_chunk) -> moe_status {
+      const int par = static_cast<int>(cidx & 1);
+      const int32_t* num_tiles = reinterpret_cast<const int32_t*>(ws + L.num_tiles[par]);
+      const int32_t* tbase = reinterpret_cast<const int32_t*>(ws + L.tile_base[par]);
+      const bool windowed = p->offload;
+      const int hb = windowed ? (e0 / s.window) & 1 : 0;
+      moe_status r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_ready[par], 0), "ready wait");
+      if (r2 == MOE_OK && windowed) r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_copy[hb], 0), "copy wait");
+      if (r2 != MOE_OK) return r2;
+      // 6. grouped gate/up + SwiGLU (class 0 routed on the gathered rows, class 1 shared on the chunk's X rows)
+      r2 = (p->pairs & MOE_PAIRS_GATE_UP) ? pair_gate_up(par, num_tiles, tbase, e0, e1, windowed)
+                                          : single_gate_up(par, num_tiles, tbase, e0, e1, windowed);
+      // 7. grouped down (class 0 routed h rows -> y, class 1 shared h rows -> s), once the previous chunk's combine
+      // has read y and s
+      if (r2 == MOE_OK) r2 = cuda_status(cudaStreamWaitEvent(st, p->ev_comb, 0), "combine wait");
+      if (r2 == MOE_OK)
+        r2 = (p->pairs & MOE_PAIRS_DOWN) ? pair_down(par, num_tiles, tbase, e0, e1, windowed)
+                                         : single_down(par, num_tiles, tbase, e0, e1, windowed);
       if (r2 != MOE_OK) return r2;
       if (windowed) {
         r2 = cuda_status(cudaEventRecord(p->ev_rel[hb], st), "slot release event");
@@ -1418,6 +1595,18 @@ moe_status moe_prefill_set_combine(moe_plan_t p, int32_t mode) {
   return MOE_OK;
 }
 
+moe_status moe_prefill_set_cta_pairs(moe_plan_t p, int32_t which) {
+  if (!p) return fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+  if (which & ~(MOE_PAIRS_GATE_UP | MOE_PAIRS_DOWN)) return fail(MOE_ERR_INVALID_ARG, "unknown bits in %d", which);
+  if (which && !p->pair_ok)
+    return fail(MOE_ERR_UNSUPPORTED, "CTA pairs need bf16 expert weights, inter and shared_inter multiples of 128, "
+                                     "hidden a multiple of 256 and room for a cluster of two CTAs");
+  p->pairs = which;
+  return MOE_OK;
+}
+
+int32_t moe_prefill_cta_pairs(moe_plan_t p) { return p ? p->pairs : 0; }
+
 moe_status moe_prefill_check(void* workspace, moe_stream_t stream) {
   if (!workspace) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
   CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
@@ -1576,6 +1765,8 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
     cl.b_up_offset = n;
     n_tiles = n / half;
     st = encode_bf16_2d(&g.tmB[0], b, 2ull * n, k_dim, half);
+    if (st == MOE_OK) st = encode_bf16_halves(&g.tmBg[0], b, 1, n, k_dim, half);
+    g.tmBg[1] = g.tmBg[0];
   }
   if (st == MOE_OK) st = encode_bf16_2d(&g.tmA[0], a, m, k_dim, kABoxRows);
   if (st != MOE_OK) return st;

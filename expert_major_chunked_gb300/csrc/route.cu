@@ -578,14 +578,23 @@ __device__ __forceinline__ void column_bases(const int32_t* counts, int32_t* bas
 
 // One CTA of 512 threads; thread i owns expert i and, when E > 512, expert i + 512: per-expert totals, expert offsets,
 // per-(block, expert) row bases, and the tile lists of the gate/up and down GEMMs (expert-major: expert, then N tile,
-// then M tile). 512 threads of at most 64 registers leave room on an SM for a GEMM CTA beside it: this kernel runs
+// then M tile; or, for grouped_pair_kernel, expert, then weight block, then token tile of pair_tile_width rows). 512
+// threads of at most 64 registers leave room on an SM for a GEMM CTA beside it: this kernel runs
 // while the previous chunk's GEMMs hold every SM.
 constexpr int kScanThreads = 512;
+
+// Row tiles of an expert with `rows` member rows: 128-row tiles (grouped_gemm_kernel) or pair_tile_width-row tiles
+// (grouped_pair_kernel).
+__device__ __forceinline__ int row_tiles(int rows, int pair) {
+  return pair ? pair_tile_count(rows) : (rows + kBlockM - 1) / kBlockM;
+}
+__device__ __forceinline__ int row_tile_width(int rows, int pair) { return pair ? pair_tile_width(rows) : kBlockM; }
+
 __global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermuteParams p) {
   __shared__ int sm[33];
   const int E = p.E, nblk = p.nblk;
   const int halves = (E + kScanThreads - 1) / kScanThreads;  // 1, or 2 for E > 512
-  int tot[2] = {0, 0}, off[2] = {0, 0}, mt[2] = {0, 0}, gu_base[2] = {0, 0}, dn_base[2] = {0, 0};
+  int tot[2] = {0, 0}, off[2] = {0, 0}, gu_base[2] = {0, 0}, dn_base[2] = {0, 0};
   int R = 0, n_gu = 0, n_dn = 0;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -596,10 +605,11 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermutePara
     int sum = 0;
     off[h] = R + block_exclusive_scan(tot[h], &sum, sm);
     R += sum;
-    mt[h] = (e < E) ? (tot[h] + kBlockM - 1) / kBlockM : 0;
-    gu_base[h] = n_gu + block_exclusive_scan(mt[h] * p.nt_gu, &sum, sm);
+    const int mt_gu = (e < E) ? row_tiles(tot[h], p.pair_gu) : 0;
+    const int mt_dn = (e < E) ? row_tiles(tot[h], p.pair_dn) : 0;
+    gu_base[h] = n_gu + block_exclusive_scan(mt_gu * p.nt_gu, &sum, sm);
     n_gu += sum;
-    dn_base[h] = n_dn + block_exclusive_scan(mt[h] * p.nt_down, &sum, sm);
+    dn_base[h] = n_dn + block_exclusive_scan(mt_dn * p.nt_down, &sum, sm);
     n_dn += sum;
   }
   if (threadIdx.x == 0) {
@@ -608,9 +618,10 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermutePara
     p.tile_base[E] = n_gu;
     p.tile_base[E + 1 + E] = n_dn;
   }
-  const int mts = (p.n + kBlockM - 1) / kBlockM;
-  const int n_gu_all = n_gu + (p.nt_gu_shared > 0 ? mts * p.nt_gu_shared : 0);
-  const int n_dn_all = n_dn + (p.nt_down_shared > 0 ? mts * p.nt_down_shared : 0);
+  const int mts_gu = row_tiles(p.n, p.pair_gu), mts_dn = row_tiles(p.n, p.pair_dn);
+  const int swid_gu = row_tile_width(p.n, p.pair_gu), swid_dn = row_tile_width(p.n, p.pair_dn);
+  const int n_gu_all = n_gu + (p.nt_gu_shared > 0 ? mts_gu * p.nt_gu_shared : 0);
+  const int n_dn_all = n_dn + (p.nt_down_shared > 0 ? mts_dn * p.nt_down_shared : 0);
   const bool fits = n_gu_all <= p.cap_gu && n_dn_all <= p.cap_down;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -622,28 +633,35 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermutePara
     p.tile_base[e] = gu_base[h];
     p.tile_base[E + 1 + e] = dn_base[h];
     if (!fits) continue;
-    // an expert with a single M tile is the only reader of its weight tiles: mark them for streaming
-    const int stream = (mt[h] == 1) ? static_cast<int>(1u << 31) : 0;
-    for (int nn = 0; nn < p.nt_gu; ++nn)
-      for (int m = 0; m < mt[h]; ++m)
-        p.tiles_gu[gu_base[h] + nn * mt[h] + m] = make_int4(e | (nn << 16) | stream, off[h] + m * kBlockM,
-                                                            min(kBlockM, tot[h] - m * kBlockM), off[h] + m * kBlockM);
-    for (int nn = 0; nn < p.nt_down; ++nn)
-      for (int m = 0; m < mt[h]; ++m)
-        p.tiles_down[dn_base[h] + nn * mt[h] + m] = make_int4(e | (nn << 16) | stream, off[h] + m * kBlockM,
-                                                              min(kBlockM, tot[h] - m * kBlockM), off[h] + m * kBlockM);
+    // an expert with a single row tile is the only reader of its weight tiles: mark them for streaming
+    {
+      const int mt = row_tiles(tot[h], p.pair_gu), wid = row_tile_width(tot[h], p.pair_gu);
+      const int stream = (mt == 1) ? static_cast<int>(1u << 31) : 0;
+      for (int nn = 0; nn < p.nt_gu; ++nn)
+        for (int m = 0; m < mt; ++m)
+          p.tiles_gu[gu_base[h] + nn * mt + m] =
+              make_int4(e | (nn << 16) | stream, off[h] + m * wid, min(wid, tot[h] - m * wid), off[h] + m * wid);
+    }
+    {
+      const int mt = row_tiles(tot[h], p.pair_dn), wid = row_tile_width(tot[h], p.pair_dn);
+      const int stream = (mt == 1) ? static_cast<int>(1u << 31) : 0;
+      for (int nn = 0; nn < p.nt_down; ++nn)
+        for (int m = 0; m < mt; ++m)
+          p.tiles_down[dn_base[h] + nn * mt + m] =
+              make_int4(e | (nn << 16) | stream, off[h] + m * wid, min(wid, tot[h] - m * wid), off[h] + m * wid);
+    }
   }
   if (fits) {
     // shared expert (class 1): gate/up reads the chunk's rows of X, down reads the shared h rows
-    for (int i = threadIdx.x; i < mts * p.nt_gu_shared; i += blockDim.x) {
-      const int nn = i / mts, m = i % mts;
-      p.tiles_gu[n_gu + i] = make_int4((1 << 15) | (nn << 16), static_cast<int>(p.token0) + m * kBlockM,
-                                       min(kBlockM, p.n - m * kBlockM), m * kBlockM);
+    for (int i = threadIdx.x; i < mts_gu * p.nt_gu_shared; i += blockDim.x) {
+      const int nn = i / mts_gu, m = i % mts_gu;
+      p.tiles_gu[n_gu + i] = make_int4((1 << 15) | (nn << 16), static_cast<int>(p.token0) + m * swid_gu,
+                                       min(swid_gu, p.n - m * swid_gu), m * swid_gu);
     }
-    for (int i = threadIdx.x; i < mts * p.nt_down_shared; i += blockDim.x) {
-      const int nn = i / mts, m = i % mts;
+    for (int i = threadIdx.x; i < mts_dn * p.nt_down_shared; i += blockDim.x) {
+      const int nn = i / mts_dn, m = i % mts_dn;
       p.tiles_down[n_dn + i] =
-          make_int4((1 << 15) | (nn << 16), m * kBlockM, min(kBlockM, p.n - m * kBlockM), m * kBlockM);
+          make_int4((1 << 15) | (nn << 16), m * swid_dn, min(swid_dn, p.n - m * swid_dn), m * swid_dn);
     }
   }
   if (threadIdx.x == 0) {

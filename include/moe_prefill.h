@@ -319,6 +319,21 @@ enum { MOE_COMBINE_F32 = 0, MOE_COMBINE_F64_TREE = 1 };
 moe_status moe_prefill_set_combine(moe_plan_t plan, int32_t mode);
 
 /*
+ * moe_prefill_set_cta_pairs — which expert projections of later runs of this plan run on CTA pairs: a mask of
+ * MOE_PAIRS_GATE_UP and MOE_PAIRS_DOWN (default MOE_PAIRS_GATE_UP where the plan allows it; 0: both on single CTAs).
+ * The pair kernel takes an expert's weights as the 256-row operand of tcgen05.mma.cta_group::2 (two SMs share one
+ * tile) and its member rows in steps of 32; the single-CTA kernel takes 128 member rows against 256 weight rows.
+ * Both accumulate every output element over K in the same order, so the choice changes no output byte. Needs bf16
+ * expert weights, inter and shared_inter multiples of 128 and hidden a multiple of 256: MOE_ERR_UNSUPPORTED for a
+ * non-zero mask otherwise. MOE_ERR_INVALID_ARG: NULL plan or unknown bits.
+ * moe_prefill_cta_pairs — the plan's current mask (0 for NULL).
+ * The expert-major projections they compute: "Flash Next EXL3: exact deep prefill", introduction.
+ */
+enum { MOE_PAIRS_GATE_UP = 1, MOE_PAIRS_DOWN = 2 };
+moe_status moe_prefill_set_cta_pairs(moe_plan_t plan, int32_t which);
+int32_t moe_prefill_cta_pairs(moe_plan_t plan);
+
+/*
  * moe_prefill_check — wait for `stream`, then read and clear the device error word in the workspace header.
  * Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_CUDA (a failed synchronisation).
  */
