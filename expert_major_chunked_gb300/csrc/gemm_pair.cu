@@ -211,17 +211,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         // this CTA's N/2 token rows in one box (the rows after them land in the slot and are not read)
         const bool small = N / 2 <= kPairTBoxRowsSmall;
         const void* tTok = small ? &p.tmTs[ti.cls] : &p.tmT[ti.cls];
-        const uint32_t t_bytes = (small ? kPairTBoxRowsSmall : kPairTBoxRows) * 128u;
+        const uint32_t t_bytes = kPairKB * (small ? kPairTBoxRowsSmall : kPairTBoxRows) * 128u;
         const uint32_t bytes = 2u * (kPairStageWBytes + t_bytes);
         const int slot = C.w_group_mod <= 0
                              ? ti.group
                              : (C.w_slot_map != nullptr ? __ldg(C.w_slot_map + ti.group) : ti.group % C.w_group_mod);
-        // gate/up: 64 gate rows and the same 64 up rows in one box at (k, j, 2 x slot); down: 128 rows
+        // gate/up: 64 gate rows and the same 64 up rows in one box at (0, j, 2 x slot, k block); down: 128 rows
         const int w_c1 = EPI == kEpiSwiGLU ? ti.wb * 128 + 64 * static_cast<int>(rank)
                                            : slot * C.w_group_rows + ti.wb * 256 + 128 * static_cast<int>(rank);
         const int t_row = ti.t_row0 + static_cast<int>(rank) * (N / 2);
         const bool stream = C.w_stream && ti.stream;
-        for (int kb = 0; kb < C.kblocks; ++kb) {
+        for (int kb = 0; kb < C.kblocks; kb += kPairKB) {
           if (!ptx::wait_bounded(empty0 + 8u * stage, phase ^ 1u, tmo, abort_flag)) {
             pair_raise(p, abort_flag, kSiteProducerEmpty);
             failed = true;
@@ -231,18 +231,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           const uint32_t fb = full_even + 8u * stage;
           const uint32_t w_dst = sW + stage * kPairStageWBytes;
           const uint32_t t_dst = sT + stage * kPairStageTBytes;
-          const int kc = kb * kBlockK;
           if (EPI == kEpiSwiGLU) {
             if (stream)
-              ptx::tma_load_3d_pair_hint(w_dst, tW, kc, w_c1, 2 * slot, fb, pol_stream);
+              ptx::tma_load_4d_pair_hint(w_dst, tW, 0, w_c1, 2 * slot, kb, fb, pol_stream);
             else
-              ptx::tma_load_3d_pair(w_dst, tW, kc, w_c1, 2 * slot, fb);
+              ptx::tma_load_4d_pair(w_dst, tW, 0, w_c1, 2 * slot, kb, fb);
           } else if (stream) {
-            ptx::tma_load_2d_pair_hint(w_dst, tW, kc, w_c1, fb, pol_stream);
+            ptx::tma_load_3d_pair_hint(w_dst, tW, 0, w_c1, kb, fb, pol_stream);
           } else {
-            ptx::tma_load_2d_pair(w_dst, tW, kc, w_c1, fb);
+            ptx::tma_load_3d_pair(w_dst, tW, 0, w_c1, kb, fb);
           }
-          ptx::tma_load_2d_pair(t_dst, tTok, kc, t_row, fb);
+          ptx::tma_load_3d_pair(t_dst, tTok, 0, t_row, kb, fb);
           issued_any = true;
           if (++stage == kPairStages) {
             stage = 0;
@@ -277,19 +276,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kMaxN);
-        const uint32_t idesc = ptx::idesc_bf16_f32(256u, static_cast<uint32_t>(pair_width(ti.n)));
-        for (int kb = 0; kb < C.kblocks; ++kb) {
+        const int N = pair_width(ti.n);
+        const uint32_t idesc = ptx::idesc_bf16_f32(256u, static_cast<uint32_t>(N));
+        const uint32_t t_kb_bytes = (N / 2 <= kPairTBoxRowsSmall ? kPairTBoxRowsSmall : kPairTBoxRows) * 128u;
+        for (int kb = 0; kb < C.kblocks; kb += kPairKB) {
           if (!ptx::wait_bounded(full0 + 8u * stage, phase, tmo, abort_flag)) {
             pair_raise(p, abort_flag, kSiteMmaFull);
             failed = true;
             break;
           }
           ptx::tc_fence_after();
-          const uint64_t a_desc = ptx::sw128_kmajor_desc(sW + stage * kPairStageWBytes);
-          const uint64_t b_desc = ptx::sw128_kmajor_desc(sT + stage * kPairStageTBytes);
 #pragma unroll
-          for (int kk = 0; kk < kBlockK / 16; ++kk)
-            ptx::umma_bf16_pair(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | kk) != 0 ? 1u : 0u);
+          for (int j = 0; j < kPairKB; ++j) {
+            // K block kb + j: its weight rows (16 KB) and token rows follow those of block kb + j - 1 in the slot
+            const uint64_t a_desc = ptx::sw128_kmajor_desc(sW + stage * kPairStageWBytes + j * 16384u);
+            const uint64_t b_desc = ptx::sw128_kmajor_desc(sT + stage * kPairStageTBytes + j * t_kb_bytes);
+#pragma unroll
+            for (int kk = 0; kk < kBlockK / 16; ++kk)
+              ptx::umma_bf16_pair(d_tmem, a_desc + 2u * kk, b_desc + 2u * kk, idesc, (kb | j | kk) != 0 ? 1u : 0u);
+          }
           ptx::umma_commit_pair(empty0 + 8u * stage, 0x3);  // frees the stage in both CTAs
           issued_any = true;
           if (++stage == kPairStages) {

@@ -128,14 +128,15 @@ struct GemmParams {
 // tcgen05.mma.cta_group::2, M = 256 rows of weights (128 in each CTA's shared memory and TMEM lanes) times N tokens
 // (N = the tile's token count rounded up to 32, at most 256; each CTA loads N/2 of the token rows). The output is
 // the transpose of the single-CTA kernel's tile: TMEM lane = weight row (an output column), TMEM column = token.
-constexpr int kPairStages = 6;
+constexpr int kPairKB = 2;                // 64-wide K blocks per stage: one box per operand carries both
+constexpr int kPairStages = 3;
 constexpr int kPairWBoxRows = 64;         // gate/up: 64 gate and 64 up rows per CTA in one 3-D box
 constexpr int kPairDownBoxRows = 128;     // down: 128 weight rows per CTA in one box
 constexpr int kPairTBoxRows = 128;        // token rows per box (one box: a CTA's N/2 <= 128 rows, and the rest unused)
 constexpr int kPairTBoxRowsSmall = 32;    // token rows per box for tiles with N/2 <= 32
 constexpr int kPairMaxTokens = 256;       // UMMA N limit
-constexpr int kPairStageWBytes = 128 * kBlockK * 2;                  // 16 KB: 128 weight rows
-constexpr int kPairStageTBytes = (kPairMaxTokens / 2) * kBlockK * 2; // 16 KB: up to 128 token rows
+constexpr int kPairStageWBytes = kPairKB * 128 * kBlockK * 2;                  // 32 KB: 128 weight rows
+constexpr int kPairStageTBytes = kPairKB * (kPairMaxTokens / 2) * kBlockK * 2; // 32 KB: up to 128 token rows
 constexpr int kPairThreads = 320;          // warp 0 TMA, warp 1 MMA (+ TMEM alloc), warps 2..9 epilogue (two groups)
 constexpr int kPairXchgBytes = 2 * 8192;   // per epilogue group: a 16-column slice staged in shared memory
 constexpr int kPairSmemBytes = 1024 /*align slack*/ + kPairStages * (kPairStageWBytes + kPairStageTBytes) +
@@ -169,9 +170,12 @@ struct PairClass {
 // operand; z = tokens (1..256); w = first output row. A weight block is 128 values of j (gate/up: 64 gate and 64 up
 // rows per CTA) or 256 output columns (down: 128 per CTA).
 struct PairParams {
-  CUtensorMap tmW[2];         // weights, bf16: gate/up as (K, I, 2 x groups) with box 64 x 64 x 2; down box 128 x 64
-  CUtensorMap tmT[2];         // token rows (gathered rows or X; h or shared h), bf16, box 128 rows x 64
-  CUtensorMap tmTs[2];        // the same, box 32 rows x 64
+  // Every map has the 64-wide K block as its outermost dimension (stride 128 B), so that one box holds kPairKB
+  // consecutive K blocks of its rows, one after the other.
+  CUtensorMap tmW[2];         // weights, bf16: gate/up as (64, I, 2 x groups, K/64), box 64 x 64 x 2 x kPairKB;
+                              // down as (64, rows, K/64), box 64 x 128 x kPairKB
+  CUtensorMap tmT[2];         // token rows (gathered rows or X; h or shared h), (64, rows, K/64), box 64 x 128 x kPairKB
+  CUtensorMap tmTs[2];        // the same, box 64 x 32 x kPairKB
   PairClass cls[2];
   const int4* tiles;
   const int32_t* num_tiles;

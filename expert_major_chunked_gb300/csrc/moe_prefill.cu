@@ -103,6 +103,45 @@ moe_status encode_bf16_halves(CUtensorMap* m, const void* ptr, uint64_t groups, 
   return MOE_OK;
 }
 
+// The same fused gate/up weights with the 64-wide K block as the outermost dimension: (64, half_rows, 2 x groups,
+// cols / 64), strides (cols x 2, half_rows x cols x 2, 128) bytes. A box of 64 x box_rows x 2 x kb at
+// (0, j, 2g, k block) holds, for each of kb consecutive K blocks in turn, box_rows gate rows then the same up rows.
+moe_status encode_bf16_halves_kb(CUtensorMap* m, const void* ptr, uint64_t groups, uint64_t half_rows, uint64_t cols,
+                                 uint32_t box_rows, uint32_t kb) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kBlockK), half_rows, 2 * groups, cols / kBlockK};
+  const cuuint64_t strides[3] = {cols * 2, half_rows * cols * 2, static_cast<cuuint64_t>(kBlockK) * 2};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kBlockK), box_rows, 2, kb};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %llu groups of 2 x [%llu x %llu] by K blocks",
+                (int)r, (unsigned long long)groups, (unsigned long long)half_rows, (unsigned long long)cols);
+  return MOE_OK;
+}
+
+// bf16 matrix [rows][cols] (row-major) with the 64-wide K block as the outermost dimension: (64, rows, cols / 64),
+// strides (cols x 2, 128) bytes; a box of 64 x box_rows x kb holds box_rows rows of each of kb consecutive K blocks.
+moe_status encode_bf16_rows_kb(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                               uint32_t kb) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBlockK), rows, cols / kBlockK};
+  const cuuint64_t strides[2] = {cols * 2, static_cast<cuuint64_t>(kBlockK) * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kBlockK), box_rows, kb};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%llu x %llu] matrix by K blocks, box %u rows",
+                (int)r, (unsigned long long)rows, (unsigned long long)cols, box_rows);
+  return MOE_OK;
+}
+
 // fp32 output matrix [rows][cols] with row stride ld elements (ld % 4 == 0), written by TMA stores of 32 x 32
 // blocks staged with 128-byte swizzle; stores past rows or cols are clipped.
 moe_status encode_f32_out(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t cols, uint64_t ld) {
@@ -561,12 +600,13 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_halves(&p->tm_wsgu3, ws_gu, 1, s.Is, s.H, s.gu_half_s);
   p->pair_ok = fmt == kFmtBf16 && s.I % 128 == 0 && s.Is % 128 == 0 && s.H % 256 == 0 && pair_cluster_slots() > 0;
   if (st == MOE_OK && p->pair_ok && !p->offload)
-    st = encode_bf16_halves(&p->tm_wgu_p, w_gu, s.E, s.I, s.H, kPairWBoxRows);
+    st = encode_bf16_halves_kb(&p->tm_wgu_p, w_gu, s.E, s.I, s.H, kPairWBoxRows, kPairKB);
   if (st == MOE_OK && p->pair_ok && !p->offload)
-    st = encode_bf16_2d(&p->tm_wdown_p, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, kPairDownBoxRows);
-  if (st == MOE_OK && p->pair_ok && s.Is > 0) st = encode_bf16_halves(&p->tm_wsgu_p, ws_gu, 1, s.Is, s.H, kPairWBoxRows);
+    st = encode_bf16_rows_kb(&p->tm_wdown_p, w_down, static_cast<uint64_t>(s.E) * s.H, s.I, kPairDownBoxRows, kPairKB);
   if (st == MOE_OK && p->pair_ok && s.Is > 0)
-    st = encode_bf16_2d(&p->tm_wsdown_p, ws_down, s.H, s.Is, kPairDownBoxRows);
+    st = encode_bf16_halves_kb(&p->tm_wsgu_p, ws_gu, 1, s.Is, s.H, kPairWBoxRows, kPairKB);
+  if (st == MOE_OK && p->pair_ok && s.Is > 0)
+    st = encode_bf16_rows_kb(&p->tm_wsdown_p, ws_down, s.H, s.Is, kPairDownBoxRows, kPairKB);
   p->pairs = p->pair_ok ? MOE_PAIRS_GATE_UP : 0;
   if (st == MOE_OK) {
     int lo = 0, hi = 0;
@@ -672,9 +712,10 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
   // activation descriptors: X per run; workspace-resident ones cached per workspace address
   CUtensorMap tm_x, tm_x_p, tm_x_ps;
   moe_status rc = encode_bf16_2d(&tm_x, x, static_cast<uint64_t>(T), s.H, kABoxRows);
-  if (rc == MOE_OK && p->pair_ok) rc = encode_bf16_2d(&tm_x_p, x, static_cast<uint64_t>(T), s.H, kPairTBoxRows);
   if (rc == MOE_OK && p->pair_ok)
-    rc = encode_bf16_2d(&tm_x_ps, x, static_cast<uint64_t>(T), s.H, kPairTBoxRowsSmall);
+    rc = encode_bf16_rows_kb(&tm_x_p, x, static_cast<uint64_t>(T), s.H, kPairTBoxRows, kPairKB);
+  if (rc == MOE_OK && p->pair_ok)
+    rc = encode_bf16_rows_kb(&tm_x_ps, x, static_cast<uint64_t>(T), s.H, kPairTBoxRowsSmall, kPairKB);
   if (rc != MOE_OK) return rc;
   if (p->ws_cached != workspace) {
     const uint64_t R = static_cast<uint64_t>(s.C) * s.k;
@@ -699,15 +740,16 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
     for (int b = 0; b < 2 && p->pair_ok; ++b) {
       const uint32_t box = b == 0 ? kPairTBoxRows : kPairTBoxRowsSmall;
       CUtensorMap* xp = b == 0 ? p->tm_xp_p : p->tm_xp_ps;
-      if (rc == MOE_OK) rc = encode_bf16_2d(&xp[0], ws + L.xp[0], R, s.H, box);
-      if (rc == MOE_OK) rc = encode_bf16_2d(&xp[1], ws + L.xp[1], R, s.H, box);
-      if (rc == MOE_OK) rc = encode_bf16_2d(b == 0 ? &p->tm_h_p : &p->tm_h_ps, h, R, s.I, box);
-      if (rc == MOE_OK && s.Is > 0) rc = encode_bf16_2d(b == 0 ? &p->tm_hs_p : &p->tm_hs_ps, hs, s.C, s.Is, box);
+      if (rc == MOE_OK) rc = encode_bf16_rows_kb(&xp[0], ws + L.xp[0], R, s.H, box, kPairKB);
+      if (rc == MOE_OK) rc = encode_bf16_rows_kb(&xp[1], ws + L.xp[1], R, s.H, box, kPairKB);
+      if (rc == MOE_OK) rc = encode_bf16_rows_kb(b == 0 ? &p->tm_h_p : &p->tm_h_ps, h, R, s.I, box, kPairKB);
+      if (rc == MOE_OK && s.Is > 0)
+        rc = encode_bf16_rows_kb(b == 0 ? &p->tm_hs_p : &p->tm_hs_ps, hs, s.C, s.Is, box, kPairKB);
     }
     if (rc == MOE_OK && p->pair_ok && p->offload)
-      rc = encode_bf16_halves(&p->tm_ring_gu_p, ws + L.ring_gu, ring_slots, s.I, s.H, kPairWBoxRows);
+      rc = encode_bf16_halves_kb(&p->tm_ring_gu_p, ws + L.ring_gu, ring_slots, s.I, s.H, kPairWBoxRows, kPairKB);
     if (rc == MOE_OK && p->pair_ok && p->offload)
-      rc = encode_bf16_2d(&p->tm_ring_down_p, ws + L.ring_down, ring_slots * s.H, s.I, kPairDownBoxRows);
+      rc = encode_bf16_rows_kb(&p->tm_ring_down_p, ws + L.ring_down, ring_slots * s.H, s.I, kPairDownBoxRows, kPairKB);
     if (rc != MOE_OK) {
       p->ws_cached = nullptr;
       return rc;

@@ -270,6 +270,23 @@ __device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t smem_dst, const v
       ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t smem_dst, const void* tmap, int32_t c0, int32_t c1,
+                                                 int32_t c2, int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t smem_dst, const void* tmap, int32_t c0, int32_t c1,
+                                                      int32_t c2, int32_t c3, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+      ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar),
+        "l"(policy)
+      : "memory");
+}
 // TMEM allocation for a CTA pair: one warp of each CTA of the pair executes it; the same columns are allocated in
 // both CTAs.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
