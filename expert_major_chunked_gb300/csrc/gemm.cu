@@ -563,7 +563,8 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
   }
   if (warp == 0 && lane == 0) {
     ptx::tma_prefetch_desc(&p.tmA[0]);
-    ptx::tma_prefetch_desc(&p.tmB[0]);
+    ptx::tma_prefetch_desc(EPI == kEpiSwiGLU ? &p.tmBg[0] : &p.tmB[0]);
+    ptx::tma_prefetch_desc(&p.tmS[0]);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), 2 * kMaxN);
@@ -593,9 +594,7 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
         const uint32_t bytes = b_loads * C.b_box_rows * (kCodeBytes + kScaleBlocks);
         const int gslot = b_slot(C, ti.group);
         const int b_row0 = tile_b_row<EPI>(C, gslot, ti.n_idx);
-        const int b_row1 = b_row0 + C.b_up_offset;
         const int r0 = b_row0 - gslot * C.b_group_rows;  // first row inside the group
-        const int64_t planes = kScaleBlocks * C.kblocks;  // scale blocks per row
         const bool hint = C.b_stream && ti.stream;
         for (int kb = 0; kb < C.kblocks; ++kb) {
           if (!ptx::wait_bounded(c_empty0 + 8u * slot, phase ^ 1u, tmo, abort_flag)) {
@@ -608,20 +607,23 @@ __global__ void __launch_bounds__(kGemmThreadsQ, 1) grouped_gemm_q_kernel(const 
           const uint32_t c_dst = sC + slot * kQStageCodeBytes;
           const uint32_t s_dst = sS + slot * kQStageScaleBytes;
           const int kx = kb * static_cast<int>(kCodeBytes);  // inner coordinate of the code map, in bytes
-          if (hint) {
-            ptx::tma_load_2d_hint(c_dst, tB, kx, b_row0, fb, pol_stream);
-            if (EPI == kEpiSwiGLU)
-              ptx::tma_load_2d_hint(c_dst + C.b_box_rows * kCodeBytes, tB, kx, b_row1, fb, pol_stream);
+          if (EPI == kEpiSwiGLU) {
+            // the tile's gate and up code rows in one box of the (bytes, j, 2 x slot + half) view
+            const void* tBg = &p.tmBg[ti.cls];
+            if (hint)
+              ptx::tma_load_3d_hint(c_dst, tBg, kx, r0, 2 * gslot, fb, pol_stream);
+            else
+              ptx::tma_load_3d(c_dst, tBg, kx, r0, 2 * gslot, fb);
+            // the step's scale blocks of those rows in one box of the (row in half, half, plane, expert) view:
+            // block h of the gate rows, then of the up rows, for each h in turn
+            ptx::tma_load_4d(s_dst, &p.tmS[ti.cls], r0, 0, kScaleBlocks * kb, ti.group, fb);
           } else {
-            ptx::tma_load_2d(c_dst, tB, kx, b_row0, fb);
-            if (EPI == kEpiSwiGLU) ptx::tma_load_2d(c_dst + C.b_box_rows * kCodeBytes, tB, kx, b_row1, fb);
-          }
-          for (int h = 0; h < kScaleBlocks; ++h) {
-            const uint8_t* plane = C.b_scale + (static_cast<int64_t>(ti.group) * planes + kScaleBlocks * kb + h) *
-                                                   static_cast<int64_t>(C.b_group_rows);
-            ptx::bulk_load(s_dst + h * C.n_tile, plane + r0, C.b_box_rows, fb);
-            if (EPI == kEpiSwiGLU)
-              ptx::bulk_load(s_dst + h * C.n_tile + C.b_box_rows, plane + r0 + C.b_up_offset, C.b_box_rows, fb);
+            if (hint)
+              ptx::tma_load_2d_hint(c_dst, tB, kx, b_row0, fb, pol_stream);
+            else
+              ptx::tma_load_2d(c_dst, tB, kx, b_row0, fb);
+            // the step's scale blocks of the tile's rows in one box of the (row, plane, expert) view
+            ptx::tma_load_3d(s_dst, &p.tmS[ti.cls], r0, kScaleBlocks * kb, ti.group, fb);
           }
           ++issued;
           if (++slot == kQStagesC) {

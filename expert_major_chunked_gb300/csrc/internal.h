@@ -107,8 +107,12 @@ struct GemmClass {
 struct GemmParams {
   CUtensorMap tmA[2];
   CUtensorMap tmB[2];
-  CUtensorMap tmBg[2];        // SwiGLU, bf16 weights: the fused gate/up weights as (K, I, 2 x groups), box 64 x
-                              // b_box_rows x 2: a tile's gate rows and up rows in one load
+  CUtensorMap tmBg[2];        // SwiGLU: the fused gate/up weights (bf16, or the codes of block-scaled weights) as
+                              // (K, I, 2 x groups), box 64 (or a code row's step bytes) x b_box_rows x 2: a tile's
+                              // gate rows and up rows in one load
+  CUtensorMap tmS[2];         // block-scaled weights: the scale planes, uint8. SwiGLU: (row in half I, half 2,
+                              // plane, expert), box b_box_rows x 2 x blocks per step x 1; F32: (row, plane, expert),
+                              // box b_box_rows x blocks per step x 1
   CUtensorMap tmOut[2];       // F32 outputs with out_tma != 0: fp32 [rows][out_ld] map, box 32 x 32, 128B swizzle
   GemmClass cls[2];
   const int4* tiles;          // device tile list (nullptr: dense mode)

@@ -159,6 +159,48 @@ moe_status encode_f32_out(CUtensorMap* m, void* ptr, uint64_t rows, uint64_t col
   return MOE_OK;
 }
 
+// uint8 tensor of `rank` dimensions (dims[0] innermost, strides in bytes for dims 1..rank-1), no swizzle, zero fill.
+moe_status encode_u8_nd(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                        const cuuint32_t* box, const char* what) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for %s", (int)r, what);
+  return MOE_OK;
+}
+
+// Codes of fused gate/up weights, `groups` groups of [2][half_rows][row_bytes], as (row_bytes, half_rows, 2 x groups):
+// a box of step_bytes x box_rows x 2 holds box_rows gate code rows, then the same up rows.
+moe_status encode_u8_halves(CUtensorMap* m, const void* ptr, uint64_t groups, uint64_t half_rows, uint64_t row_bytes,
+                            uint32_t box_rows, uint32_t step_bytes) {
+  const cuuint64_t dims[3] = {row_bytes, half_rows, 2 * groups};
+  const cuuint64_t strides[2] = {row_bytes, half_rows * row_bytes};
+  const cuuint32_t box[3] = {step_bytes, box_rows, 2};
+  return encode_u8_nd(m, ptr, 3, dims, strides, box, "gate/up code halves");
+}
+
+// Scale planes [groups][planes][2 x half_rows] of fused gate/up weights as (half_rows, 2, planes, groups): a box of
+// box_rows x 2 x blocks x 1 holds, for each of `blocks` planes in turn, box_rows gate scales then the same up scales.
+moe_status encode_u8_scales_gu(CUtensorMap* m, const void* ptr, uint64_t groups, uint64_t planes, uint64_t half_rows,
+                               uint32_t box_rows, uint32_t blocks) {
+  const cuuint64_t dims[4] = {half_rows, 2, planes, groups};
+  const cuuint64_t strides[3] = {half_rows, 2 * half_rows, planes * 2 * half_rows};
+  const cuuint32_t box[4] = {box_rows, 2, blocks, 1};
+  return encode_u8_nd(m, ptr, 4, dims, strides, box, "gate/up scale planes");
+}
+
+// Scale planes [groups][planes][rows] as (rows, planes, groups): a box of box_rows x blocks x 1.
+moe_status encode_u8_scales(CUtensorMap* m, const void* ptr, uint64_t groups, uint64_t planes, uint64_t rows,
+                            uint32_t box_rows, uint32_t blocks) {
+  const cuuint64_t dims[3] = {rows, planes, groups};
+  const cuuint64_t strides[2] = {rows, planes * rows};
+  const cuuint32_t box[3] = {box_rows, blocks, 1};
+  return encode_u8_nd(m, ptr, 3, dims, strides, box, "down scale planes");
+}
+
 // Code matrix [rows][cols] of bytes (row-major), boxes of box_rows x box_bytes, no swizzle (the decoder warps read
 // the rows densely), zero fill out of range.
 moe_status encode_u8_2d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
@@ -382,7 +424,8 @@ struct moe_plan {
   int device, num_sms;
   const void *w_router, *w_gu, *w_down, *ws_gu, *ws_down;
   CUtensorMap tm_wr_narrow, tm_wr_wide, tm_wgu, tm_wdown, tm_wsgu, tm_wsdown;
-  CUtensorMap tm_wgu3, tm_wsgu3;  // the gate/up weights as gate/up halves (one load per tile and K step)
+  CUtensorMap tm_wgu3, tm_wsgu3;  // the gate/up weights (or codes) as gate/up halves (one load per tile and K step)
+  CUtensorMap tm_sgu, tm_sdown;   // block-scaled weights: their scale planes, one load per tile and K step
   // descriptors of workspace-resident activations, cached per workspace pointer
   const void* ws_cached = nullptr;
   CUtensorMap tm_xp[2], tm_h, tm_hs, tm_ring_gu, tm_ring_down, tm_ring_gu3;
@@ -597,6 +640,18 @@ moe_status plan_impl(const moe_dims* dims, const void* w_router, const void* w_g
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsgu, ws_gu, 2ull * s.Is, s.H, s.gu_half_s);
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_2d(&p->tm_wsdown, ws_down, s.H, s.Is, s.bn_down);
   if (st == MOE_OK && !p->offload && !mxfp8) st = encode_bf16_halves(&p->tm_wgu3, w_gu, s.E, s.I, s.H, s.gu_half);
+  if (st == MOE_OK && !p->offload && mxfp8)
+    st = encode_u8_halves(&p->tm_wgu3, w_gu, s.E, s.I, static_cast<uint64_t>(s.H) / 64 * s.cb64, s.gu_half, s.cb64);
+  if (mxfp8) {
+    // scale planes: one per scale block along K (MXFP8: 32 weights, NVFP4: 16), 64 / block blocks per K step
+    const uint32_t blocks = fmt == kFmtNvfp4 ? 4u : 2u;
+    if (st == MOE_OK)
+      st = encode_u8_scales_gu(&p->tm_sgu, gu_scale, s.E, static_cast<uint64_t>(s.H) / 64 * blocks, s.I, s.gu_half,
+                               blocks);
+    if (st == MOE_OK)
+      st = encode_u8_scales(&p->tm_sdown, down_scale, s.E, static_cast<uint64_t>(s.I) / 64 * blocks, s.H, s.bn_down,
+                            blocks);
+  }
   if (st == MOE_OK && s.Is > 0) st = encode_bf16_halves(&p->tm_wsgu3, ws_gu, 1, s.Is, s.H, s.gu_half_s);
   p->pair_ok = fmt == kFmtBf16 && s.I % 128 == 0 && s.Is % 128 == 0 && s.H % 256 == 0 && pair_cluster_slots() > 0;
   if (st == MOE_OK && p->pair_ok && !p->offload)
@@ -737,6 +792,9 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       rc = encode_u8_2d(&p->tm_ring_down, ws + L.ring_down, ring_slots * s.H, s.I / 64 * s.cb64, s.bn_down, s.cb64);
     if (rc == MOE_OK && p->offload && s.fmt == kFmtBf16)
       rc = encode_bf16_halves(&p->tm_ring_gu3, ws + L.ring_gu, ring_slots, s.I, s.H, s.gu_half);
+    if (rc == MOE_OK && p->offload && s.fmt != kFmtBf16)
+      rc = encode_u8_halves(&p->tm_ring_gu3, ws + L.ring_gu, ring_slots, s.I, static_cast<uint64_t>(s.H) / 64 * s.cb64,
+                            s.gu_half, s.cb64);
     for (int b = 0; b < 2 && p->pair_ok; ++b) {
       const uint32_t box = b == 0 ? kPairTBoxRows : kPairTBoxRowsSmall;
       CUtensorMap* xp = b == 0 ? p->tm_xp_p : p->tm_xp_ps;
@@ -1195,6 +1253,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       c_r.out_ld = s.I;
       c_r.out = h;
       c_r.b_scale = p->w_gu_scale;
+      gu.tmS[0] = gu.tmS[1] = p->tm_sgu;
       gu.cls[0] = c_r;
       if (s.Is > 0) {
         gu.tmA[1] = tm_x;
@@ -1218,7 +1277,6 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
         gu.tmBg[1] = gu.tmBg[0];
         gu.cls[1] = c_r;
       }
-      if (s.fmt != kFmtBf16) gu.tmBg[0] = gu.tmBg[1];  // routed tiles run in the decoding kernel: no bf16 view
       gu.tiles = reinterpret_cast<const int4*>(ws + L.tiles_gu[par]);
       gu.num_tiles = num_tiles;
       gu.err = &hdr->err;
@@ -1249,6 +1307,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       d_r.out = y;
       d_r.out_tma = 1;
       d_r.b_scale = p->w_down_scale;
+      dn.tmS[0] = dn.tmS[1] = p->tm_sdown;
       dn.cls[0] = d_r;
       dn.tmOut[0] = p->tm_y;
       if (s.Is > 0) {

@@ -101,6 +101,16 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t smem_dst, const void* 
       : "memory");
 }
 
+// 4-D tile load, completion counted on an mbarrier.
+__device__ __forceinline__ void tma_load_4d(uint32_t smem_dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+      ::"r"(smem_dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
 // Plain (non-tensor) bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte aligned),
 // completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t smem_dst, const void* src, uint32_t bytes, uint32_t bar) {
