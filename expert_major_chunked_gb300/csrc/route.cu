@@ -227,38 +227,49 @@ __device__ __forceinline__ void load_logits(const float* lrow, int E, int lane, 
   }
 }
 
+// A float's bits as an unsigned key with the same order (for non-NaN values; -0 is taken as +0 first, so the two
+// zeros tie as they compare equal).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // (rounds) rounds of warp argmax by (value desc, id asc); marks the first k in *sel, returns the k-th and (k+1)-th.
+// Each round: every lane offers its best unselected value; the warp takes the largest key (redux max), then the
+// smallest id among the lanes holding it (redux min).
 template <int EPL>
 __device__ __forceinline__ void select_top(const float (&v)[EPL], int E, int k, int lane, uint32_t* sel, float* vk,
                                            float* vk1) {
+  uint32_t key[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) key[j] = order_key(v[j]);
   uint32_t s = 0;
   float a = 0.0f, b = -FLT_MAX;
   const int rounds = (k + 1 < E) ? k + 1 : E;
   for (int r = 0; r < rounds; ++r) {
-    float bv = -FLT_MAX;
+    uint32_t bk = 0;
     int bid = INT_MAX;
 #pragma unroll
     for (int j = 0; j < EPL; ++j) {
       const int e = j * 32 + lane;
-      if (e < E && !((s >> j) & 1u) && (bid == INT_MAX || v[j] > bv)) {
-        bv = v[j];
+      if (e < E && !((s >> j) & 1u) && (bid == INT_MAX || key[j] > bk)) {
+        bk = key[j];
         bid = e;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-      if (ov > bv || (ov == bv && oid < bid)) {
-        bv = ov;
-        bid = oid;
-      }
-    }
+    // lanes with nothing left offer key 0 and id INT_MAX; a real key is never 0 (it would be a NaN's)
+    const uint32_t wk = __reduce_max_sync(0xffffffffu, bid == INT_MAX ? 0u : bk);
+    const int wid = static_cast<int>(
+        __reduce_min_sync(0xffffffffu, (bid != INT_MAX && bk == wk) ? static_cast<uint32_t>(bid) : 0x7FFFFFFFu));
+    const float wv = wid == INT_MAX ? -FLT_MAX : key_value(wk);
     if (r < k) {
-      if (bid != INT_MAX && (bid & 31) == lane) s |= 1u << (bid >> 5);
-      if (r == k - 1) a = bv;
+      if (wid != INT_MAX && (wid & 31) == lane) s |= 1u << (wid >> 5);
+      if (r == k - 1) a = wv;
     } else {
-      b = bv;
+      b = wv;
     }
   }
   *sel = s;
