@@ -73,6 +73,9 @@ _SIGS = {
     "moe_prefill_run_noalloc": ([_P, _P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P], ctypes.c_int),
     "moe_prefill_debug_gemm": ([_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                 ctypes.c_uint64, _P], ctypes.c_int),
+    "moe_prefill_debug_gemm_pairs_scratch": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32], ctypes.c_size_t),
+    "moe_prefill_debug_gemm_pairs": ([_P, _P, _P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P,
+                                      ctypes.c_size_t, _P, _P, ctypes.c_uint64, _P], ctypes.c_int),
 }
 
 
@@ -244,6 +247,16 @@ def moe_prefill_run_stats(workspace, stream=None) -> dict:
 
 def moe_prefill_debug_gemm(a, b, c, m, n, k_dim, epilogue, err_word, stall_flag=None, timeout_ns=0, stream=None):
     _check(lib().moe_prefill_debug_gemm(a, b, c, m, n, k_dim, epilogue, err_word, stall_flag, timeout_ns, stream))
+
+
+def moe_prefill_debug_gemm_pairs_scratch(m, n, epilogue) -> int:
+    return int(lib().moe_prefill_debug_gemm_pairs_scratch(m, n, epilogue))
+
+
+def moe_prefill_debug_gemm_pairs(a, b, c, m, n, k_dim, epilogue, scratch, scratch_bytes, err_word, stall_flag=None,
+                                 timeout_ns=0, stream=None):
+    _check(lib().moe_prefill_debug_gemm_pairs(a, b, c, m, n, k_dim, epilogue, scratch, scratch_bytes, err_word,
+                                              stall_flag, timeout_ns, stream))
 
 
 # ---------------------------------------------------------------------------------------------------- torch helper

@@ -1886,4 +1886,68 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
                      "debug GEMM launch");
 }
 
+// Tiles of the pair kernel for one dense GEMM: m token rows as one group (pair_tile_count(m) tiles of
+// pair_tile_width(m) rows) times the weight blocks (F32: n / 256; SwiGLU: n / 128).
+size_t moe_prefill_debug_gemm_pairs_scratch(int32_t m, int32_t n, int32_t epilogue) {
+  if (m < 1 || n < 1 || (epilogue != kEpiF32 && epilogue != kEpiSwiGLU)) return 0;
+  const size_t tiles = static_cast<size_t>(pair_tile_count(m)) * (epilogue == kEpiF32 ? n / 256 : n / 128);
+  return 16 * (tiles + 1);
+}
+
+moe_status moe_prefill_debug_gemm_pairs(const void* a, const void* b, void* c, int32_t m, int32_t n, int32_t k_dim,
+                                        int32_t epilogue, void* scratch, size_t scratch_bytes, int32_t* err_word,
+                                        const int32_t* stall_flag, uint64_t timeout_ns, moe_stream_t stream) {
+  if (!a || !b || !c || !err_word || !scratch)
+    return fail(MOE_ERR_INVALID_ARG, "a, b, c, scratch and err_word must not be NULL");
+  if (epilogue != kEpiF32 && epilogue != kEpiSwiGLU) return fail(MOE_ERR_INVALID_ARG, "epilogue must be 0 or 1");
+  if (m < 1 || k_dim < 128 || k_dim % 128) return fail(MOE_ERR_INVALID_ARG, "need m >= 1, k_dim % 128 == 0");
+  if ((epilogue == kEpiF32 && (n < 256 || n % 256)) || (epilogue == kEpiSwiGLU && (n < 128 || n % 128)))
+    return fail(MOE_ERR_UNSUPPORTED, "the pair kernel needs n % 256 == 0 (epilogue 0) or n % 128 == 0 (epilogue 1)");
+  if (!aligned16(a) || !aligned16(b) || !aligned16(c) || !aligned16(scratch))
+    return fail(MOE_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+  const size_t need = moe_prefill_debug_gemm_pairs_scratch(m, n, epilogue);
+  if (scratch_bytes < need) return fail(MOE_ERR_WORKSPACE, "scratch needs %zu bytes", need);
+  int device = 0, num_sms = 0;
+  moe_status st = check_device(&device, &num_sms);
+  if (st != MOE_OK) return st;
+  if (pair_cluster_slots() <= 0) return fail(MOE_ERR_UNSUPPORTED, "no room for a cluster of two CTAs");
+  const int width = pair_tile_width(m), mt = pair_tile_count(m);
+  const int nblocks = epilogue == kEpiF32 ? n / 256 : n / 128;
+  const int ntiles = mt * nblocks;
+  std::vector<int4> host(static_cast<size_t>(ntiles) + 1);
+  host[0] = make_int4(ntiles, 0, 0, 0);
+  for (int wb = 0; wb < nblocks; ++wb)
+    for (int i = 0; i < mt; ++i)
+      host[1 + static_cast<size_t>(wb) * mt + i] =
+          make_int4(wb << 16, i * width, std::min(width, m - i * width), i * width);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  st = cuda_status(cudaMemcpyAsync(scratch, host.data(), host.size() * sizeof(int4), cudaMemcpyHostToDevice, cs),
+                   "tile list copy");
+  if (st != MOE_OK) return st;
+  PairParams prm;
+  memset(&prm, 0, sizeof prm);
+  if (epilogue == kEpiF32)
+    st = encode_bf16_rows_kb(&prm.tmW[0], b, n, k_dim, kPairDownBoxRows, kPairKB);
+  else
+    st = encode_bf16_halves_kb(&prm.tmW[0], b, 1, n, k_dim, kPairWBoxRows, kPairKB);
+  if (st == MOE_OK) st = encode_bf16_rows_kb(&prm.tmT[0], a, m, k_dim, kPairTBoxRows, kPairKB);
+  if (st == MOE_OK) st = encode_bf16_rows_kb(&prm.tmTs[0], a, m, k_dim, kPairTBoxRowsSmall, kPairKB);
+  if (st != MOE_OK) return st;
+  prm.tmW[1] = prm.tmW[0];
+  prm.tmT[1] = prm.tmT[0];
+  prm.tmTs[1] = prm.tmTs[0];
+  PairClass cl{};
+  cl.kblocks = k_dim / kBlockK;
+  cl.w_up_offset = n;
+  cl.out = c;
+  cl.out_ld = n;
+  prm.cls[0] = prm.cls[1] = cl;
+  prm.tiles = reinterpret_cast<const int4*>(static_cast<char*>(scratch) + 16);
+  prm.num_tiles = static_cast<const int32_t*>(scratch);
+  prm.err = err_word;
+  prm.stall_flag = stall_flag;
+  prm.timeout_ns = timeout_ns ? timeout_ns : 2000000000ull;
+  return cuda_status(launch_grouped_pair(prm, epilogue, ntiles, cs), "debug pair GEMM launch");
+}
+
 }  // extern "C"

@@ -447,6 +447,23 @@ moe_status moe_prefill_debug_gemm(const void* a, const void* b, void* c, int32_t
                                   int32_t epilogue, int32_t* err_word, const int32_t* stall_flag,
                                   uint64_t timeout_ns, moe_stream_t stream);
 
+/*
+ * moe_prefill_debug_gemm_pairs — the same dense GEMM through the CTA-pair kernel the layer uses for its expert
+ * projections (b as the 256-row weight operand, the rows of a in token tiles of at most 256).
+ *   epilogue 0:  c = float [m][n] = a . b^T; n a multiple of 256.
+ *   epilogue 1:  c = bf16 [m][n] = bf16(silu(a . bg^T) * (a . bu^T)), b = gate rows then up rows; n a multiple of 128.
+ *   k_dim a multiple of 128, m >= 1.
+ *   scratch      device memory of at least moe_prefill_debug_gemm_pairs_scratch(m, n, epilogue) bytes (16-byte
+ *                aligned) for the tile list, which is copied there on `stream` from pageable host memory.
+ *   err_word, stall_flag, timeout_ns: as for moe_prefill_debug_gemm.
+ * MOE_ERR_UNSUPPORTED for other n or when no cluster of two CTAs fits; MOE_ERR_WORKSPACE for a short scratch.
+ * moe_prefill_debug_gemm_pairs_scratch returns 0 for invalid arguments.
+ */
+size_t moe_prefill_debug_gemm_pairs_scratch(int32_t m, int32_t n, int32_t epilogue);
+moe_status moe_prefill_debug_gemm_pairs(const void* a, const void* b, void* c, int32_t m, int32_t n, int32_t k_dim,
+                                        int32_t epilogue, void* scratch, size_t scratch_bytes, int32_t* err_word,
+                                        const int32_t* stall_flag, uint64_t timeout_ns, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -151,6 +151,28 @@ def gpu_swiglu(a, b):
     return out_bits(c.cpu())
 
 
+def gpu_swiglu_pairs(a, b):
+    """The same SwiGLU GEMM through the CTA-pair kernel (K padded with zeros to its multiple of 128)."""
+    from expert_major_chunked_gb300 import binding
+    m, K = a.shape
+    n = b.shape[0] // 2
+    Kp = (K + 127) // 128 * 128
+    ap = torch.zeros((m, Kp), dtype=torch.bfloat16)
+    bp = torch.zeros((2 * n, Kp), dtype=torch.bfloat16)
+    ap[:, :K] = a
+    bp[:, :K] = b
+    da, db = ap.cuda(), bp.cuda()
+    c = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+    need = binding.moe_prefill_debug_gemm_pairs_scratch(m, n, 1)
+    scratch = torch.zeros(need // 4 + 4, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.moe_prefill_debug_gemm_pairs(da.data_ptr(), db.data_ptr(), c.data_ptr(), m, n, Kp, 1, scratch.data_ptr(),
+                                         scratch.numel() * 4, err.data_ptr())
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return out_bits(c.cpu())
+
+
 def check_swiglu_bits(gpu_bits, a, b, orc):
     """The SwiGLU epilogue's bf16 h equals the oracle's h (one expert FFN, h = bf16(silu(g) * u)) bit for bit."""
     m, K = a.shape

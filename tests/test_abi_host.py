@@ -197,3 +197,25 @@ def test_binding_signatures_match_the_header():
     assert set(sigs) == set(counts), sorted(set(sigs) ^ set(counts))
     for name, (argtypes, _) in sigs.items():
         assert len(argtypes) == counts[name], (name, len(argtypes), counts[name])
+
+
+def test_debug_gemm_pairs_scratch_and_argument_checks(L):
+    """The pair kernel's diagnostic entry: scratch sizes, and arguments rejected before any device use (the
+    pointers below are never dereferenced)."""
+    from expert_major_chunked_gb300 import binding as b
+    # 313 token rows: two token tiles (160 + 153); n = 512: two F32 weight blocks of 256, four SwiGLU blocks of 128
+    assert b.moe_prefill_debug_gemm_pairs_scratch(313, 512, 0) == 16 * (2 * 2 + 1)
+    assert b.moe_prefill_debug_gemm_pairs_scratch(313, 512, 1) == 16 * (2 * 4 + 1)
+    assert b.moe_prefill_debug_gemm_pairs_scratch(257, 256, 0) == 16 * (2 + 1)
+    assert b.moe_prefill_debug_gemm_pairs_scratch(256, 256, 0) == 16 * (1 + 1)
+    assert b.moe_prefill_debug_gemm_pairs_scratch(0, 512, 0) == 0
+    assert b.moe_prefill_debug_gemm_pairs_scratch(1, 256, 2) == 0
+    p = ctypes.c_void_p(1 << 20)
+    f = L.moe_prefill_debug_gemm_pairs
+    assert f(None, p, p, 1, 256, 128, 0, p, 64, p, None, 0, None) == -1      # NULL a
+    assert f(p, p, p, 1, 256, 64, 0, p, 64, p, None, 0, None) == -1          # k_dim % 128
+    assert f(p, p, p, 1, 128, 128, 0, p, 64, p, None, 0, None) == -2         # F32 needs n % 256
+    assert f(p, p, p, 1, 192, 128, 1, p, 64, p, None, 0, None) == -2         # SwiGLU needs n % 128
+    assert f(p, p, p, 1, 256, 128, 3, p, 64, p, None, 0, None) == -1         # unknown epilogue
+    assert f(p, p, p, 300, 512, 128, 0, p, 16, p, None, 0, None) == -3       # scratch too small
+    assert b"scratch" in L.moe_prefill_last_error()

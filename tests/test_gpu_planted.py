@@ -44,6 +44,10 @@ def gpu():
         res[key] = (args, pc.gpu_combine(*args))
     a, b = pc.swiglu_midpoint_inputs()
     res["swiglu_mid"] = ((a, b), pc.gpu_swiglu(a, b))
+    res["swiglu_mid_pairs"] = ((a, b), pc.gpu_swiglu_pairs(a, b))
+    # dimensions where the gate/up projection runs on CTA pairs (the default for them)
+    wide = _small_inputs(2, H=256, I=128, Is=128)
+    res["layer_pairs"] = (wide, GpuLayer(wide, K_SMALL, max_chunk=CHUNK).run(CHUNK))
     return res
 
 
@@ -55,6 +59,8 @@ GATES = {
     "combine_bits": lambda g, o: pc.check_combine_bits(g["combine"][1], *g["combine"][0], o),
     "combine_ties": lambda g, o: pc.check_combine_bits(g["combine_mid"][1], *g["combine_mid"][0], o),
     "swiglu_ties": lambda g, o: pc.check_swiglu_bits(g["swiglu_mid"][1], *g["swiglu_mid"][0], o),
+    "swiglu_ties_pairs": lambda g, o: pc.check_swiglu_bits(g["swiglu_mid_pairs"][1], *g["swiglu_mid_pairs"][0], o),
+    "layer_output_pairs": lambda g, o: pc.check_output(g["layer_pairs"][1], g["layer_pairs"][0], K_SMALL, o),
 }
 
 # planted mistake -> the gates that must go red on it
@@ -63,12 +69,12 @@ RED = {
     "shared_added_first": ["combine_bits"],
     "tie_to_higher_id": ["routing_ids_planted_ties"],
     "scan_base_off_by_one": ["permutation"],
-    "round_half_away": ["combine_ties", "swiglu_ties", "combine_bits"],
-    "h_not_rounded": ["layer_output"],
-    "gate_up_swapped": ["layer_output"],
-    "no_renormalise": ["routing_weights", "layer_output"],
-    "shared_dropped": ["layer_output"],
-    "silu_sign_flipped": ["layer_output"],
+    "round_half_away": ["combine_ties", "swiglu_ties", "swiglu_ties_pairs", "combine_bits"],
+    "h_not_rounded": ["layer_output", "layer_output_pairs"],
+    "gate_up_swapped": ["layer_output", "layer_output_pairs"],
+    "no_renormalise": ["routing_weights", "layer_output", "layer_output_pairs"],
+    "shared_dropped": ["layer_output", "layer_output_pairs"],
+    "silu_sign_flipped": ["layer_output", "layer_output_pairs"],
 }
 
 
