@@ -234,7 +234,9 @@ struct PermuteParams {
   uint32_t* masks;            // [nblk][E]
   int32_t* counts;            // [nblk][E]
   int32_t* block_band;        // [nblk]
-  int32_t* base;              // [nblk][E]
+  int32_t* base;              // [nblk][E]: rows of expert e in the blocks before block b (relative to the expert's
+                              // first row, which is offsets[e])
+  int32_t* totals;            // [E]: rows of expert e in the chunk
   int32_t* offsets;           // [E+1] (workspace)
   int32_t* offsets_out;       // user [E+1] for this chunk, or nullptr
   int32_t* token_row;         // [n][k]
@@ -252,6 +254,7 @@ struct PermuteParams {
   int32_t pair_gu, pair_dn;   // 1: that GEMM's tile list is for grouped_pair_kernel (its nt_* count weight blocks)
 };
 cudaError_t launch_count(const PermuteParams& p, cudaStream_t stream);
+cudaError_t launch_block_bases(const PermuteParams& p, cudaStream_t stream);
 cudaError_t launch_scan_tiles(const PermuteParams& p, cudaStream_t stream);
 cudaError_t launch_permute(const PermuteParams& p, cudaStream_t stream);
 

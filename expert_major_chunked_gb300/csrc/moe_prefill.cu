@@ -248,8 +248,8 @@ moe_status check_device(int* device, int* num_sms) {
 
 // ------------------------------------------------------------------ workspace layout
 struct Layout {
-  size_t hdr, wnorm, logits, topk_id, topk_w, band, band_info, masks, counts, base, block_band, offsets, h, hs, y, s,
-      total;
+  size_t hdr, wnorm, logits, topk_id, topk_w, band, band_info, masks, counts, base, totals, block_band, offsets, h, hs,
+      y, s, total;
   // two sets (chunk parity): the member lists of chunk c+1 are built while chunk c's GEMMs still read chunk c's
   size_t token_row[2], num_tiles[2], tiles_gu[2], tiles_down[2], xp[2], tile_base[2];
   size_t ring_gu, ring_down;  // offloaded experts: the HBM ring of expert slots, then the hot set's slots
@@ -321,6 +321,7 @@ Layout make_layout(const Shape& s) {
   L.masks = take(nblk * E * 4);
   L.counts = take(nblk * E * 4);
   L.base = take(nblk * E * 4);
+  L.totals = take(E * 4);
   L.block_band = take(nblk * 4);
   L.offsets = take((E + 1) * 4);
   for (int b = 0; b < 2; ++b) {
@@ -1021,6 +1022,7 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       q.counts = reinterpret_cast<int32_t*>(ws + L.counts);
       q.block_band = reinterpret_cast<int32_t*>(ws + L.block_band);
       q.base = reinterpret_cast<int32_t*>(ws + L.base);
+      q.totals = reinterpret_cast<int32_t*>(ws + L.totals);
       q.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
       q.offsets_out = expert_offsets ? expert_offsets + cidx * (s.E + 1) : nullptr;
       q.token_row = reinterpret_cast<int32_t*>(ws + L.token_row[par]);
@@ -1046,8 +1048,9 @@ moe_status run_impl(moe_plan_t p, const void* x, int64_t T, int32_t chunk, void*
       }
       if (r2 != MOE_OK) return r2;
       {
-        LaunchScope ls(p, MOE_KERNEL_SCAN, side);
-        r2 = cuda_status(launch_scan_tiles(q, side), "scan launch");
+        LaunchScope ls(p, MOE_KERNEL_SCAN, side, 2);
+        r2 = cuda_status(launch_block_bases(q, side), "block bases launch");
+        if (r2 == MOE_OK) r2 = cuda_status(launch_scan_tiles(q, side), "scan launch");
       }
       if (r2 != MOE_OK) return r2;
       {

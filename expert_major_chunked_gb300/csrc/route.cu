@@ -559,36 +559,41 @@ __device__ int block_exclusive_scan(int v, int* total, int* smem32) {
   return r;
 }
 
-// Column e of counts[nblk][E] (coalesced across the warp), 16 blocks per batch so that 16 loads are in flight.
-__device__ __forceinline__ int column_total(const int32_t* counts, int e, int E, int nblk) {
-  int total = 0;
-  for (int b0 = 0; b0 < nblk; b0 += 16) {
-    int c[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) total += c[j];
+// Per expert, its total rows in the chunk and, for every 32-token block, the rows of that expert in the blocks before
+// it (the block's base relative to the expert's first row). ceil(E/32) CTAs of 1024 threads: lane l handles expert
+// 32 x CTA + l (consecutive experts: the counts rows load coalesced), warp w the w-th of 32 contiguous ranges of
+// blocks; the 32 range sums of an expert meet in shared memory. Each thread walks at most ceil(nblk / 32) blocks.
+constexpr int kBaseWarps = 32;
+__global__ void __launch_bounds__(kBaseWarps * 32) block_bases_kernel(PermuteParams p) {
+  __shared__ int part[kBaseWarps][33];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int e = blockIdx.x * 32 + lane;
+  const int E = p.E, nblk = p.nblk;
+  const int per = (nblk + kBaseWarps - 1) / kBaseWarps;
+  const int b0 = min(nblk, warp * per), b1 = min(nblk, b0 + per);
+  int sum = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) sum += p.counts[static_cast<int64_t>(b) * E + e];
   }
-  return total;
-}
-
-// Row base of every (block, expert e): off + the counts of the earlier blocks.
-__device__ __forceinline__ void column_bases(const int32_t* counts, int32_t* base, int e, int E, int nblk, int off) {
-  int run = off;
-  for (int b0 = 0; b0 < nblk; b0 += 16) {
-    int c[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) c[j] = (b0 + j < nblk) ? counts[static_cast<int64_t>(b0 + j) * E + e] : 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (b0 + j < nblk) base[static_cast<int64_t>(b0 + j) * E + e] = run;
-      run += c[j];
+  part[warp][lane] = sum;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += part[w][lane];
+  if (e < E) {
+    if (warp == kBaseWarps - 1) p.totals[e] = before + sum;
+    int run = before;
+    for (int b = b0; b < b1; ++b) {
+      const int64_t be = static_cast<int64_t>(b) * E + e;
+      const int c = p.counts[be];
+      p.base[be] = run;
+      run += c;
     }
   }
 }
 
-// One CTA of 512 threads; thread i owns expert i and, when E > 512, expert i + 512: per-expert totals, expert offsets,
-// per-(block, expert) row bases, and the tile lists of the gate/up and down GEMMs (expert-major: expert, then N tile,
+// One CTA of 512 threads; thread i owns expert i and, when E > 512, expert i + 512: expert offsets (an exclusive scan
+// of the totals block_bases_kernel left), and the tile lists of the gate/up and down GEMMs (expert-major: expert, then N tile,
 // then M tile; or, for grouped_pair_kernel, expert, then weight block, then token tile of pair_tile_width rows). 512
 // threads of at most 64 registers leave room on an SM for a GEMM CTA beside it: this kernel runs
 // while the previous chunk's GEMMs hold every SM.
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermutePara
   for (int h = 0; h < 2; ++h) {
     if (h >= halves) break;
     const int e = static_cast<int>(threadIdx.x) + h * kScanThreads;
-    if (e < E) tot[h] = column_total(p.counts, e, E, nblk);
+    if (e < E) tot[h] = p.totals[e];
     // exclusive scans over the experts of this half, after those of the half before
     int sum = 0;
     off[h] = R + block_exclusive_scan(tot[h], &sum, sm);
@@ -640,7 +645,6 @@ __global__ void __launch_bounds__(kScanThreads, 2) scan_tiles_kernel(PermutePara
     if (h >= halves || e >= E) continue;
     p.offsets[e] = off[h];
     if (p.offsets_out) p.offsets_out[e] = off[h];
-    column_bases(p.counts, p.base, e, E, nblk, off[h]);
     p.tile_base[e] = gu_base[h];
     p.tile_base[E + 1 + e] = dn_base[h];
     if (!fits) continue;
@@ -706,7 +710,7 @@ __global__ void __launch_bounds__(kPermuteWarps * 32) permute_kernel(PermutePara
       e = 0;
     }
     const int64_t be = static_cast<int64_t>(b) * E + e;
-    int row = p.base[be] + __popc(p.masks[be] & ((1u << i) - 1u));
+    int row = p.offsets[e] + p.base[be] + __popc(p.masks[be] & ((1u << i) - 1u));
     if (row < 0 || row >= p.n * k) {
       atomicCAS(&p.hdr->err, 0, dev_error_code(kDevErrBounds, kSiteRouting, t));
       row = 0;
@@ -755,6 +759,11 @@ cudaError_t launch_topk(const RouteParams& p, cudaStream_t stream) {
 cudaError_t launch_count(const PermuteParams& p, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(kCountWarps) * p.E * sizeof(uint32_t);
   count_kernel<<<(p.nblk + kCountWarps - 1) / kCountWarps, kCountWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_bases(const PermuteParams& p, cudaStream_t stream) {
+  block_bases_kernel<<<(p.E + 31) / 32, kBaseWarps * 32, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
