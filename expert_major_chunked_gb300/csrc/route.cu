@@ -422,77 +422,85 @@ __global__ void __launch_bounds__(256) band_kernel(RouteParams p) {
   __shared__ BandScratch band_scratch[8];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int E = p.E, k = p.k, H = p.H;
-  for (int t = blockIdx.x * 8 + warp; t < p.n; t += gridDim.x * 8) {
-    if (p.band_flag[t] != 2) continue;
-    float v[EPL];
-    load_logits(p.logits + static_cast<int64_t>(t) * E, E, lane, v);
-    const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
-    const BandInfo bi = p.band_info[t];
-    BandScratch& B = band_scratch[warp];
-    uint32_t sure, cand;
-    int cidx[EPL];
-    int need;
-    const int ncand = band_candidates(v, E, k, lane, bi.tau, bi.vk, bi.vk1, B, &sure, &cand, cidx, &need);
-    uint32_t chosen = 0;
-    if (ncand <= kMaxCand) {
-      // level 0: float sums of the exact products (also S for every level's bound)
-      band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);
-      int certified = 0;
-      if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-24));
-      certified = __shfl_sync(0xffffffffu, certified, 0);
-      int level = 0;
-      if (!certified) {
-        // level 1: double sums
-        level = 1;
-        band_values<double>(B, ncand, xrow, p.w_router, H, lane, false);
-        if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-53));
+  // the warp's tokens t0 + i * stride; their flags are read 32 at a time (one load per lane, then a ballot) instead
+  // of one dependent load per token
+  const int stride = gridDim.x * 8;
+  for (int t0 = blockIdx.x * 8 + warp; t0 < p.n; t0 += 32 * stride) {
+    const int tl = t0 + lane * stride;
+    uint32_t todo = __ballot_sync(0xffffffffu, tl < p.n && p.band_flag[tl] == 2);
+    while (todo != 0u) {
+      const int t = t0 + (__ffs(todo) - 1) * stride;
+      todo &= todo - 1u;
+      float v[EPL];
+      load_logits(p.logits + static_cast<int64_t>(t) * E, E, lane, v);
+      const uint16_t* xrow = p.x + static_cast<int64_t>(t) * H;
+      const BandInfo bi = p.band_info[t];
+      BandScratch& B = band_scratch[warp];
+      uint32_t sure, cand;
+      int cidx[EPL];
+      int need;
+      const int ncand = band_candidates(v, E, k, lane, bi.tau, bi.vk, bi.vk1, B, &sure, &cand, cidx, &need);
+      uint32_t chosen = 0;
+      if (ncand <= kMaxCand) {
+        // level 0: float sums of the exact products (also S for every level's bound)
+        band_values<float>(B, ncand, xrow, p.w_router, H, lane, true);
+        int certified = 0;
+        if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-24));
         certified = __shfl_sync(0xffffffffu, certified, 0);
-      }
-      if (!certified) {
-        level = 2;
-        for (int c = lane; c < ncand; c += 32)
-          B.val[c] = exact_logit(xrow, p.w_router + static_cast<int64_t>(B.id[c]) * H, H);
+        int level = 0;
+        if (!certified) {
+          // level 1: double sums
+          level = 1;
+          band_values<double>(B, ncand, xrow, p.w_router, H, lane, false);
+          if (lane == 0) certified = band_select(B, ncand, need, band_bound(H, 0x1p-53));
+          certified = __shfl_sync(0xffffffffu, certified, 0);
+        }
+        if (!certified) {
+          level = 2;
+          for (int c = lane; c < ncand; c += 32)
+            B.val[c] = exact_logit(xrow, p.w_router + static_cast<int64_t>(B.id[c]) * H, H);
+          __syncwarp();
+          if (lane == 0) band_select(B, ncand, need, -1.0);
+        }
         __syncwarp();
-        if (lane == 0) band_select(B, ncand, need, -1.0);
-      }
-      __syncwarp();
-      if (lane == 0) atomicAdd(&p.hdr->band_levels[level], 1);  // diagnostic counter only
-      chosen = chosen_mask(B, cand, cidx);
-    } else {
-      // more candidates than the scratch list holds (e.g. all-zero tokens): sequential float64 sums per lane
-      if (lane == 0) atomicAdd(&p.hdr->band_levels[3], 1);  // diagnostic counter only
-      double d[EPL];
-#pragma unroll
-      for (int j = 0; j < EPL; ++j) {
-        d[j] = 0.0;
-        if ((cand >> j) & 1u) d[j] = exact_logit(xrow, p.w_router + static_cast<int64_t>(j * 32 + lane) * H, H);
-      }
-      for (int r = 0; r < need; ++r) {
-        double bv = -DBL_MAX;
-        int bid = INT_MAX;
-#pragma unroll
+        if (lane == 0) atomicAdd(&p.hdr->band_levels[level], 1);  // diagnostic counter only
+        chosen = chosen_mask(B, cand, cidx);
+      } else {
+        // more candidates than the scratch list holds (e.g. all-zero tokens): sequential float64 sums per lane
+        if (lane == 0) atomicAdd(&p.hdr->band_levels[3], 1);  // diagnostic counter only
+        double d[EPL];
+  #pragma unroll
         for (int j = 0; j < EPL; ++j) {
-          if (((cand & ~chosen) >> j) & 1u) {
-            if (bid == INT_MAX || d[j] > bv) {
-              bv = d[j];
-              bid = j * 32 + lane;
+          d[j] = 0.0;
+          if ((cand >> j) & 1u) d[j] = exact_logit(xrow, p.w_router + static_cast<int64_t>(j * 32 + lane) * H, H);
+        }
+        for (int r = 0; r < need; ++r) {
+          double bv = -DBL_MAX;
+          int bid = INT_MAX;
+  #pragma unroll
+          for (int j = 0; j < EPL; ++j) {
+            if (((cand & ~chosen) >> j) & 1u) {
+              if (bid == INT_MAX || d[j] > bv) {
+                bv = d[j];
+                bid = j * 32 + lane;
+              }
             }
           }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-          if (ov > bv || (ov == bv && oid < bid)) {
-            bv = ov;
-            bid = oid;
+  #pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const double ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
+            if (ov > bv || (ov == bv && oid < bid)) {
+              bv = ov;
+              bid = oid;
+            }
           }
+          if (bid != INT_MAX && (bid & 31) == lane) chosen |= 1u << (bid >> 5);
         }
-        if (bid != INT_MAX && (bid & 31) == lane) chosen |= 1u << (bid >> 5);
       }
+      write_selection(p, t, lane, sure | chosen, v);
+      __syncwarp();
     }
-    write_selection(p, t, lane, sure | chosen, v);
-    __syncwarp();
   }
 }
 
@@ -592,11 +600,11 @@ __global__ void __launch_bounds__(kBaseWarps * 32) block_bases_kernel(PermutePar
   }
 }
 
-// One CTA of 512 threads; thread i owns expert i and, when E > 512, expert i + 512: expert offsets (an exclusive scan
-// of the totals block_bases_kernel left), and the tile lists of the gate/up and down GEMMs (expert-major: expert, then N tile,
-// then M tile; or, for grouped_pair_kernel, expert, then weight block, then token tile of pair_tile_width rows). 512
-// threads of at most 64 registers leave room on an SM for a GEMM CTA beside it: this kernel runs
-// while the previous chunk's GEMMs hold every SM.
+// One CTA of 512 threads; thread i owns expert i and, when E > 512, expert i + 512: expert offsets (an exclusive
+// scan of the totals block_bases_kernel left), and the tile lists of the gate/up and down GEMMs (expert-major:
+// expert, then N tile, then M tile; or, for grouped_pair_kernel, expert, then weight block, then token tile of
+// pair_tile_width rows). 512 threads of at most 64 registers leave room on an SM for a GEMM CTA beside it: this
+// kernel runs while the previous chunk's GEMMs hold every SM.
 constexpr int kScanThreads = 512;
 
 // Row tiles of an expert with `rows` member rows: 128-row tiles (grouped_gemm_kernel) or pair_tile_width-row tiles
