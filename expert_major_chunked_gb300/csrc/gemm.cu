@@ -8,10 +8,13 @@
 // so every output element is computed with the same accumulation order whatever the tile's row position or the
 // number of members of its expert. That makes each row independent of the chunk size.
 //
-// bf16 weights, grouped_gemm_kernel (192 threads): warp 0 lane 0 issues TMA loads; warp 1 owns the TMEM allocation
-// and lane 0 issues the UMMAs; warps 2..5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..+31) and
-// store the outputs. Two TMEM accumulators of 256 columns let the epilogue of one tile overlap the main loop of the
-// next.
+// bf16 weights, grouped_gemm_kernel (192 threads): warp 0 lane 0 issues TMA loads, two per stage (the tile's rows in
+// one 128-row box, and its weight rows in one box: for gate/up a 3-D box of the tile's gate rows then its up rows);
+// warp 1 owns the TMEM allocation and lane 0 issues the UMMAs; warps 2..5 read the accumulator back (warp w reads
+// TMEM lanes 32*(w%4)..+31) and store the outputs. Two TMEM accumulators of 256 columns let the epilogue of one tile
+// overlap the main loop of the next. The layer runs its gate/up projection on CTA pairs by default
+// (grouped_pair_kernel, gemm_pair.cu), with the same bytes; this kernel serves the down projection, the router GEMM,
+// the shared expert of block-scaled plans, and layers whose dimensions the pair kernel does not take.
 //
 // Block-scaled FP8 weights (MXFP8: E4M3 codes, one E8M0 power-of-two scale per 32 weights along K),
 // grouped_gemm_q_kernel (480 threads): the weight codes stream through their own ring of 5 stages, which carries

@@ -4,10 +4,14 @@
 // exact deep prefill", introduction) on the same tile lists' experts and rows, with the operands the other way
 // round: M = 256 rows of an expert's weights (each CTA holds 128 of them in shared memory, and their accumulators
 // in its 128 TMEM lanes), N = the tile's tokens rounded up to 32 (at most 256; each CTA loads half of the token
-// rows, and the tensor cores of the pair read both halves). Per SM and 64-wide K step that is 16 KB of weights and
+// rows, and the tensor cores of the pair read both halves). Per SM and 64-wide K block that is 16 KB of weights and
 // N/2 x 128 B of tokens for 128 x N x 64 multiply-adds, against 48 KB for 128 x 256 x 64 in the single-CTA kernel;
-// and an expert's rows are covered in steps of 32 tokens instead of 128 rows. The K loop is the same (64 per stage,
-// 16 per instruction, in order), so each output element is accumulated in the same order as there.
+// and an expert's rows are covered in steps of 32 tokens instead of 128 rows. The K order is the same (64-wide K
+// blocks, 16 per instruction, in order), so each output element is accumulated in the same order as there.
+//
+// A stage is two K blocks. A stage costs about the same per TMA operation whatever the box size, so each CTA loads a
+// stage with two: its weight rows of both K blocks in one box, its token rows of both K blocks in another (the maps
+// have the K block as their outermost dimension).
 //
 // Roles (320 threads per CTA, both CTAs): warp 0 lane 0 loads the CTA's weight and token boxes; their completion is
 // counted on the even CTA's full barrier. Warp 1 of the even CTA issues the UMMAs and commits each stage to the
