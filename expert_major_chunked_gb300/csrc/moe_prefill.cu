@@ -1,5 +1,6 @@
 // Host side of the C ABI declared in include/moe_prefill.h: validation, workspace layout, TMA descriptors and the
-// chunk loop. All arithmetic runs in the kernels of gemm.cu, route.cu and combine.cu.
+// chunk loop. All arithmetic runs in the kernels of gemm.cu, gemm_pair.cu, route.cu, combine.cu, combine_f64.cu and
+// ring.cu.
 #include "../../include/moe_prefill.h"
 #include "internal.h"
 
