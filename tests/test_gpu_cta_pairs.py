@@ -114,3 +114,21 @@ def test_pairs_refused_where_dimensions_do_not_allow():
     with pytest.raises(binding.MoeError):
         g.layer.cta_pairs = 4
     g.layer.cta_pairs = 0
+
+
+@pytest.mark.parametrize("name,tokens,chunks", [("e512_t16022", 4096, (2048, 4096)),
+                                                ("e128_t3001", 3001, (256, 3001))])
+def test_pairs_equal_single_cta_on_workload_shapes(name, tokens, chunks):
+    """The two GEMM kernels on the workloads' own dimensions (H = 2048; E = 512, I = 512, k = 10 or E = 128,
+    I = 768, I_s = 2048, k = 8), at a chunk size the workload uses and in one pass: the same output bytes for every
+    choice of kernel per projection."""
+    from layer_helpers import cpu_inputs
+    wl, inp = cpu_inputs(name, tokens=tokens)
+    g = GpuLayer(inp, wl.top_k, max_chunk=max(chunks))
+    for chunk in chunks:
+        outs = {}
+        for mask in MASKS:
+            g.layer.cta_pairs = mask
+            outs[mask] = out_bits(g.run(chunk)["out"])
+        for mask in MASKS[1:]:
+            np.testing.assert_array_equal(outs[mask], outs[0], err_msg=f"{name} chunk {chunk} mask {mask}")
